@@ -1,0 +1,711 @@
+// dv_abi.cu -- C entry points of libdv: argument checks, workspace layout and
+// the launch sequence of the sparse layer decode.  See include/dv.h.
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "dv_internal.h"
+
+using namespace dv;
+
+namespace {
+
+constexpr int kLayerLaunches = 7;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t esize(int dtype) { return dtype == DV_F16 ? 2 : 4; }
+int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+int batch_pad(int B)
+{
+    if (B <= 8) {
+        int p = 1;
+        while (p < B)
+            p <<= 1;
+        return p;
+    }
+    return (int)align_up((size_t)B, 8);
+}
+
+dv_status check_desc(const dv_layer_desc *D)
+{
+    if (!D)
+        return DV_ERR_INVALID_ARG;
+    if (D->d_model <= 0 || D->n_heads <= 0 || D->head_dim <= 0 || D->d_ffn <= 0 ||
+        D->pred_rank <= 0 || D->kv_cap <= 0)
+        return DV_ERR_INVALID_ARG;
+    if (D->dtype != DV_F32 && D->dtype != DV_F16)
+        return DV_ERR_INVALID_ARG;
+    if (D->norm != DV_LAYERNORM && D->norm != DV_RMSNORM)
+        return DV_ERR_INVALID_ARG;
+    if (!(D->ln_eps > 0.f) || !std::isfinite(D->ln_eps))
+        return DV_ERR_INVALID_ARG;
+    const int epc = (int)(16 / esize(D->dtype));
+    if (D->d_model % epc || D->pred_rank % epc)
+        return DV_ERR_UNSUPPORTED;
+    const int dh = D->head_dim;
+    const size_t hb = (size_t)dh * esize(D->dtype);
+    if ((dh & (dh - 1)) || hb < 16 || hb > 512)
+        return DV_ERR_UNSUPPORTED;
+    // activations of one row must fit the row-dot kernel's shared memory
+    if ((size_t)D->d_model * 4 > kSmemCap || (size_t)D->pred_rank * 4 > kSmemCap)
+        return DV_ERR_UNSUPPORTED;
+    if ((long long)3 * D->n_heads * dh > (1 << 24) || D->d_ffn > (1 << 24) ||
+        (long long)D->kv_cap * dh > (1LL << 31) / 4)
+        return DV_ERR_UNSUPPORTED;
+    return DV_OK;
+}
+
+dv_status check_weights(const dv_layer_weights *w)
+{
+    if (!w)
+        return DV_ERR_INVALID_ARG;
+    const void *p[] = {w->ln1_g, w->ln1_b, w->w_qkv, w->b_qkv, w->w_oT, w->b_o, w->ln2_g,
+                       w->ln2_b, w->w1, w->b1, w->w2T, w->b2, w->pred_h, w->pred_a, w->pred_b};
+    for (const void *q : p)
+        if (!q || !aligned16(q))
+            return DV_ERR_INVALID_ARG;
+    return DV_OK;
+}
+
+bool ptr_ok(const void *p) { return p && aligned16(p); }
+
+dv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DV_OK : DV_ERR_CUDA; }
+
+struct Launch {
+    cudaStream_t st;
+    int nsm;
+    void *const *events;  // optional trace events
+    int n_events;
+    int next_event;
+
+    dv_status mark()
+    {
+        if (!events)
+            return DV_OK;
+        if (next_event >= n_events)
+            return DV_ERR_INVALID_ARG;
+        cudaEvent_t ev = static_cast<cudaEvent_t>(events[next_event++]);
+        return cuda_status(cudaEventRecord(ev, st));
+    }
+};
+
+dv_status make_launch(void *stream, void *const *events, int n_events, Launch *L)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return DV_ERR_CUDA;
+    int nsm = 0;
+    if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        nsm <= 0)
+        return DV_ERR_CUDA;
+    L->st = static_cast<cudaStream_t>(stream);
+    L->nsm = nsm;
+    L->events = events;
+    L->n_events = n_events;
+    L->next_event = 0;
+    return DV_OK;
+}
+
+int choose_nseg(int rows, int K, int epc, int total_warps)
+{
+    const int chunks = K / epc;
+    int nseg = ceil_div(4LL * total_warps, rows > 0 ? rows : 1);
+    if (nseg > kMaxSeg)
+        nseg = kMaxSeg;
+    while (nseg > 1 && (chunks % nseg != 0 || chunks / nseg < 64))
+        --nseg;
+    return nseg < 1 ? 1 : nseg;
+}
+
+int choose_groups(int rows, int d, int epc, int total_warps)
+{
+    const int S = ceil_div(d, 32 * epc);
+    int G = ceil_div(total_warps, S);
+    const int gmax_rows = ceil_div(rows, 8);
+    if (G > gmax_rows)
+        G = gmax_rows;
+    if (G > kMaxColGroups)
+        G = kMaxColGroups;
+    return G < 1 ? 1 : G;
+}
+
+template <typename P>
+P *at(void *ws, size_t off) { return reinterpret_cast<P *>(static_cast<char *>(ws) + off); }
+
+// ---------------------------------------------------------------------------
+// The three blocks of the decode step.
+
+dv_status run_predict(const dv_layer_desc &D, const dv_layer_weights &w, const float *xp, int B,
+                      int kh, int kn, const dv_selection &sel, float *sh_user, float *sn_user,
+                      void *ws, const WsLayout &L, Launch &lc)
+{
+    const int d = D.d_model, H = D.n_heads, N = D.d_ffn, r = D.pred_rank;
+    const int epc = (int)(16 / esize(D.dtype));
+    const int total_warps = lc.nsm * kWarpsPerBlock;
+    int *ctl = at<int>(ws, L.ctl);
+
+    RowArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.K = d;
+    a.max_rows = H + r;
+    a.nseg = choose_nseg(a.max_rows, d, epc, total_warps);
+    a.seglen = d / a.nseg;
+    a.B = B;
+    a.x = xp;
+    a.x_ld = d;
+    a.w0 = w.pred_h;
+    a.w1 = w.pred_a;
+    a.split_rows = H;
+    a.out0 = at<float>(ws, L.s_h);
+    a.out1 = at<float>(ws, L.u);
+    a.user_scores = sh_user;
+    a.part = at<float>(ws, L.part_pred1);
+    a.rowcnt = at<int>(ws, L.cnt_pred1);
+    a.topk_n = H;
+    a.topk_k = kh;
+    a.idx_out = sel.idx_h;
+    a.u_out = sel.u_h;
+    a.n_u_out = sel.n_u_h;
+    a.done = ctl + 1;
+    a.status = ctl;
+    int nb = rowdot_nb(B, d, RK_PRED1);
+    dim3 grid(lc.nsm, ceil_div(B, nb));
+    dv_status s = lc.mark();
+    if (s)
+        return s;
+    if (launch_rowdot(RK_PRED1, D.dtype, nb, a, grid, rowdot_smem(RK_PRED1, nb, d, H), lc.st,
+                      false) != cudaSuccess)
+        return DV_ERR_CUDA;
+
+    RowArgs b2;
+    std::memset(&b2, 0, sizeof(b2));
+    b2.K = r;
+    b2.max_rows = N;
+    b2.nseg = 1;
+    b2.seglen = r;
+    b2.B = B;
+    b2.x = at<float>(ws, L.u);
+    b2.x_ld = r;
+    b2.w0 = w.pred_b;
+    b2.out0 = at<float>(ws, L.s_n);
+    b2.user_scores = sn_user;
+    b2.topk_n = N;
+    b2.topk_k = kn;
+    b2.hist = at<int>(ws, L.hist);
+    b2.idx_out = sel.idx_n;
+    b2.u_out = sel.u_n;
+    b2.n_u_out = sel.n_u_n;
+    b2.done = ctl + 2;
+    b2.status = ctl;
+    nb = rowdot_nb(B, r, RK_PRED2);
+    grid = dim3(lc.nsm, ceil_div(B, nb));
+    if ((s = lc.mark()))
+        return s;
+    if (launch_rowdot(RK_PRED2, D.dtype, nb, b2, grid, rowdot_smem(RK_PRED2, nb, r, N), lc.st,
+                      false) != cudaSuccess)
+        return DV_ERR_CUDA;
+    return DV_OK;
+}
+
+dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const float *x, int B,
+                   const int32_t *u_h, const int32_t *n_u_h, int max_u_h, void *kc, void *vc,
+                   int kv_len, float *h1, void *ws, const WsLayout &L, Launch &lc)
+{
+    const int d = D.d_model, H = D.n_heads, dh = D.head_dim;
+    const int epc = (int)(16 / esize(D.dtype));
+    const int total_warps = lc.nsm * kWarpsPerBlock;
+    int *ctl = at<int>(ws, L.ctl);
+
+    RowArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.K = d;
+    a.max_rows = 3 * max_u_h * dh;
+    a.nseg = choose_nseg(a.max_rows, d, epc, total_warps);
+    a.seglen = d / a.nseg;
+    a.B = B;
+    a.n_sel = n_u_h;
+    a.max_sel = max_u_h;
+    a.sel = u_h;
+    a.sel_range = H;
+    a.x = x;
+    a.x_ld = d;
+    a.norm_g = w.ln1_g;
+    a.norm_b = w.ln1_b;
+    a.norm_kind = D.norm;
+    a.eps = D.ln_eps;
+    a.w0 = w.w_qkv;
+    a.bias = w.b_qkv;
+    a.H = H;
+    a.dh = dh;
+    a.out0 = at<float>(ws, L.q);
+    a.kc = kc;
+    a.vc = vc;
+    a.kv_len = kv_len;
+    a.kv_cap = D.kv_cap;
+    a.q_scale = (float)(1.0 / std::sqrt((double)dh));
+    a.part = at<float>(ws, L.part_qkv);
+    a.rowcnt = at<int>(ws, L.cnt_qkv);
+    a.status = ctl;
+    int nb = rowdot_nb(B, d, RK_QKV);
+    dim3 grid(lc.nsm, ceil_div(B, nb));
+    dv_status s = lc.mark();
+    if (s)
+        return s;
+    if (launch_rowdot(RK_QKV, D.dtype, nb, a, grid, rowdot_smem(RK_QKV, nb, d, 0), lc.st,
+                      false) != cudaSuccess)
+        return DV_ERR_CUDA;
+
+    AttnArgs t;
+    std::memset(&t, 0, sizeof(t));
+    t.B = B;
+    t.H = H;
+    t.dh = dh;
+    t.kv_cap = D.kv_cap;
+    t.kv_len = kv_len;
+    t.n_sel = n_u_h;
+    t.max_sel = max_u_h;
+    t.sel = u_h;
+    t.q = at<float>(ws, L.q);
+    t.kc = kc;
+    t.vc = vc;
+    const int L1 = kv_len + 1;
+    const int want = ceil_div(2LL * total_warps, (long long)B * max_u_h);
+    int split_len = ceil_div(L1, want < 1 ? 1 : want);
+    if (split_len < kAttnMinSplit)
+        split_len = kAttnMinSplit;
+    t.split_len = split_len;
+    t.splits = ceil_div(L1, split_len);
+    if (t.splits > L.attn_splits_max)
+        return DV_ERR_WORKSPACE;
+    t.part = at<float>(ws, L.attn_part);
+    t.cnt = at<int>(ws, L.attn_cnt);
+    t.o = at<float>(ws, L.o);
+    t.status = ctl;
+    const int lpk = (int)((size_t)dh * esize(D.dtype) / 16);
+    if ((s = lc.mark()))
+        return s;
+    if (launch_attn(D.dtype, lpk, t, dim3(lc.nsm), lc.st, false) != cudaSuccess)
+        return DV_ERR_CUDA;
+
+    ColArgs c;
+    std::memset(&c, 0, sizeof(c));
+    c.d = d;
+    c.B = B;
+    c.n_sel = n_u_h;
+    c.max_sel = max_u_h;
+    c.sel = u_h;
+    c.sel_range = H;
+    c.dh = dh;
+    c.w = w.w_oT;
+    c.coef = at<float>(ws, L.o);
+    c.coef_ld = max_u_h * dh;
+    c.res = x;
+    c.bias = w.b_o;
+    c.out = h1;
+    c.G = choose_groups(max_u_h * dh, d, epc, total_warps);
+    c.part = at<float>(ws, L.cpart_o);
+    c.cnt = at<int>(ws, L.ccnt_o);
+    c.status = ctl;
+    nb = colacc_nb(B);
+    if ((s = lc.mark()))
+        return s;
+    if (launch_colacc(CK_OPROJ, D.dtype, nb, c, dim3(lc.nsm, ceil_div(B, nb)), lc.st, false) !=
+        cudaSuccess)
+        return DV_ERR_CUDA;
+    return DV_OK;
+}
+
+dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float *h1, int B,
+                  const int32_t *u_n, const int32_t *n_u_n, int max_u_n, float *y, void *ws,
+                  const WsLayout &L, Launch &lc)
+{
+    const int d = D.d_model, N = D.d_ffn;
+    const int epc = (int)(16 / esize(D.dtype));
+    const int total_warps = lc.nsm * kWarpsPerBlock;
+    int *ctl = at<int>(ws, L.ctl);
+
+    RowArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.K = d;
+    a.max_rows = max_u_n;
+    a.nseg = choose_nseg(a.max_rows, d, epc, total_warps);
+    a.seglen = d / a.nseg;
+    a.B = B;
+    a.n_sel = n_u_n;
+    a.max_sel = max_u_n;
+    a.sel = u_n;
+    a.sel_range = N;
+    a.x = h1;
+    a.x_ld = d;
+    a.norm_g = w.ln2_g;
+    a.norm_b = w.ln2_b;
+    a.norm_kind = D.norm;
+    a.eps = D.ln_eps;
+    a.w0 = w.w1;
+    a.bias = w.b1;
+    a.out0 = at<float>(ws, L.act);
+    a.part = at<float>(ws, L.part_fc1);
+    a.rowcnt = at<int>(ws, L.cnt_fc1);
+    a.status = ctl;
+    int nb = rowdot_nb(B, d, RK_FC1);
+    dv_status s = lc.mark();
+    if (s)
+        return s;
+    if (launch_rowdot(RK_FC1, D.dtype, nb, a, dim3(lc.nsm, ceil_div(B, nb)),
+                      rowdot_smem(RK_FC1, nb, d, 0), lc.st, false) != cudaSuccess)
+        return DV_ERR_CUDA;
+
+    ColArgs c;
+    std::memset(&c, 0, sizeof(c));
+    c.d = d;
+    c.B = B;
+    c.n_sel = n_u_n;
+    c.max_sel = max_u_n;
+    c.sel = u_n;
+    c.sel_range = N;
+    c.dh = 1;
+    c.w = w.w2T;
+    c.coef = at<float>(ws, L.act);
+    c.coef_ld = max_u_n;
+    c.res = h1;
+    c.bias = w.b2;
+    c.out = y;
+    c.G = choose_groups(max_u_n, d, epc, total_warps);
+    c.part = at<float>(ws, L.cpart_2);
+    c.cnt = at<int>(ws, L.ccnt_2);
+    c.status = ctl;
+    nb = colacc_nb(B);
+    if ((s = lc.mark()))
+        return s;
+    if (launch_colacc(CK_FC2, D.dtype, nb, c, dim3(lc.nsm, ceil_div(B, nb)), lc.st, false) !=
+        cudaSuccess)
+        return DV_ERR_CUDA;
+    return DV_OK;
+}
+
+dv_status check_ws(const dv_layer_desc &D, int B, void *ws, size_t ws_bytes, WsLayout *L)
+{
+    if (!ws_layout(D, B, L))
+        return DV_ERR_INVALID_ARG;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < L->total)
+        return DV_ERR_WORKSPACE;
+    return DV_OK;
+}
+
+bool sel_ok(const dv_selection *sel)
+{
+    return sel && sel->idx_h && sel->idx_n && sel->u_h && sel->n_u_h && sel->u_n && sel->n_u_n;
+}
+
+dv_status layer_decode_impl(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x,
+                            const float *x_pred, int batch, int k_heads, int k_neurons, void *kc,
+                            void *vc, int kv_len, const dv_selection *sel, float *h1, float *y,
+                            void *ws, size_t ws_bytes, void *const *events, int n_events,
+                            void *stream)
+{
+    dv_status s = check_desc(desc);
+    if (s)
+        return s;
+    if ((s = check_weights(w)))
+        return s;
+    const dv_layer_desc &D = *desc;
+    if (batch < 1 || batch > DV_MAX_BATCH || k_heads < 1 || k_heads > D.n_heads ||
+        k_neurons < 1 || k_neurons > D.d_ffn || kv_len < 0 || kv_len >= D.kv_cap)
+        return DV_ERR_INVALID_ARG;
+    if (!ptr_ok(x) || (x_pred && !ptr_ok(x_pred)) || !ptr_ok(y) || (h1 && !ptr_ok(h1)) ||
+        !ptr_ok(kc) || !ptr_ok(vc) || !sel_ok(sel))
+        return DV_ERR_INVALID_ARG;
+    if (events && n_events < kLayerLaunches + 1)
+        return DV_ERR_INVALID_ARG;
+    WsLayout L;
+    if ((s = check_ws(D, batch, ws, ws_bytes, &L)))
+        return s;
+    Launch lc;
+    if ((s = make_launch(stream, events, n_events, &lc)))
+        return s;
+    float *h1p = h1 ? h1 : at<float>(ws, L.h1);
+    const int max_u_h = batch * k_heads < D.n_heads ? batch * k_heads : D.n_heads;
+    const int max_u_n = batch * k_neurons < D.d_ffn ? batch * k_neurons : D.d_ffn;
+    if ((s = run_predict(D, *w, x_pred ? x_pred : x, batch, k_heads, k_neurons, *sel, nullptr,
+                         nullptr, ws, L, lc)))
+        return s;
+    if ((s = run_attn(D, *w, x, batch, sel->u_h, sel->n_u_h, max_u_h, kc, vc, kv_len, h1p, ws, L,
+                      lc)))
+        return s;
+    if ((s = run_mlp(D, *w, h1p, batch, sel->u_n, sel->n_u_n, max_u_n, y, ws, L, lc)))
+        return s;
+    if ((s = lc.mark()))
+        return s;
+    return cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+
+namespace dv {
+
+bool ws_layout(const dv_layer_desc &D, int B, WsLayout *L)
+{
+    if (check_desc(&D) != DV_OK || B < 1 || B > DV_MAX_BATCH)
+        return false;
+    const size_t d = D.d_model, H = D.n_heads, dh = D.head_dim, N = D.d_ffn, r = D.pred_rank;
+    const size_t bp = (size_t)batch_pad(B);
+    const size_t splits = (size_t)ceil_div(D.kv_cap, kAttnMinSplit);
+    const size_t S = (size_t)ceil_div(D.d_model, 32 * (int)(16 / esize(D.dtype)));
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes, 256);
+        return o;
+    };
+    std::memset(L, 0, sizeof(*L));
+    L->ctl = take(64 * 4);
+    L->hist = take((size_t)B * kTopkBins * 4);
+    L->s_h = take((size_t)B * H * 4);
+    L->u = take((size_t)B * r * 4);
+    L->s_n = take((size_t)B * N * 4);
+    L->q = take((size_t)B * H * dh * 4);
+    L->attn_part = take((size_t)B * H * splits * (kAttnRec + dh) * 4);
+    L->attn_cnt = take((size_t)B * H * 4);
+    L->o = take((size_t)B * H * dh * 4);
+    L->h1 = take((size_t)B * d * 4);
+    L->act = take((size_t)B * N * 4);
+    L->part_pred1 = take(bp * (H + r) * kMaxSeg * 4);
+    L->part_qkv = take(bp * 3 * H * dh * kMaxSeg * 4);
+    L->part_fc1 = take(bp * N * kMaxSeg * 4);
+    L->cnt_pred1 = take(bp * (H + r) * 4);
+    L->cnt_qkv = take(bp * 3 * H * dh * 4);
+    L->cnt_fc1 = take(bp * N * 4);
+    L->cpart_o = take(bp * kMaxColGroups * d * 4);
+    L->cpart_2 = take(bp * kMaxColGroups * d * 4);
+    L->ccnt_o = take(bp * S * 4);
+    L->ccnt_2 = take(bp * S * 4);
+    L->stage_x = take((size_t)B * d * 4);
+    L->stage_xp = take((size_t)B * d * 4);
+    L->stage_y = take((size_t)B * d * 4);
+    L->sel_idx_h = take((size_t)B * H * 4);
+    L->sel_idx_n = take((size_t)B * N * 4);
+    L->sel_u_h = take(H * 4);
+    L->sel_n_u_h = take(4);
+    L->sel_u_n = take(N * 4);
+    L->sel_n_u_n = take(4);
+    L->total = off;
+    L->bpad = (int)bp;
+    L->attn_splits_max = (int)splits;
+    return true;
+}
+
+}  // namespace dv
+
+extern "C" {
+
+const char *dv_status_string(int status)
+{
+    switch (status) {
+    case DV_OK: return "ok";
+    case DV_ERR_INVALID_ARG: return "invalid argument";
+    case DV_ERR_UNSUPPORTED: return "unsupported shape or type";
+    case DV_ERR_CUDA: return "CUDA runtime error";
+    case DV_ERR_TIMEOUT: return "device wait timed out";
+    case DV_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case DV_ERR_DEVICE_INDEX: return "a kernel met an index outside its range";
+    default: return "unknown status";
+    }
+}
+
+int dv_abi_version(void) { return DV_ABI_VERSION; }
+
+size_t dv_workspace_size(const dv_layer_desc *desc, int batch)
+{
+    if (!desc)
+        return 0;
+    WsLayout L;
+    if (!ws_layout(*desc, batch, &L))
+        return 0;
+    return L.total;
+}
+
+int dv_workspace_init(void *ws, size_t ws_bytes, void *stream)
+{
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < 256)
+        return DV_ERR_WORKSPACE;
+    return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream)));
+}
+
+int dv_check(void *ws, size_t ws_bytes, void *stream)
+{
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < 256)
+        return DV_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess)
+        return DV_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return DV_ERR_CUDA;
+    if (v != 0 && cudaMemset(ws, 0, sizeof(int)) != cudaSuccess)
+        return DV_ERR_CUDA;
+    return v;
+}
+
+int dv_layer_decode_launches(const dv_layer_desc *desc, int batch)
+{
+    if (check_desc(desc) != DV_OK || batch < 1 || batch > DV_MAX_BATCH)
+        return 0;
+    return kLayerLaunches;
+}
+
+int dv_predict_topk(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x_pred,
+                    int batch, int k_heads, int k_neurons, const dv_selection *sel,
+                    float *scores_h, float *scores_n, void *ws, size_t ws_bytes, void *stream)
+{
+    dv_status s = check_desc(desc);
+    if (s)
+        return s;
+    if (!w || !ptr_ok(w->pred_h) || !ptr_ok(w->pred_a) || !ptr_ok(w->pred_b))
+        return DV_ERR_INVALID_ARG;
+    const dv_layer_desc &D = *desc;
+    if (batch < 1 || batch > DV_MAX_BATCH || k_heads < 1 || k_heads > D.n_heads ||
+        k_neurons < 1 || k_neurons > D.d_ffn || !ptr_ok(x_pred) || !sel_ok(sel))
+        return DV_ERR_INVALID_ARG;
+    WsLayout L;
+    if ((s = check_ws(D, batch, ws, ws_bytes, &L)))
+        return s;
+    Launch lc;
+    if ((s = make_launch(stream, nullptr, 0, &lc)))
+        return s;
+    if ((s = run_predict(D, *w, x_pred, batch, k_heads, k_neurons, *sel, scores_h, scores_n, ws,
+                         L, lc)))
+        return s;
+    return cuda_status(cudaGetLastError());
+}
+
+int dv_sparse_attn(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x, int batch,
+                   const int32_t *u_h, const int32_t *n_u_h, int max_u_h, void *k_cache,
+                   void *v_cache, int kv_len, float *h1, void *ws, size_t ws_bytes, void *stream)
+{
+    dv_status s = check_desc(desc);
+    if (s)
+        return s;
+    if ((s = check_weights(w)))
+        return s;
+    const dv_layer_desc &D = *desc;
+    if (batch < 1 || batch > DV_MAX_BATCH || max_u_h < 1 || max_u_h > D.n_heads || kv_len < 0 ||
+        kv_len >= D.kv_cap || !ptr_ok(x) || !ptr_ok(h1) || !u_h || !n_u_h || !ptr_ok(k_cache) ||
+        !ptr_ok(v_cache) || x == h1)
+        return DV_ERR_INVALID_ARG;
+    WsLayout L;
+    if ((s = check_ws(D, batch, ws, ws_bytes, &L)))
+        return s;
+    Launch lc;
+    if ((s = make_launch(stream, nullptr, 0, &lc)))
+        return s;
+    if ((s = run_attn(D, *w, x, batch, u_h, n_u_h, max_u_h, k_cache, v_cache, kv_len, h1, ws, L,
+                      lc)))
+        return s;
+    return cuda_status(cudaGetLastError());
+}
+
+int dv_sparse_mlp(const dv_layer_desc *desc, const dv_layer_weights *w, const float *h1, int batch,
+                  const int32_t *u_n, const int32_t *n_u_n, int max_u_n, float *y, void *ws,
+                  size_t ws_bytes, void *stream)
+{
+    dv_status s = check_desc(desc);
+    if (s)
+        return s;
+    if ((s = check_weights(w)))
+        return s;
+    const dv_layer_desc &D = *desc;
+    if (batch < 1 || batch > DV_MAX_BATCH || max_u_n < 1 || max_u_n > D.d_ffn || !ptr_ok(h1) ||
+        !ptr_ok(y) || !u_n || !n_u_n || h1 == y)
+        return DV_ERR_INVALID_ARG;
+    WsLayout L;
+    if ((s = check_ws(D, batch, ws, ws_bytes, &L)))
+        return s;
+    Launch lc;
+    if ((s = make_launch(stream, nullptr, 0, &lc)))
+        return s;
+    if ((s = run_mlp(D, *w, h1, batch, u_n, n_u_n, max_u_n, y, ws, L, lc)))
+        return s;
+    return cuda_status(cudaGetLastError());
+}
+
+int dv_layer_decode(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x,
+                    const float *x_pred, int batch, int k_heads, int k_neurons, void *k_cache,
+                    void *v_cache, int kv_len, const dv_selection *sel, float *h1, float *y,
+                    void *ws, size_t ws_bytes, void *stream)
+{
+    return layer_decode_impl(desc, w, x, x_pred, batch, k_heads, k_neurons, k_cache, v_cache,
+                             kv_len, sel, h1, y, ws, ws_bytes, nullptr, 0, stream);
+}
+
+int dv_layer_decode_traced(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x,
+                           const float *x_pred, int batch, int k_heads, int k_neurons,
+                           void *k_cache, void *v_cache, int kv_len, const dv_selection *sel,
+                           float *h1, float *y, void *ws, size_t ws_bytes, void *const *events,
+                           int n_events, void *stream)
+{
+    if (!events)
+        return DV_ERR_INVALID_ARG;
+    for (int i = 0; i < n_events; ++i)
+        if (!events[i])
+            return DV_ERR_INVALID_ARG;
+    return layer_decode_impl(desc, w, x, x_pred, batch, k_heads, k_neurons, k_cache, v_cache,
+                             kv_len, sel, h1, y, ws, ws_bytes, events, n_events, stream);
+}
+
+int dv_layer_decode_host(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x_host,
+                         const float *x_pred_host, int batch, int k_heads, int k_neurons,
+                         void *k_cache, void *v_cache, int kv_len, const dv_selection *sel,
+                         float *y_host, void *ws, size_t ws_bytes, void *stream)
+{
+    dv_status s = check_desc(desc);
+    if (s)
+        return s;
+    if (!x_host || !y_host || batch < 1 || batch > DV_MAX_BATCH)
+        return DV_ERR_INVALID_ARG;
+    WsLayout L;
+    if ((s = check_ws(*desc, batch, ws, ws_bytes, &L)))
+        return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t bytes = (size_t)batch * desc->d_model * sizeof(float);
+    float *x_dev = at<float>(ws, L.stage_x);
+    float *xp_dev = x_pred_host ? at<float>(ws, L.stage_xp) : nullptr;
+    float *y_dev = at<float>(ws, L.stage_y);
+    if (cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return DV_ERR_CUDA;
+    if (xp_dev &&
+        cudaMemcpyAsync(xp_dev, x_pred_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return DV_ERR_CUDA;
+    dv_selection own;
+    if (!sel) {  // keep the selection in the workspace
+        own.idx_h = at<int32_t>(ws, L.sel_idx_h);
+        own.idx_n = at<int32_t>(ws, L.sel_idx_n);
+        own.u_h = at<int32_t>(ws, L.sel_u_h);
+        own.n_u_h = at<int32_t>(ws, L.sel_n_u_h);
+        own.u_n = at<int32_t>(ws, L.sel_u_n);
+        own.n_u_n = at<int32_t>(ws, L.sel_n_u_n);
+        sel = &own;
+    }
+    s = layer_decode_impl(desc, w, x_dev, xp_dev, batch, k_heads, k_neurons, k_cache, v_cache,
+                          kv_len, sel, nullptr, y_dev, ws, ws_bytes, nullptr, 0, stream);
+    if (s)
+        return s;
+    if (cudaMemcpyAsync(y_host, y_dev, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return DV_ERR_CUDA;
+    return cuda_status(cudaStreamSynchronize(st));
+}
+
+int dv_hbm_copy(void *dst, const void *src, size_t bytes, void *stream)
+{
+    if (!ptr_ok(dst) || !ptr_ok(src) || bytes == 0 || (bytes & 15u))
+        return DV_ERR_INVALID_ARG;
+    Launch lc;
+    dv_status s = make_launch(stream, nullptr, 0, &lc);
+    if (s)
+        return s;
+    return cuda_status(launch_copy(dst, src, bytes / 16, lc.nsm * 4, lc.st));
+}
+
+}  // extern "C"

@@ -1,0 +1,173 @@
+// dv_common.cuh -- device helpers shared by the sm_103a kernels of libdv.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dv_internal.h"
+
+namespace dv {
+
+#define DV_DEV __device__ __forceinline__
+
+constexpr int kWarp = 32;
+
+// ---------------------------------------------------------------------------
+// Global-memory access.
+//
+// Weights and KV rows are read exactly once per call: 16-byte vector loads
+// through the non-coherent path, not allocated in L1, with a 256-byte L2
+// prefetch hint so DRAM sees whole bursts.
+DV_DEV uint4 ld_stream(const void *p)
+{
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+// Values written by other CTAs of the same kernel: read at L2 (bypass L1).
+DV_DEV float ld_cg(const float *p) { return __ldcg(p); }
+DV_DEV int ld_cg(const int *p) { return __ldcg(p); }
+
+// Record the first device-side fault in the workspace status word.
+DV_DEV void set_status(int *status, int code)
+{
+    if (status)
+        atomicCAS(status, 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// Storage types.  A 16-byte vector holds EPC elements of T.
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<float> {
+    static constexpr int EPC = 4;
+    DV_DEV static void unpack(const uint4 &v, float (&f)[4])
+    {
+        f[0] = __uint_as_float(v.x);
+        f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z);
+        f[3] = __uint_as_float(v.w);
+    }
+    DV_DEV static float load(const float *p, size_t i) { return p[i]; }
+    DV_DEV static float to_float(float v) { return v; }
+    DV_DEV static float from_float(float v) { return v; }
+};
+
+template <>
+struct Elem<__half> {
+    static constexpr int EPC = 8;
+    DV_DEV static void unpack(const uint4 &v, float (&f)[8])
+    {
+        const __half2 *h = reinterpret_cast<const __half2 *>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 t = __half22float2(h[i]);
+            f[2 * i] = t.x;
+            f[2 * i + 1] = t.y;
+        }
+    }
+    DV_DEV static float load(const __half *p, size_t i) { return __half2float(p[i]); }
+    DV_DEV static float to_float(__half v) { return __half2float(v); }
+    DV_DEV static __half from_float(float v) { return __float2half_rn(v); }
+};
+
+// ---------------------------------------------------------------------------
+// Warp and block reductions / scans.
+DV_DEV float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+DV_DEV int warp_sum_int(int v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+DV_DEV int warp_incl_scan(int v, int lane)
+{
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o)
+            v += t;
+    }
+    return v;
+}
+
+// Exclusive prefix sum over the block (blockDim.x a multiple of 32, <= 1024).
+// `scratch` holds >= 33 ints of shared memory.  Returns this thread's
+// exclusive prefix; *total receives the block total.  Contains barriers.
+DV_DEV int block_excl_scan(int v, int *scratch, int *total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nw = blockDim.x >> 5;
+    int inc = warp_incl_scan(v, lane);
+    if (lane == 31)
+        scratch[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        int t = lane < nw ? scratch[lane] : 0;
+        int ti = warp_incl_scan(t, lane);
+        if (lane < nw)
+            scratch[lane] = ti - t;
+        if (lane == 31)
+            scratch[32] = ti;
+    }
+    __syncthreads();
+    int r = scratch[warp] + inc - v;
+    *total = scratch[32];
+    __syncthreads();
+    return r;
+}
+
+// Sum over the block (float); result valid in every thread.  Barriers inside.
+DV_DEV float block_sum(float v, float *scratch)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nw = blockDim.x >> 5;
+    v = warp_sum(v);
+    if (lane == 0)
+        scratch[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        float t = lane < nw ? scratch[lane] : 0.f;
+        t = warp_sum(t);
+        if (lane == 0)
+            scratch[32] = t;
+    }
+    __syncthreads();
+    float r = scratch[32];
+    __syncthreads();
+    return r;
+}
+
+// ---------------------------------------------------------------------------
+// Order-preserving key of a binary32 score: larger float -> larger unsigned.
+// -0.0 is folded onto +0.0 so equal scores tie (and the lower index wins).
+DV_DEV unsigned score_key(float s)
+{
+    unsigned u = __float_as_uint(s);
+    if (u == 0x80000000u)
+        u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch (griddepcontrol); no-ops when the kernel was
+// launched without the attribute.
+DV_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+DV_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+}  // namespace dv

@@ -1,0 +1,135 @@
+// dv_internal.h -- argument blocks, workspace layout and launcher entry
+// points shared by the host code and the kernel translation units of libdv.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "dv.h"
+
+namespace dv {
+
+constexpr int kThreads = 512;                    // block size of the GEMV kernels
+constexpr int kWarpsPerBlock = kThreads / 32;
+constexpr int kTopkBins = 2048;                  // first radix digit: 11 bits
+constexpr int kMaxSeg = 4;                       // row segments of the row-dot kernel
+constexpr int kMaxColGroups = 64;                // row groups of the column kernel
+constexpr int kAttnMinSplit = 32;                // KV positions per attention split (min)
+constexpr int kAttnRec = 4;                      // floats before o[] in a split record
+constexpr size_t kSmemCap = 200 * 1024;          // dynamic shared memory budget
+constexpr int kMaxDevices = 64;
+
+enum RowKind { RK_PRED1 = 0, RK_PRED2 = 1, RK_QKV = 2, RK_FC1 = 3 };
+enum ColKind { CK_OPROJ = 0, CK_FC2 = 1 };
+
+// ---------------------------------------------------------------------------
+// Row-dot kernel: out_row = dot(W[row], xs) over a list of rows, with an
+// optional norm of the activations, a per-kind epilogue and (predictor kinds)
+// a fused top-k done by the last CTA.
+struct RowArgs {
+    int K;            // row length in elements
+    int nseg;         // segments per row
+    int seglen;       // K / nseg (multiple of 16 bytes)
+    int B;            // batch rows
+    int max_rows;     // host bound on the number of rows
+    const int32_t *n_sel;  // device length of the gather list (QKV, FC1)
+    int max_sel;      // host bound on *n_sel
+    const int32_t *sel;    // gather list (u_h for QKV, u_n for FC1)
+    int sel_range;    // valid gathered indices are [0, sel_range)
+    const float *x;   // activations [B][x_ld]
+    int x_ld;
+    const void *norm_g, *norm_b;  // NULL: no norm
+    int norm_kind;
+    float eps;
+    const void *w0, *w1;  // PRED1: pred_h, pred_a; PRED2: pred_b; QKV: w_qkv; FC1: w1
+    const void *bias;     // QKV: b_qkv; FC1: b1
+    int H, dh, split_rows;
+    float *out0, *out1;   // PRED1: s_h, u; PRED2: s_n; QKV: q; FC1: act
+    float *user_scores;   // optional copy of the scores (predictor kinds)
+    void *kc, *vc;
+    int kv_len, kv_cap;
+    float q_scale;
+    float *part;          // segment partials [tiles][max_rows][nseg][NB]
+    int *rowcnt;          // segment arrivals [tiles][max_rows]
+    // fused top-k
+    int topk_n, topk_k;
+    int *hist;            // PRED2: first-digit histogram [B][kTopkBins], zero at rest
+    int32_t *idx_out;     // [B][topk_k]
+    int32_t *u_out, *n_u_out;
+    int *done;            // CTA arrival counter, zero at rest
+    int *status;
+};
+
+// Column-accumulate kernel: out[b][c] = res[b][c] + bias[c]
+//                                      + sum_i coef[b][i] * W[row(i)][c].
+struct ColArgs {
+    int d;
+    int B;
+    const int32_t *n_sel;
+    int max_sel;
+    const int32_t *sel;   // u_h (OPROJ, rows = heads x dh) or u_n (FC2)
+    int sel_range;
+    int dh;
+    const void *w;        // w_oT or w2T
+    const float *coef;    // [B][coef_ld]
+    int coef_ld;
+    const float *res;     // [B][d]
+    const void *bias;     // [d]
+    float *out;           // [B][d]
+    int G;                // row groups (split-K)
+    float *part;          // [tiles][G][NB][d]
+    int *cnt;             // [tiles][slices], zero at rest
+    int *status;
+};
+
+// Split-KV decode attention over the selected heads.
+struct AttnArgs {
+    int B, H, dh, kv_cap, kv_len;
+    const int32_t *n_sel;
+    int max_sel;
+    const int32_t *sel;
+    const float *q;       // [B][max_sel][dh], already scaled
+    const void *kc, *vc;  // [B][H][kv_cap][dh]
+    int splits, split_len;
+    float *part;          // [B][max_sel][splits][kAttnRec + dh]
+    int *cnt;             // [B][max_sel], zero at rest
+    float *o;             // [B][max_sel][dh]
+    int *status;
+};
+
+// ---------------------------------------------------------------------------
+// Workspace layout (byte offsets from the workspace base, 256-byte aligned).
+struct WsLayout {
+    size_t ctl;       // int[64]: [0] status, [1] done(pred1), [2] done(pred2)
+    size_t hist;      // int[B][kTopkBins]
+    size_t s_h, u, s_n;
+    size_t q, attn_part, attn_cnt, o;
+    size_t h1, act;
+    size_t part_pred1, part_qkv, part_fc1;
+    size_t cnt_pred1, cnt_qkv, cnt_fc1;
+    size_t cpart_o, cpart_2, ccnt_o, ccnt_2;
+    size_t stage_x, stage_xp, stage_y;
+    size_t sel_idx_h, sel_idx_n, sel_u_h, sel_n_u_h, sel_u_n, sel_n_u_n;
+    size_t total;
+    int bpad;         // batch rounded up to the largest batch tile (8)
+    int attn_splits_max;
+};
+
+bool ws_layout(const dv_layer_desc &D, int B, WsLayout *L);
+
+// Launchers (one per kernel family); return the CUDA error of the launch.
+cudaError_t launch_rowdot(int kind, int dtype, int nb, const RowArgs &a, dim3 grid, size_t smem,
+                          cudaStream_t st, bool pdl);
+cudaError_t launch_colacc(int kind, int dtype, int nb, const ColArgs &a, dim3 grid,
+                          cudaStream_t st, bool pdl);
+cudaError_t launch_attn(int dtype, int lanes_per_key, const AttnArgs &a, dim3 grid,
+                        cudaStream_t st, bool pdl);
+cudaError_t launch_copy(void *dst, const void *src, size_t n16, int grid, cudaStream_t st);
+
+// Largest-batch tile each kernel family handles per CTA.
+int rowdot_nb(int B, int K, int kind);
+int colacc_nb(int B);
+size_t rowdot_smem(int kind, int nb, int K, int topk_n);
+
+}  // namespace dv

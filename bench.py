@@ -1,0 +1,508 @@
+#!/usr/bin/env python3
+"""Benchmark of the contextually sparse (DejaVu) layer decode at the OPT-175B shape.
+
+One step = one sparse decode of one OPT-175B-shaped layer (d=12288, 96 heads
+x 128, N=49152, predictor rank 1000, fp16 storage, fp32 arithmetic, batch 1,
+KV length 2048, keep 2458 neurons / 20 heads): predictor + top-k, head-sparse
+QKV + KV append, decode attention over the selected heads, head-sparse
+out-projection, fc1 gather + ReLU, fc2 gather, both residuals.
+
+Inputs are synthetic (seeded torch RNG on the device) and resident in HBM
+before timing.  Each step decodes the next of `--copies` distinct layer
+copies (4 x 3.9 GB by default), so no step's 519 MB of required bytes can be
+served from the 129 MB L2 left over by the previous step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle (the
+plain binary64 C implementation) on the same workload.  Under torchrun (N > 1)
+each rank runs an independent replica (the path has no cross-GPU exchange).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+KERNELS = ["pred_stage1_head_topk", "pred_stage2_neuron_topk", "qkv_ln1_kv_append",
+           "attn_decode", "oproj_residual", "fc1_ln2_relu", "fc2_residual"]
+KERNEL_BYTES_KEY = ["pred_stage1", "pred_stage2", "qkv", "attn", "oproj", "fc1", "fc2"]
+METRIC = "µs per sparse layer-decode and achieved HBM GB/s (% roofline) at OPT-175B shape"
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
+    p.add_argument("--config", default="opt175b")
+    p.add_argument("--batch", type=int, default=None)
+    p.add_argument("--copies", type=int, default=4)
+    p.add_argument("--cpu-budget-s", type=float, default=15.0)
+    p.add_argument("--no-extras", action="store_true",
+                   help="skip dense baseline, e2e, copy peak and CPU baseline legs")
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas: a barrier and a max over ranks, nothing else)
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return rank, world
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Largest value over all ranks (the whole job ends when the slowest rank does)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_us_per_decode(max_ms: float, steps: int, world: int) -> float:
+    """Aggregate time per layer decode over all replicas: the slowest rank's
+    wall time divided by every decode the job completed."""
+    return max_ms * 1000.0 / (steps * world)
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled while the timed loop runs
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_uuid=None, interval_ms=50):
+        self.proc = None
+        self.lines = []
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", str(interval_ms)]
+        if gpu_uuid:
+            cmd += ["-i", gpu_uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"samples": 0, "note": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [ln.split(",") for ln in out.strip().splitlines() if ln.count(",") >= 8]
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() in ("active", "1"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "of measured (MEASURED_PEAKS.json hbm_gbs)"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "of fallback (6.8 TB/s)"
+
+
+def profile_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the
+    current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    from attention_dv_predict_gb300 import build as dv_build
+
+    if d.get("source_hash") != dv_build.source_hash():
+        return None
+    v = d.get("kernels", {}).get(kernel, {}).get("dram_bytes_per_launch")
+    return float(v) if v is not None else None
+
+
+# ---------------------------------------------------------------------------
+# the CUDA arm
+
+
+def workload_config(cfg, B):
+    return {"workload": f"{cfg.name}-sparse-layer-decode", "d_model": cfg.d_model,
+            "n_heads": cfg.n_heads, "head_dim": cfg.head_dim, "d_ffn": cfg.d_ffn,
+            "pred_rank": cfg.pred_rank, "batch": B, "kv_len": cfg.kv_len,
+            "k_neurons": cfg.k_neurons, "k_heads": cfg.k_heads, "storage": cfg.dtype}
+
+
+def run_cuda(args):
+    import torch
+
+    rank, world = dist_init("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        from attention_dv_predict_gb300 import build as dv_build
+
+        dv_build.build()
+    barrier()
+    from attention_dv_predict_gb300 import dv
+    from attention_dv_predict_gb300 import traffic
+    import dv_inputs
+
+    cfg = dv_inputs.CONFIGS[args.config]
+    B = args.batch or cfg.batch
+    cfg = cfg.with_(batch=B)
+    k_h, k_n = cfg.k_heads, cfg.k_neurons
+    desc = dv.desc_from_config(cfg)
+    copies = max(1, args.copies)
+
+    layers, caches = [], []
+    for i in range(copies):
+        w = dv_inputs.make_weights(cfg, seed=1000 * rank + i, device=dev)
+        layers.append(dv.Layer(desc, w))
+        caches.append(dv_inputs.make_kv(cfg, B, seed=1000 * rank + i, device=dev))
+    x = dv_inputs.make_x(cfg, B, seed=rank, device=dev)
+    y = torch.empty_like(x)
+    sel = dv.SelectionBuffers(desc, B, k_h, k_n)
+    ws = dv.Workspace(desc, B)
+    stream = torch.cuda.Stream(device=dev)
+    n_launch = dv.dv_layer_decode_launches(desc, B)
+
+    def step(i, s):
+        kc, vc = caches[i % copies]
+        dv.dv_layer_decode(layers[i % copies], x, k_h, k_n, kc, vc, cfg.kv_len, sel, y, ws,
+                           stream=s)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(copies):
+            step(i, stream)
+    stream.synchronize()
+    if dv.dv_check(ws, stream) != dv.DV_OK:
+        raise RuntimeError("device status set after the first steps")
+    u_h, u_n = sel.unions()
+    n_u_h, n_u_n = int(u_h.numel()), int(u_n.numel())
+
+    # one CUDA graph per layer copy; a step is one graph replay
+    graphs = []
+    with torch.cuda.stream(stream):
+        for i in range(copies):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(i, stream)
+            graphs.append(g)
+    stream.synchronize()
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % copies].replay()
+    stream.synchronize()
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid)
+    time.sleep(0.3)  # let the sampler start before the timed region
+    barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for i in range(args.steps):
+            graphs[i % copies].replay()
+        t1.record(stream)
+    t1.synchronize()
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    ms = t0.elapsed_time(t1)
+    ms_max = max_over_ranks(ms, dev)
+    if dv.dv_check(ws, stream) != dv.DV_OK:
+        raise RuntimeError("device status set during the timed steps")
+
+    us_per_decode = whole_job_us_per_decode(ms_max, args.steps, world)
+    step_bytes = traffic.sparse_step_bytes(cfg.d_model, cfg.n_heads, cfg.head_dim, cfg.d_ffn,
+                                           cfg.pred_rank, 2 if cfg.dtype == "f16" else 4, B,
+                                           n_u_h, n_u_n, cfg.kv_len)
+    peak, peak_src = measured_peaks()
+    rank_us = ms_max * 1000.0 / args.steps
+    achieved = step_bytes.total / (rank_us * 1e-6) / 1e9
+
+    # per-kernel durations: the same steps with an event before every kernel
+    kt = min(args.steps, 200)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_launch + 1)] for _ in range(kt)]
+    with torch.cuda.stream(stream):
+        for i in range(kt):
+            kc, vc = caches[i % copies]
+            dv.dv_layer_decode_traced(layers[i % copies], x, k_h, k_n, kc, vc, cfg.kv_len, sel,
+                                      y, ws, evs[i], stream=stream)
+    stream.synchronize()
+    per_kernel = [statistics.mean(evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(kt))
+                  for k in range(n_launch)]
+    traced_step_ms = statistics.mean(evs[i][0].elapsed_time(evs[i][n_launch]) for i in range(kt))
+    kb = traffic.kernel_bytes(cfg.d_model, cfg.n_heads, cfg.head_dim, cfg.d_ffn, cfg.pred_rank,
+                              2 if cfg.dtype == "f16" else 4, B, n_u_h, n_u_n, cfg.kv_len)
+    dom = max(range(n_launch), key=lambda k: per_kernel[k])
+    dom_bytes = kb[KERNEL_BYTES_KEY[dom]]
+    dom_gbs = dom_bytes / (per_kernel[dom] * 1e-3) / 1e9
+    kernels = {KERNELS[k]: {"us": round(per_kernel[k] * 1e3, 2),
+                            "share": round(per_kernel[k] / sum(per_kernel), 4),
+                            "alg_bytes": kb[KERNEL_BYTES_KEY[k]],
+                            "gbs": round(kb[KERNEL_BYTES_KEY[k]] / (per_kernel[k] * 1e-3) / 1e9, 1)}
+               for k in range(n_launch)}
+
+    line = {
+        "metric": METRIC, "value": round(us_per_decode, 3), "unit": "µs per layer-decode",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_max / args.steps, 6), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": dict(workload_config(cfg, B), copies=copies,
+                       l2="each step reads a different layer copy; 519 MB/step > 129 MB L2",
+                       parallelism="replicas" if world > 1 else "single GPU"),
+        "achieved_gbs": round(achieved, 1),
+        "roofline_frac_step": round(achieved / peak, 4),
+        "required_bytes_per_step": step_bytes.total,
+        "union": {"heads": n_u_h, "neurons": n_u_n},
+        "roofline": {"bound": "hbm", "kernel": KERNELS[dom], "achieved": round(dom_gbs, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
+                     "traffic": profile_traffic(KERNELS[dom]), "peak_source": peak_src,
+                     "alg_bytes_per_launch": dom_bytes},
+        "kernels": kernels,
+        "traced_step_us": round(traced_step_ms * 1e3, 2),
+        "gpu_launches": args.steps * n_launch,
+        "clocks": clocks,
+    }
+
+    if not args.no_extras:
+        line.update(extras(args, dv, traffic, cfg, desc, layers, caches, x, sel, ws, stream,
+                           rank, us_per_decode, k_h, k_n, B))
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def extras(args, dv, traffic, cfg, desc, layers, caches, x, sel, ws, stream, rank,
+           us_per_decode, k_h, k_n, B):
+    import numpy as np
+    import torch
+
+    out = {}
+    copies = len(layers)
+    # end to end through the C ABI with host activations (pinned), copies inside
+    xh = x.cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    ke = min(args.steps, 500)
+    for i in range(min(5, ke)):
+        kc, vc = caches[i % copies]
+        dv.dv_layer_decode_host(layers[i % copies], xh, k_h, k_n, kc, vc, cfg.kv_len, yh, ws,
+                                stream=stream)
+    t = time.perf_counter()
+    for i in range(ke):
+        kc, vc = caches[i % copies]
+        dv.dv_layer_decode_host(layers[i % copies], xh, k_h, k_n, kc, vc, cfg.kv_len, yh, ws,
+                                stream=stream)
+    e2e_us = (time.perf_counter() - t) * 1e6 / ke
+    out["e2e"] = {"value": round(e2e_us, 3), "unit": "µs per layer-decode",
+                  "h2d_bytes_per_step": int(xh.numel() * 4), "d2h_bytes_per_step": int(yh.numel() * 4),
+                  "steps": ke, "api": "dv_layer_decode_host"}
+
+    # dense-decode baseline: the same library with every head and neuron selected
+    dsel = dv.SelectionBuffers(desc, B, cfg.n_heads, cfg.d_ffn)
+    yd = torch.empty_like(x)
+    kd = min(args.steps, 30)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            kc, vc = caches[i % copies]
+            dv.dv_layer_decode(layers[i % copies], x, cfg.n_heads, cfg.d_ffn, kc, vc, cfg.kv_len,
+                               dsel, yd, ws, stream=stream)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(kd):
+            kc, vc = caches[i % copies]
+            dv.dv_layer_decode(layers[i % copies], x, cfg.n_heads, cfg.d_ffn, kc, vc, cfg.kv_len,
+                               dsel, yd, ws, stream=stream)
+        b.record(stream)
+    b.synchronize()
+    dense_us = a.elapsed_time(b) * 1e3 / kd
+    dense_bytes = traffic.dense_step_bytes(cfg.d_model, cfg.n_heads, cfg.head_dim, cfg.d_ffn,
+                                           2 if cfg.dtype == "f16" else 4, B, cfg.kv_len)
+    out["dense_baseline"] = {"us_per_decode": round(dense_us, 2),
+                             "speedup_sparse": round(dense_us / us_per_decode, 3),
+                             "bytes_per_step": dense_bytes,
+                             "achieved_gbs": round(dense_bytes / (dense_us * 1e-6) / 1e9, 1),
+                             "note": "same library, every head and neuron selected"}
+
+    # copy bandwidth of the library's own copy kernel (read + write bytes)
+    n = 1 << 30
+    src = torch.empty(n, dtype=torch.uint8, device=x.device)
+    dst = torch.empty_like(src)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            dv.dv_hbm_copy(dst, src, stream=stream)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(10):
+            dv.dv_hbm_copy(dst, src, stream=stream)
+        b.record(stream)
+    b.synchronize()
+    out["copy_peak_gbs"] = round(2 * n * 10 / (a.elapsed_time(b) * 1e-3) / 1e9, 1)
+    del src, dst
+
+    if rank == 0:
+        out["cpu_baseline"] = cpu_baseline(cfg, layers[0], caches[0], x, k_h, k_n,
+                                           args.cpu_budget_s)
+    return out
+
+
+def _oracle_inputs(cfg, layer, cache, x):
+    import oracle
+
+    w = {k: v.detach().cpu().numpy() for k, v in layer.weights.items()}
+    D = oracle.desc_from_config(cfg)
+    kc, vc = cache
+    return D, w, kc.cpu().numpy(), vc.cpu().numpy(), x.cpu().numpy()
+
+
+def cpu_baseline(cfg, layer, cache, x, k_h, k_n, budget_s):
+    """The CPU oracle (single-threaded C, binary64) on the same workload."""
+    import oracle
+
+    D, w, kc, vc, xh = _oracle_inputs(cfg, layer, cache, x)
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while True:
+        t = time.perf_counter()
+        oracle.layer_decode(D, w, xh, k_h, k_n, kc, vc, cfg.kv_len, inplace=True)
+        times.append(time.perf_counter() - t)
+        if time.perf_counter() >= t_end or len(times) >= 50:
+            break
+    us = statistics.median(times) * 1e6
+    return {"value": round(us, 1), "unit": "µs per layer-decode", "cores": 1, "kind": "oracle",
+            "sample": f"{len(times)} full layer decodes of the same {cfg.name} workload "
+                      f"(median), single-threaded C oracle on the host"}
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the CPU oracle
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import torch
+
+    import dv_inputs
+    import oracle
+    from oracle import build as oracle_build
+
+    oracle_build.build()
+    cfg = dv_inputs.CONFIGS[args.config]
+    B = args.batch or cfg.batch
+    cfg = cfg.with_(batch=B)
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = dv_inputs.make_weights(cfg, seed=0, device=gen_dev)
+    kc, vc = dv_inputs.make_kv(cfg, B, seed=0, device=gen_dev)
+    x = dv_inputs.make_x(cfg, B, seed=0, device=gen_dev)
+    wn = {k: v.cpu().numpy() for k, v in w.items()}
+    del w
+    kch, vch, xh = kc.cpu().numpy(), vc.cpu().numpy(), x.cpu().numpy()
+    D = oracle.desc_from_config(cfg)
+
+    def one():
+        oracle.layer_decode(D, wn, xh, cfg.k_heads, cfg.k_neurons, kch, vch, cfg.kv_len,
+                            inplace=True)
+
+    budget = 150.0
+    t = time.perf_counter()
+    one()
+    first = time.perf_counter() - t
+    warm = min(args.warmup, max(0, int(20.0 / max(first, 1e-3))))
+    for _ in range(max(0, warm - 1)):
+        one()
+    steps_run = max(1, min(args.steps, int(budget / max(first, 1e-3))))
+    t = time.perf_counter()
+    for _ in range(steps_run):
+        one()
+    sec = time.perf_counter() - t
+    us = sec * 1e6 / steps_run
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(us, 1),
+        "unit": "µs per layer-decode", "n_gpus": world, "steps": args.steps,
+        "steps_run": steps_run, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(cfg, B),
+        "cpu_baseline": {"value": round(us, 1), "unit": "µs per layer-decode", "cores": 1,
+                         "kind": "oracle",
+                         "sample": f"{steps_run} of the {args.steps} requested steps (bounded to "
+                                   f"~{int(budget)} s), each one full layer decode"},
+        "e2e": {"value": round(us, 1), "unit": "µs per layer-decode", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "note": "the reference arm is the CPU oracle (no upstream code exists to install)",
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_cuda(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,264 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Sizes: the tiny shape and a ragged shape that spans several tiles with
+ragged tails run in full; the OPT-6.7B/66B/175B shapes run at their full
+sizes in the launch configuration the benchmark times, and the oracle
+(plain C, binary64) computes every output for comparison.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import dv_inputs
+import oracle
+from parity import (assert_close, check_layer_parity, check_topk_rows, make_case,
+                    run_gpu_layer)
+
+pytestmark = pytest.mark.gpu
+
+CFG = dv_inputs.CONFIGS
+RAGGED = dv_inputs.LayerConfig("ragged", 264, 6, 64, 1000, 40, 37, 2, "f16",
+                               dv_inputs.Fraction(77, 1000), k_heads_fixed=3)
+
+
+@pytest.fixture(scope="module")
+def dv():
+    from attention_dv_predict_gb300 import build
+
+    build.build()
+    from attention_dv_predict_gb300 import dv as mod
+
+    return mod
+
+
+def test_tiny_fp32_layer(dv):
+    case = make_case(CFG["tiny"])
+    g = run_gpu_layer(dv, case)
+    out = check_layer_parity(case, g, tight=True)
+    assert out["diff_heads"] == 0 and out["diff_neurons"] == 0
+
+
+@pytest.mark.parametrize("norm", ["layernorm", "rmsnorm"])
+def test_tiny_batch3_union_and_norms(dv, norm):
+    case = make_case(CFG["tiny"].with_(norm=norm), B=3, separate_x_pred=True)
+    g = run_gpu_layer(dv, case)
+    check_layer_parity(case, g, tight=True)
+    assert CFG["tiny"].k_neurons <= g["u_n"].size <= 3 * CFG["tiny"].k_neurons
+
+
+@pytest.mark.parametrize("B", [1, 2, 5])
+def test_ragged_fp16_shapes(dv, B):
+    case = make_case(RAGGED, B=B, seed=B)
+    g = run_gpu_layer(dv, case)
+    check_layer_parity(case, g)
+
+
+def test_select_everything_equals_dense_oracle(dv):
+    cfg = CFG["tiny"]
+    case = make_case(cfg, B=2, k_h=cfg.n_heads, k_n=cfg.d_ffn)
+    g = run_gpu_layer(dv, case)
+    D = oracle.desc_from_config(case.cfg, case.kv_cap)
+    h1, y, _, _, _ = oracle.dense_layer(D, case.w_host, case.x, case.kc, case.vc, case.kv_len)
+    assert np.array_equal(g["u_h"], np.arange(cfg.n_heads))
+    assert np.array_equal(g["u_n"], np.arange(cfg.d_ffn))
+    assert_close(g["y"], y, "y", 1e-4, 1e-5)
+    assert_close(g["h1"], h1, "h1", 1e-4, 1e-5)
+
+
+@pytest.mark.parametrize("kv_len", [0, 1, 31, 32, 33])
+def test_kv_length_edges(dv, kv_len):
+    case = make_case(RAGGED, B=2, kv_len=kv_len, kv_cap=kv_len + 3)
+    g = run_gpu_layer(dv, case)
+    check_layer_parity(case, g)
+
+
+def test_k_equals_one(dv):
+    case = make_case(RAGGED, B=3, k_h=1, k_n=1)
+    g = run_gpu_layer(dv, case)
+    check_layer_parity(case, g)
+
+
+def test_ties_pick_lower_index(dv):
+    """Duplicate predictor rows give exactly equal scores: when only one of a
+    tied pair is kept, it is the lower index."""
+    cfg = CFG["tiny"]
+    case = make_case(cfg, B=1, k_h=3, k_n=101)
+    for key in ("pred_h", "pred_b"):
+        h = case.w_host[key]
+        h[1::2] = h[0::2]  # rows 2i and 2i+1 identical -> equal scores
+        case.w_dev[key].copy_(torch.from_numpy(h))
+    g = run_gpu_layer(dv, case)
+    D = oracle.desc_from_config(case.cfg, case.kv_cap)
+    p = oracle.predict(D, case.w_host, case.x, case.k_h, case.k_n)
+    for got, want, s, k in ((g["idx_h"], p["idx_h"], p["s_h"], case.k_h),
+                            (g["idx_n"], p["idx_n"], p["s_n"], case.k_n)):
+        check_topk_rows(got, want, s, k, "ties")
+        kept = set(got[0].tolist())
+        # k is odd, so at least one pair is split by the boundary
+        singles = [i for i in kept if (i ^ 1) not in kept]
+        assert singles and all(i % 2 == 0 for i in singles), singles
+
+
+def test_predict_scores_and_sets(dv):
+    case = make_case(RAGGED, B=4, seed=11)
+    desc = dv.desc_from_config(case.cfg, case.kv_cap)
+    layer = dv.Layer(desc, case.w_dev)
+    sel = dv.SelectionBuffers(desc, case.B, case.k_h, case.k_n)
+    ws = dv.Workspace(desc, case.B)
+    x = torch.from_numpy(case.x).cuda()
+    sh = torch.empty((case.B, case.cfg.n_heads), device="cuda")
+    sn = torch.empty((case.B, case.cfg.d_ffn), device="cuda")
+    dv.dv_predict_topk(layer, x, case.k_h, case.k_n, sel, ws, sh, sn)
+    torch.cuda.synchronize()
+    D = oracle.desc_from_config(case.cfg, case.kv_cap)
+    p = oracle.predict(D, case.w_host, case.x, case.k_h, case.k_n)
+    assert_close(sh.cpu().numpy(), p["s_h"], "head scores", 1e-4, 1e-5)
+    assert_close(sn.cpu().numpy(), p["s_n"], "neuron scores", 1e-4, 1e-5)
+    check_topk_rows(sel.idx_h.cpu().numpy(), p["idx_h"], p["s_h"], case.k_h, "heads")
+    check_topk_rows(sel.idx_n.cpu().numpy(), p["idx_n"], p["s_n"], case.k_n, "neurons")
+
+
+def test_blocks_on_caller_index_sets(dv):
+    """dv_sparse_attn and dv_sparse_mlp on index sets the caller chooses."""
+    case = make_case(RAGGED, B=2, seed=5)
+    desc = dv.desc_from_config(case.cfg, case.kv_cap)
+    layer = dv.Layer(desc, case.w_dev)
+    ws = dv.Workspace(desc, case.B)
+    rng = np.random.default_rng(0)
+    u_h = np.sort(rng.choice(case.cfg.n_heads, 4, replace=False)).astype(np.int32)
+    u_n = np.sort(rng.choice(case.cfg.d_ffn, 300, replace=False)).astype(np.int32)
+    x = torch.from_numpy(case.x).cuda()
+    kc = torch.from_numpy(case.kc).cuda()
+    vc = torch.from_numpy(case.vc).cuda()
+    h1 = torch.empty_like(x)
+    y = torch.empty_like(x)
+    uh_d = torch.from_numpy(u_h).cuda()
+    un_d = torch.from_numpy(u_n).cuda()
+    nuh = torch.tensor([u_h.size], dtype=torch.int32, device="cuda")
+    nun = torch.tensor([u_n.size], dtype=torch.int32, device="cuda")
+    dv.dv_sparse_attn(layer, x, uh_d, nuh, kc, vc, case.kv_len, h1, ws)
+    dv.dv_sparse_mlp(layer, h1, un_d, nun, y, ws)
+    torch.cuda.synchronize()
+    D = oracle.desc_from_config(case.cfg, case.kv_cap)
+    h1o, _, _, _ = oracle.sparse_attn(D, case.w_host, case.x, u_h, case.kc, case.vc, case.kv_len)
+    assert_close(h1.cpu().numpy() - case.x, h1o - case.x, "h1 - x")
+    yo, _ = oracle.sparse_mlp(D, case.w_host, h1.cpu().numpy().astype(np.float64), u_n)
+    assert_close(y.cpu().numpy(), yo, "y")
+    assert_close(y.cpu().numpy() - h1.cpu().numpy(), yo - h1.cpu().numpy(), "y - h1")
+    # a device count below the buffer length uses only the prefix
+    nun.fill_(100)
+    dv.dv_sparse_mlp(layer, h1, un_d, nun, y, ws)
+    torch.cuda.synchronize()
+    yo2, _ = oracle.sparse_mlp(D, case.w_host, h1.cpu().numpy().astype(np.float64), u_n[:100])
+    assert_close(y.cpu().numpy(), yo2, "y (prefix)")
+
+
+def test_out_of_range_indices_are_skipped_and_reported(dv):
+    case = make_case(RAGGED, B=1, seed=6)
+    desc = dv.desc_from_config(case.cfg, case.kv_cap)
+    layer = dv.Layer(desc, case.w_dev)
+    ws = dv.Workspace(desc, 1)
+    h1 = torch.from_numpy(case.x).cuda()
+    y = torch.empty_like(h1)
+    un = torch.tensor([3, case.cfg.d_ffn + 5, 7], dtype=torch.int32, device="cuda")
+    nun = torch.tensor([3], dtype=torch.int32, device="cuda")
+    dv.dv_sparse_mlp(layer, h1, un, nun, y, ws)
+    assert dv.dv_check(ws) == dv.DV_ERR_DEVICE_INDEX
+    assert dv.dv_check(ws) == dv.DV_OK  # reading clears it
+
+
+def test_deterministic_and_graph_replay(dv):
+    case = make_case(RAGGED, B=3, seed=7)
+    g1 = run_gpu_layer(dv, case)
+    g2 = run_gpu_layer(dv, case)
+    assert np.array_equal(g1["y"], g2["y"]) and np.array_equal(g1["idx_n"], g2["idx_n"])
+    # capture the whole decode in a CUDA graph and replay it
+    desc = dv.desc_from_config(case.cfg, case.kv_cap)
+    layer = dv.Layer(desc, case.w_dev)
+    sel = dv.SelectionBuffers(desc, case.B, case.k_h, case.k_n)
+    ws = dv.Workspace(desc, case.B)
+    x = torch.from_numpy(case.x).cuda()
+    kc = torch.from_numpy(case.kc).cuda()
+    vc = torch.from_numpy(case.vc).cuda()
+    y = torch.zeros_like(x)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            dv.dv_layer_decode(layer, x, case.k_h, case.k_n, kc, vc, case.kv_len, sel, y, ws,
+                               stream=s)
+    for _ in range(3):
+        y.zero_()
+        graph.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(y.cpu().numpy(), g1["y"])
+
+
+def test_host_entry_point_matches_device(dv):
+    case = make_case(RAGGED, B=2, seed=8)
+    g = run_gpu_layer(dv, case)
+    desc = dv.desc_from_config(case.cfg, case.kv_cap)
+    layer = dv.Layer(desc, case.w_dev)
+    ws = dv.Workspace(desc, case.B)
+    kc = torch.from_numpy(case.kc).cuda()
+    vc = torch.from_numpy(case.vc).cuda()
+    xh = torch.from_numpy(case.x).pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    dv.dv_layer_decode_host(layer, xh, case.k_h, case.k_n, kc, vc, case.kv_len, yh, ws)
+    assert np.array_equal(yh.numpy(), g["y"])
+
+
+def test_hbm_copy(dv):
+    src = torch.randn(1 << 22, device="cuda")
+    dst = torch.empty_like(src)
+    dv.dv_hbm_copy(dst, src)
+    torch.cuda.synchronize()
+    assert torch.equal(dst, src)
+
+
+def test_invalid_arguments_launch_nothing(dv):
+    case = make_case(CFG["tiny"])
+    desc = dv.desc_from_config(case.cfg, case.kv_cap)
+    layer = dv.Layer(desc, case.w_dev)
+    sel = dv.SelectionBuffers(desc, 1, case.k_h, case.k_n)
+    ws = dv.Workspace(desc, 1)
+    x = torch.from_numpy(case.x).cuda()
+    kc = torch.from_numpy(case.kc).cuda()
+    vc = torch.from_numpy(case.vc).cuda()
+    y = torch.full_like(x, 7.0)
+    for kh, kn, L in ((0, 5, 3), (case.cfg.n_heads + 1, 5, 3), (2, 0, 3), (2, 5, case.kv_cap)):
+        with pytest.raises(dv.DvError) as e:
+            dv.dv_layer_decode(layer, x, kh, kn, kc, vc, L, sel, y, ws)
+        assert e.value.status == dv.DV_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert torch.all(y == 7.0)
+
+
+# ---------------------------------------------------------------------------
+# OPT shapes at full size (inputs generated by torch's device RNG, copied to
+# the host for the oracle)
+
+
+def test_opt67b_full(dv):
+    case = make_case(CFG["opt6.7b"], gen_device="cuda", norm_affine=False)
+    g = run_gpu_layer(dv, case)
+    check_layer_parity(case, g)
+
+
+@pytest.mark.parametrize("B", [1, 8])
+def test_opt66b_full(dv, B):
+    case = make_case(CFG["opt66b"], B=B, gen_device="cuda", norm_affine=False)
+    g = run_gpu_layer(dv, case)
+    check_layer_parity(case, g)
+    if B == 8:
+        assert CFG["opt66b"].k_neurons < g["u_n"].size <= 8 * CFG["opt66b"].k_neurons
+
+
+def test_opt175b_full(dv):
+    case = make_case(CFG["opt175b"], gen_device="cuda", norm_affine=False)
+    g = run_gpu_layer(dv, case)
+    out = check_layer_parity(case, g)
+    assert g["u_n"].size == 2458 and g["u_h"].size == 20
+    print("opt175b parity", out)

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdv.so")
-SOURCES = ["dv_abi.cu", "dv_rowdot.cu", "dv_colacc.cu", "dv_attn.cu"]
+SOURCES = ["dv_abi.cu", "dv_rowdot.cu", "dv_colacc.cu", "dv_attn.cu", "dv_select.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

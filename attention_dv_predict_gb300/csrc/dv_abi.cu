@@ -52,6 +52,9 @@ dv_status check_desc(const dv_layer_desc *D)
     // activations of one row must fit the row-dot kernel's shared memory
     if ((size_t)D->d_model * 4 > kSmemCap || (size_t)D->pred_rank * 4 > kSmemCap)
         return DV_ERR_UNSUPPORTED;
+    // one warp selects the heads; the neuron selection's bitmaps fit one CTA
+    if (D->n_heads > 256 || D->d_ffn > (1 << 19))
+        return DV_ERR_UNSUPPORTED;
     if ((long long)3 * D->n_heads * dh > (1 << 24) || D->d_ffn > (1 << 24) ||
         (long long)D->kv_cap * dh > (1LL << 31) / 4)
         return DV_ERR_UNSUPPORTED;
@@ -101,6 +104,8 @@ dv_status make_launch(void *stream, void *const *events, int n_events, Launch *L
     if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         nsm <= 0)
         return DV_ERR_CUDA;
+    if (nsm * kWarpsPerBlock > kMaxWarps)
+        return DV_ERR_UNSUPPORTED;
     L->st = static_cast<cudaStream_t>(stream);
     L->nsm = nsm;
     L->events = events;
@@ -109,50 +114,49 @@ dv_status make_launch(void *stream, void *const *events, int n_events, Launch *L
     return DV_OK;
 }
 
-int choose_nseg(int rows, int K, int epc, int total_warps)
-{
-    const int chunks = K / epc;
-    int nseg = ceil_div(4LL * total_warps, rows > 0 ? rows : 1);
-    if (nseg > kMaxSeg)
-        nseg = kMaxSeg;
-    while (nseg > 1 && (chunks % nseg != 0 || chunks / nseg < 64))
-        --nseg;
-    return nseg < 1 ? 1 : nseg;
-}
-
-int choose_groups(int rows, int d, int epc, int total_warps)
-{
-    const int S = ceil_div(d, 32 * epc);
-    int G = ceil_div(total_warps, S);
-    const int gmax_rows = ceil_div(rows, 8);
-    if (G > gmax_rows)
-        G = gmax_rows;
-    if (G > kMaxColGroups)
-        G = kMaxColGroups;
-    return G < 1 ? 1 : G;
-}
-
 template <typename P>
 P *at(void *ws, size_t off) { return reinterpret_cast<P *>(static_cast<char *>(ws) + off); }
 
 // ---------------------------------------------------------------------------
-// The three blocks of the decode step.
+// The blocks of the decode step.  Every launch after the first of a call is
+// a programmatic dependent launch (the kernels wait for their inputs with
+// griddepcontrol.wait); the first one is ordered normally after prior work.
 
-dv_status run_predict(const dv_layer_desc &D, const dv_layer_weights &w, const float *xp, int B,
-                      int kh, int kn, const dv_selection &sel, float *sh_user, float *sn_user,
-                      void *ws, const WsLayout &L, Launch &lc)
+NeuronSel make_neuron_sel(const dv_layer_desc &D, int B, int kn, const dv_selection &sel,
+                          void *ws, const WsLayout &L)
+{
+    NeuronSel ns;
+    std::memset(&ns, 0, sizeof(ns));
+    ns.s_n = at<float>(ws, L.s_n);
+    ns.B = B;
+    ns.N = D.d_ffn;
+    ns.k = kn;
+    ns.hist = at<int>(ws, L.hist);
+    ns.rowbits = at<unsigned>(ws, L.nbits);
+    ns.cand_key = at<unsigned>(ws, L.cand_key);
+    ns.cand_idx = at<int>(ws, L.cand_idx);
+    ns.cand_cnt = at<int>(ws, L.cand_cnt);
+    ns.idx_n = sel.idx_n;
+    ns.u_n = sel.u_n;
+    ns.n_u_n = sel.n_u_n;
+    ns.status = at<int>(ws, L.ctl);
+    return ns;
+}
+
+// PRED1 (head scores, low-rank factor u) and PRED2 (neuron scores +
+// first-digit histogram).  PRED1 is the first launch of the call.
+dv_status run_scores(const dv_layer_desc &D, const dv_layer_weights &w, const float *xp, int B,
+                     float *sh_user, float *sn_user, void *ws, const WsLayout &L, Launch &lc)
 {
     const int d = D.d_model, H = D.n_heads, N = D.d_ffn, r = D.pred_rank;
-    const int epc = (int)(16 / esize(D.dtype));
-    const int total_warps = lc.nsm * kWarpsPerBlock;
     int *ctl = at<int>(ws, L.ctl);
 
     RowArgs a;
     std::memset(&a, 0, sizeof(a));
+    int nb = rowdot_nb(B, d, RK_PRED1);
     a.K = d;
+    a.geo = rowdot_geometry(d, D.dtype, nb);
     a.max_rows = H + r;
-    a.nseg = choose_nseg(a.max_rows, d, epc, total_warps);
-    a.seglen = d / a.nseg;
     a.B = B;
     a.x = xp;
     a.x_ld = d;
@@ -164,67 +168,57 @@ dv_status run_predict(const dv_layer_desc &D, const dv_layer_weights &w, const f
     a.user_scores = sh_user;
     a.part = at<float>(ws, L.part_pred1);
     a.rowcnt = at<int>(ws, L.cnt_pred1);
-    a.topk_n = H;
-    a.topk_k = kh;
-    a.idx_out = sel.idx_h;
-    a.u_out = sel.u_h;
-    a.n_u_out = sel.n_u_h;
-    a.done = ctl + 1;
     a.status = ctl;
-    int nb = rowdot_nb(B, d, RK_PRED1);
     dim3 grid(lc.nsm, ceil_div(B, nb));
     dv_status s = lc.mark();
     if (s)
         return s;
-    if (launch_rowdot(RK_PRED1, D.dtype, nb, a, grid, rowdot_smem(RK_PRED1, nb, d, H), lc.st,
+    if (launch_rowdot(RK_PRED1, D.dtype, nb, a, grid, rowdot_smem(RK_PRED1, nb, d), lc.st,
                       false) != cudaSuccess)
         return DV_ERR_CUDA;
 
     RowArgs b2;
     std::memset(&b2, 0, sizeof(b2));
+    nb = rowdot_nb(B, r, RK_PRED2);
     b2.K = r;
+    b2.geo = rowdot_geometry(r, D.dtype, nb);
     b2.max_rows = N;
-    b2.nseg = 1;
-    b2.seglen = r;
     b2.B = B;
     b2.x = at<float>(ws, L.u);
     b2.x_ld = r;
     b2.w0 = w.pred_b;
     b2.out0 = at<float>(ws, L.s_n);
     b2.user_scores = sn_user;
-    b2.topk_n = N;
-    b2.topk_k = kn;
     b2.hist = at<int>(ws, L.hist);
-    b2.idx_out = sel.idx_n;
-    b2.u_out = sel.u_n;
-    b2.n_u_out = sel.n_u_n;
-    b2.done = ctl + 2;
+    b2.part = at<float>(ws, L.part_pred1);
+    b2.rowcnt = at<int>(ws, L.cnt_pred1);
     b2.status = ctl;
-    nb = rowdot_nb(B, r, RK_PRED2);
     grid = dim3(lc.nsm, ceil_div(B, nb));
     if ((s = lc.mark()))
         return s;
-    if (launch_rowdot(RK_PRED2, D.dtype, nb, b2, grid, rowdot_smem(RK_PRED2, nb, r, N), lc.st,
-                      false) != cudaSuccess)
+    if (launch_rowdot(RK_PRED2, D.dtype, nb, b2, grid, rowdot_smem(RK_PRED2, nb, r), lc.st,
+                      true) != cudaSuccess)
         return DV_ERR_CUDA;
     return DV_OK;
 }
 
+// Attention block.  Fused mode (fused != nullptr): the QKV kernel selects the
+// heads itself and runs the neuron pass; the attention kernel's CTA 0
+// finishes the neuron selection.  first: this is the call's first launch.
 dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const float *x, int B,
                    const int32_t *u_h, const int32_t *n_u_h, int max_u_h, void *kc, void *vc,
-                   int kv_len, float *h1, void *ws, const WsLayout &L, Launch &lc)
+                   int kv_len, float *h1, void *ws, const WsLayout &L, Launch &lc, bool first,
+                   const dv_selection *fused, int k_heads, const NeuronSel *ns)
 {
     const int d = D.d_model, H = D.n_heads, dh = D.head_dim;
-    const int epc = (int)(16 / esize(D.dtype));
-    const int total_warps = lc.nsm * kWarpsPerBlock;
     int *ctl = at<int>(ws, L.ctl);
 
     RowArgs a;
     std::memset(&a, 0, sizeof(a));
+    int nb = rowdot_nb(B, d, RK_QKV);
     a.K = d;
+    a.geo = rowdot_geometry(d, D.dtype, nb);
     a.max_rows = 3 * max_u_h * dh;
-    a.nseg = choose_nseg(a.max_rows, d, epc, total_warps);
-    a.seglen = d / a.nseg;
     a.B = B;
     a.n_sel = n_u_h;
     a.max_sel = max_u_h;
@@ -249,13 +243,22 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     a.part = at<float>(ws, L.part_qkv);
     a.rowcnt = at<int>(ws, L.cnt_qkv);
     a.status = ctl;
-    int nb = rowdot_nb(B, d, RK_QKV);
+    if (fused) {
+        a.head_sel = 1;
+        a.s_h = at<float>(ws, L.s_h);
+        a.k_h = k_heads;
+        a.idx_h_out = fused->idx_h;
+        a.u_h_out = fused->u_h;
+        a.n_u_h_out = fused->n_u_h;
+        a.neuron_pass = 1;
+        a.ns = *ns;
+    }
     dim3 grid(lc.nsm, ceil_div(B, nb));
     dv_status s = lc.mark();
     if (s)
         return s;
-    if (launch_rowdot(RK_QKV, D.dtype, nb, a, grid, rowdot_smem(RK_QKV, nb, d, 0), lc.st,
-                      false) != cudaSuccess)
+    if (launch_rowdot(RK_QKV, D.dtype, nb, a, grid, rowdot_smem(RK_QKV, nb, d), lc.st, !first) !=
+        cudaSuccess)
         return DV_ERR_CUDA;
 
     AttnArgs t;
@@ -272,22 +275,29 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     t.kc = kc;
     t.vc = vc;
     const int L1 = kv_len + 1;
-    const int want = ceil_div(2LL * total_warps, (long long)B * max_u_h);
-    int split_len = ceil_div(L1, want < 1 ? 1 : want);
-    if (split_len < kAttnMinSplit)
-        split_len = kAttnMinSplit;
-    t.split_len = split_len;
-    t.splits = ceil_div(L1, split_len);
-    if (t.splits > L.attn_splits_max)
-        return DV_ERR_WORKSPACE;
+    const int attn_ctas = fused ? lc.nsm - 1 : lc.nsm;
+    // chunks per (batch row, head): enough CTAs to cover the SMs once
+    int chunks = attn_ctas / (B * max_u_h);
+    if (chunks < 1)
+        chunks = 1;
+    if (chunks > L1)
+        chunks = L1;
+    if (chunks > kMaxAttnChunks)
+        chunks = kMaxAttnChunks;
+    t.splits = chunks;
+    t.split_len = ceil_div(L1, chunks);
     t.part = at<float>(ws, L.attn_part);
     t.cnt = at<int>(ws, L.attn_cnt);
     t.o = at<float>(ws, L.o);
     t.status = ctl;
+    if (fused) {
+        t.neuron_final = 1;
+        t.ns = *ns;
+    }
     const int lpk = (int)((size_t)dh * esize(D.dtype) / 16);
     if ((s = lc.mark()))
         return s;
-    if (launch_attn(D.dtype, lpk, t, dim3(lc.nsm), lc.st, false) != cudaSuccess)
+    if (launch_attn(D.dtype, lpk, t, dim3(lc.nsm), lc.st, true) != cudaSuccess)
         return DV_ERR_CUDA;
 
     ColArgs c;
@@ -305,14 +315,13 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     c.res = x;
     c.bias = w.b_o;
     c.out = h1;
-    c.G = choose_groups(max_u_h * dh, d, epc, total_warps);
     c.part = at<float>(ws, L.cpart_o);
     c.cnt = at<int>(ws, L.ccnt_o);
     c.status = ctl;
     nb = colacc_nb(B);
     if ((s = lc.mark()))
         return s;
-    if (launch_colacc(CK_OPROJ, D.dtype, nb, c, dim3(lc.nsm, ceil_div(B, nb)), lc.st, false) !=
+    if (launch_colacc(CK_OPROJ, D.dtype, nb, c, dim3(lc.nsm, ceil_div(B, nb)), lc.st, true) !=
         cudaSuccess)
         return DV_ERR_CUDA;
     return DV_OK;
@@ -320,19 +329,17 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
 
 dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float *h1, int B,
                   const int32_t *u_n, const int32_t *n_u_n, int max_u_n, float *y, void *ws,
-                  const WsLayout &L, Launch &lc)
+                  const WsLayout &L, Launch &lc, bool first)
 {
     const int d = D.d_model, N = D.d_ffn;
-    const int epc = (int)(16 / esize(D.dtype));
-    const int total_warps = lc.nsm * kWarpsPerBlock;
     int *ctl = at<int>(ws, L.ctl);
 
     RowArgs a;
     std::memset(&a, 0, sizeof(a));
+    int nb = rowdot_nb(B, d, RK_FC1);
     a.K = d;
+    a.geo = rowdot_geometry(d, D.dtype, nb);
     a.max_rows = max_u_n;
-    a.nseg = choose_nseg(a.max_rows, d, epc, total_warps);
-    a.seglen = d / a.nseg;
     a.B = B;
     a.n_sel = n_u_n;
     a.max_sel = max_u_n;
@@ -350,12 +357,11 @@ dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float
     a.part = at<float>(ws, L.part_fc1);
     a.rowcnt = at<int>(ws, L.cnt_fc1);
     a.status = ctl;
-    int nb = rowdot_nb(B, d, RK_FC1);
     dv_status s = lc.mark();
     if (s)
         return s;
     if (launch_rowdot(RK_FC1, D.dtype, nb, a, dim3(lc.nsm, ceil_div(B, nb)),
-                      rowdot_smem(RK_FC1, nb, d, 0), lc.st, false) != cudaSuccess)
+                      rowdot_smem(RK_FC1, nb, d), lc.st, !first) != cudaSuccess)
         return DV_ERR_CUDA;
 
     ColArgs c;
@@ -373,14 +379,13 @@ dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float
     c.res = h1;
     c.bias = w.b2;
     c.out = y;
-    c.G = choose_groups(max_u_n, d, epc, total_warps);
     c.part = at<float>(ws, L.cpart_2);
     c.cnt = at<int>(ws, L.ccnt_2);
     c.status = ctl;
     nb = colacc_nb(B);
     if ((s = lc.mark()))
         return s;
-    if (launch_colacc(CK_FC2, D.dtype, nb, c, dim3(lc.nsm, ceil_div(B, nb)), lc.st, false) !=
+    if (launch_colacc(CK_FC2, D.dtype, nb, c, dim3(lc.nsm, ceil_div(B, nb)), lc.st, true) !=
         cudaSuccess)
         return DV_ERR_CUDA;
     return DV_OK;
@@ -429,13 +434,13 @@ dv_status layer_decode_impl(const dv_layer_desc *desc, const dv_layer_weights *w
     float *h1p = h1 ? h1 : at<float>(ws, L.h1);
     const int max_u_h = batch * k_heads < D.n_heads ? batch * k_heads : D.n_heads;
     const int max_u_n = batch * k_neurons < D.d_ffn ? batch * k_neurons : D.d_ffn;
-    if ((s = run_predict(D, *w, x_pred ? x_pred : x, batch, k_heads, k_neurons, *sel, nullptr,
-                         nullptr, ws, L, lc)))
+    const NeuronSel ns = make_neuron_sel(D, batch, k_neurons, *sel, ws, L);
+    if ((s = run_scores(D, *w, x_pred ? x_pred : x, batch, nullptr, nullptr, ws, L, lc)))
         return s;
     if ((s = run_attn(D, *w, x, batch, sel->u_h, sel->n_u_h, max_u_h, kc, vc, kv_len, h1p, ws, L,
-                      lc)))
+                      lc, false, sel, k_heads, &ns)))
         return s;
-    if ((s = run_mlp(D, *w, h1p, batch, sel->u_n, sel->n_u_n, max_u_n, y, ws, L, lc)))
+    if ((s = run_mlp(D, *w, h1p, batch, sel->u_n, sel->n_u_n, max_u_n, y, ws, L, lc, false)))
         return s;
     if ((s = lc.mark()))
         return s;
@@ -452,7 +457,7 @@ bool ws_layout(const dv_layer_desc &D, int B, WsLayout *L)
         return false;
     const size_t d = D.d_model, H = D.n_heads, dh = D.head_dim, N = D.d_ffn, r = D.pred_rank;
     const size_t bp = (size_t)batch_pad(B);
-    const size_t splits = (size_t)ceil_div(D.kv_cap, kAttnMinSplit);
+    const size_t splits = (size_t)kMaxAttnChunks;
     const size_t S = (size_t)ceil_div(D.d_model, 32 * (int)(16 / esize(D.dtype)));
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -472,14 +477,16 @@ bool ws_layout(const dv_layer_desc &D, int B, WsLayout *L)
     L->o = take((size_t)B * H * dh * 4);
     L->h1 = take((size_t)B * d * 4);
     L->act = take((size_t)B * N * 4);
-    L->part_pred1 = take(bp * (H + r) * kMaxSeg * 4);
-    L->part_qkv = take(bp * 3 * H * dh * kMaxSeg * 4);
-    L->part_fc1 = take(bp * N * kMaxSeg * 4);
-    L->cnt_pred1 = take(bp * (H + r) * 4);
+    L->part_pred1 = take(bp * kMaxWarps * 2 * 4);
+    L->part_qkv = take(bp * kMaxWarps * 2 * 4);
+    L->part_fc1 = take(bp * kMaxWarps * 2 * 4);
+    L->cnt_pred1 = take(bp * (H + r > N ? H + r : N) * 4);
     L->cnt_qkv = take(bp * 3 * H * dh * 4);
     L->cnt_fc1 = take(bp * N * 4);
-    L->cpart_o = take(bp * kMaxColGroups * d * 4);
-    L->cpart_2 = take(bp * kMaxColGroups * d * 4);
+    // column kernel: two partial slots per CTA, one column block each
+    const size_t cb_max = (size_t)colacc_block_cols(D.dtype, 1) * 2;  // NB x block columns
+    L->cpart_o = take(bp * (kMaxWarps / kWarpsPerBlock) * 2 * cb_max * 4);
+    L->cpart_2 = take(bp * (kMaxWarps / kWarpsPerBlock) * 2 * cb_max * 4);
     L->ccnt_o = take(bp * S * 4);
     L->ccnt_2 = take(bp * S * 4);
     L->stage_x = take((size_t)B * d * 4);
@@ -491,6 +498,10 @@ bool ws_layout(const dv_layer_desc &D, int B, WsLayout *L)
     L->sel_n_u_h = take(4);
     L->sel_u_n = take(N * 4);
     L->sel_n_u_n = take(4);
+    L->nbits = take((size_t)B * ((N + 31) / 32) * 4);
+    L->cand_key = take((size_t)B * kTopkCand * 4);
+    L->cand_idx = take((size_t)B * kTopkCand * 4);
+    L->cand_cnt = take((size_t)B * 4);
     L->total = off;
     L->bpad = (int)bp;
     L->attn_splits_max = (int)splits;
@@ -575,9 +586,19 @@ int dv_predict_topk(const dv_layer_desc *desc, const dv_layer_weights *w, const 
     Launch lc;
     if ((s = make_launch(stream, nullptr, 0, &lc)))
         return s;
-    if ((s = run_predict(D, *w, x_pred, batch, k_heads, k_neurons, *sel, scores_h, scores_n, ws,
-                         L, lc)))
+    if ((s = run_scores(D, *w, x_pred, batch, scores_h, scores_n, ws, L, lc)))
         return s;
+    SelectArgs sa;
+    std::memset(&sa, 0, sizeof(sa));
+    sa.s_h = at<float>(ws, L.s_h);
+    sa.H = D.n_heads;
+    sa.k_h = k_heads;
+    sa.idx_h = sel->idx_h;
+    sa.u_h = sel->u_h;
+    sa.n_u_h = sel->n_u_h;
+    sa.ns = make_neuron_sel(D, batch, k_neurons, *sel, ws, L);
+    if (launch_select(sa, lc.nsm, lc.st) != cudaSuccess)
+        return DV_ERR_CUDA;
     return cuda_status(cudaGetLastError());
 }
 
@@ -602,7 +623,7 @@ int dv_sparse_attn(const dv_layer_desc *desc, const dv_layer_weights *w, const f
     if ((s = make_launch(stream, nullptr, 0, &lc)))
         return s;
     if ((s = run_attn(D, *w, x, batch, u_h, n_u_h, max_u_h, k_cache, v_cache, kv_len, h1, ws, L,
-                      lc)))
+                      lc, true, nullptr, 0, nullptr)))
         return s;
     return cuda_status(cudaGetLastError());
 }
@@ -626,7 +647,7 @@ int dv_sparse_mlp(const dv_layer_desc *desc, const dv_layer_weights *w, const fl
     Launch lc;
     if ((s = make_launch(stream, nullptr, 0, &lc)))
         return s;
-    if ((s = run_mlp(D, *w, h1, batch, u_n, n_u_n, max_u_n, y, ws, L, lc)))
+    if ((s = run_mlp(D, *w, h1, batch, u_n, n_u_n, max_u_n, y, ws, L, lc, true)))
         return s;
     return cuda_status(cudaGetLastError());
 }

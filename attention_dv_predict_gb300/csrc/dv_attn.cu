@@ -7,14 +7,21 @@
 //   o = softmax(q . K[b, h, 0..kv_len]^T) . V[b, h, 0..kv_len]
 // with q already scaled by 1/sqrt(dh) and position kv_len just appended.
 //
-// The kv_len + 1 positions are cut into splits; one warp handles one
-// (b, head, split) unit.  A group of dh*sizeof(T)/16 lanes covers one key
-// row with 16-byte loads, so a warp scores 32/group keys per step, reduces
-// each dot product with xor shuffles inside its group and keeps a running
-// max / sum / weighted V (online softmax) per group.  Groups then merge by
-// butterfly shuffles, the split writes (max, sum, o) and the last split of
-// a (b, head) to arrive combines all splits in split order.
+// The kv_len + 1 positions of a (batch row, head) are cut into C chunks, one
+// CTA each, and a chunk's positions are split among the CTA's 16 warps.  A
+// group of dh*sizeof(T)/16 lanes covers one key row with 16-byte loads, so a
+// warp scores 32/group keys per step (two batches of steps in flight),
+// reduces each dot product with xor shuffles inside its group and keeps a
+// running max / sum / weighted V (online softmax) per group.  Groups merge by
+// butterfly shuffles, the warps of the CTA merge in shared memory, and the
+// last chunk of a (batch row, head) to arrive combines the C chunk records in
+// chunk order.
+//
+// In the fused decode, CTA 0 instead finishes the neuron selection
+// (dv_select.cuh, neuron_final): the selected neurons are needed only by the
+// fc1 kernel two launches later, so the selection overlaps the attention.
 #include "dv_common.cuh"
+#include "dv_select.cuh"
 
 namespace dv {
 namespace {
@@ -24,31 +31,45 @@ __global__ void __launch_bounds__(kThreads) k_attn(const AttnArgs a)
 {
     constexpr int EPC = Elem<T>::EPC;
     constexpr int KPW = 32 / LPK;  // keys per warp step
-    constexpr int UK = 4;          // warp steps in flight
+    constexpr int UK = 4;          // warp steps per batch (two batches in flight)
+    constexpr int DH = LPK * EPC;  // head dimension
+    __shared__ float wm[kWarpsPerBlock], wl[kWarpsPerBlock];
+    __shared__ __align__(16) float wo[kWarpsPerBlock][DH];
+    __shared__ int s_last;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int ks = lane / LPK, dc = lane % LPK;
-    const int dh = a.dh;
-    const int ns = min(max(*a.n_sel, 0), a.max_sel);
-    const int per_b = ns * a.splits;
-    const int units = a.B * per_b;
+    const int C = a.splits;  // chunks per (row, head)
     const int L1 = a.kv_len + 1;
     const T *Kc = static_cast<const T *>(a.kc);
     const T *Vc = static_cast<const T *>(a.vc);
-    const int nw = gridDim.x * kWarpsPerBlock;
+    pdl_wait();  // q, the appended K/V and the head union come from the previous kernel
+    pdl_launch_dependents();
+    const int ns = min(max(ld_cg(a.n_sel), 0), a.max_sel);
+    const int units = a.B * ns * C;
+    if (a.neuron_final && blockIdx.x == 0) {
+        extern __shared__ __align__(16) int fsm[];
+        __shared__ int fscr[48];
+        neuron_final(a.ns, final_smem(fsm, a.ns.N, fscr));
+        return;
+    }
+    const int cta0 = a.neuron_final ? 1 : 0;  // CTAs [cta0, gridDim.x) attend
 
-    for (int u = blockIdx.x * kWarpsPerBlock + warp; u < units; u += nw) {
-        const int b = u / per_b, rem = u - b * per_b;
-        const int j = rem / a.splits, sp = rem - j * a.splits;
-        const int h = a.sel[j];
-        if (h < 0 || h >= a.H) {
-            if (lane == 0)
+    for (int cu = blockIdx.x - cta0; cu < units; cu += gridDim.x - cta0) {
+        const int per_b = ns * C;
+        const int b = cu / per_b, rem = cu - b * per_b;
+        const int j = rem / C, c = rem - j * C;
+        const int h = ld_cg(a.sel + j);
+        if (h < 0 || h >= a.H) {  // uniform over the CTA
+            if (threadIdx.x == 0)
                 set_status(a.status, DV_ERR_DEVICE_INDEX);
             continue;
         }
-        const int p0 = sp * a.split_len, p1 = min(L1, p0 + a.split_len);
+        const int c0 = (int)((long long)L1 * c / C), c1 = (int)((long long)L1 * (c + 1) / C);
+        const int p0 = c0 + (int)((long long)(c1 - c0) * warp / kWarpsPerBlock);
+        const int p1 = c0 + (int)((long long)(c1 - c0) * (warp + 1) / kWarpsPerBlock);
         float q[EPC];
         {
-            const float *qp = a.q + ((size_t)b * a.max_sel + j) * dh + dc * EPC;
+            const float *qp = a.q + ((size_t)b * a.max_sel + j) * DH + dc * EPC;
 #pragma unroll
             for (int e = 0; e < EPC; e += 4) {
                 const float4 t = *reinterpret_cast<const float4 *>(qp + e);
@@ -58,30 +79,34 @@ __global__ void __launch_bounds__(kThreads) k_attn(const AttnArgs a)
                 q[e + 3] = t.w;
             }
         }
-        const size_t base = ((size_t)b * a.H + h) * (size_t)a.kv_cap * dh + (size_t)dc * EPC;
+        const size_t base = ((size_t)b * a.H + h) * (size_t)a.kv_cap * DH + (size_t)dc * EPC;
         float m = -INFINITY, l = 0.f, o[EPC];
 #pragma unroll
         for (int e = 0; e < EPC; ++e)
             o[e] = 0.f;
 
-        for (int pb = p0; pb < p1; pb += KPW * UK) {
-            uint4 kv[UK], vv[UK];
+        const int nbatch = (p1 - p0 + KPW * UK - 1) / (KPW * UK);
+        uint4 kc[UK], vc[UK];
+#pragma unroll
+        for (int uu = 0; uu < UK; ++uu) {
+            const int p = p0 + uu * KPW + ks;
+            kc[uu] = p < p1 ? ld_stream(Kc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
+            vc[uu] = p < p1 ? ld_stream(Vc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        for (int bt = 0; bt < nbatch; ++bt) {
+            const int pb = p0 + bt * KPW * UK;
+            uint4 kn[UK], vn[UK];
 #pragma unroll
             for (int uu = 0; uu < UK; ++uu) {
-                const int p = pb + uu * KPW + ks;
-                if (p < p1) {
-                    kv[uu] = ld_stream(Kc + base + (size_t)p * dh);
-                    vv[uu] = ld_stream(Vc + base + (size_t)p * dh);
-                } else {
-                    kv[uu] = make_uint4(0u, 0u, 0u, 0u);
-                    vv[uu] = make_uint4(0u, 0u, 0u, 0u);
-                }
+                const int p = pb + KPW * UK + uu * KPW + ks;
+                kn[uu] = p < p1 ? ld_stream(Kc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
+                vn[uu] = p < p1 ? ld_stream(Vc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
             }
 #pragma unroll
             for (int uu = 0; uu < UK; ++uu) {
                 const int p = pb + uu * KPW + ks;
                 float kf[EPC];
-                Elem<T>::unpack(kv[uu], kf);
+                Elem<T>::unpack(kc[uu], kf);
                 float dot = 0.f;
 #pragma unroll
                 for (int e = 0; e < EPC; ++e)
@@ -91,7 +116,7 @@ __global__ void __launch_bounds__(kThreads) k_attn(const AttnArgs a)
                     dot += __shfl_xor_sync(0xffffffffu, dot, off);
                 if (p < p1) {
                     float vf[EPC];
-                    Elem<T>::unpack(vv[uu], vf);
+                    Elem<T>::unpack(vc[uu], vf);
                     const float mn = fmaxf(m, dot);
                     const float sc = expf(m - mn);
                     const float pe = expf(dot - mn);
@@ -101,6 +126,11 @@ __global__ void __launch_bounds__(kThreads) k_attn(const AttnArgs a)
                         o[e] = fmaf(o[e], sc, pe * vf[e]);
                     m = mn;
                 }
+            }
+#pragma unroll
+            for (int uu = 0; uu < UK; ++uu) {
+                kc[uu] = kn[uu];
+                vc[uu] = vn[uu];
             }
         }
         // merge the key groups of the warp (butterfly: every lane ends with the total)
@@ -119,62 +149,92 @@ __global__ void __launch_bounds__(kThreads) k_attn(const AttnArgs a)
             }
             m = mn;
         }
-        float *dst = a.o + ((size_t)b * a.max_sel + j) * dh + dc * EPC;
-        if (a.splits == 1) {
-            if (ks == 0) {
-                const float inv = 1.f / l;
-#pragma unroll
-                for (int e = 0; e < EPC; ++e)
-                    dst[e] = o[e] * inv;
-            }
-            continue;
-        }
-        const int rec = kAttnRec + dh;
-        float *recs = a.part + ((size_t)b * a.max_sel + j) * a.splits * rec;
         if (ks == 0) {
-            float *r = recs + (size_t)sp * rec;
-            if (dc == 0) {
-                r[0] = m;
-                r[1] = l;
-            }
 #pragma unroll
             for (int e = 0; e < EPC; ++e)
-                r[kAttnRec + dc * EPC + e] = o[e];
+                wo[warp][dc * EPC + e] = o[e];
+        }
+        if (lane == 0) {
+            wm[warp] = m;
+            wl[warp] = l;
+        }
+        __syncthreads();
+        // combine the warps of the CTA (thread t owns dimension t)
+        float M = -INFINITY;
+        for (int w = 0; w < kWarpsPerBlock; ++w)
+            M = fmaxf(M, wm[w]);
+        float Ls = 0.f;
+        for (int w = 0; w < kWarpsPerBlock; ++w)
+            Ls += (wm[w] == -INFINITY) ? 0.f : wl[w] * expf(wm[w] - M);
+        const int t = threadIdx.x;
+        float Ot = 0.f;
+        if (t < DH)
+            for (int w = 0; w < kWarpsPerBlock; ++w)
+                Ot += (wm[w] == -INFINITY) ? 0.f : wo[w][t] * expf(wm[w] - M);
+        float *dst = a.o + ((size_t)b * a.max_sel + j) * DH;
+        if (C == 1) {
+            if (t < DH)
+                dst[t] = Ot / Ls;
+            __syncthreads();
+            continue;
+        }
+        const int rec = kAttnRec + DH;
+        float *recs = a.part + ((size_t)b * a.max_sel + j) * C * rec;
+        if (t < DH)
+            recs[(size_t)c * rec + kAttnRec + t] = Ot;
+        if (t == 0) {
+            recs[(size_t)c * rec] = M;
+            recs[(size_t)c * rec + 1] = Ls;
         }
         __threadfence();
-        __syncwarp();
-        int last = 0;
+        __syncthreads();
         int *cnt = a.cnt + (size_t)b * a.max_sel + j;
-        if (lane == 0)
-            last = (atomicAdd(cnt, 1) == a.splits - 1);
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (!last)
-            continue;
-        __threadfence();
-        if (ks == 0) {
-            float M = -INFINITY;
-            for (int s = 0; s < a.splits; ++s)
-                M = fmaxf(M, __ldcg(recs + (size_t)s * rec));
-            float Ls = 0.f, O[EPC];
-#pragma unroll
-            for (int e = 0; e < EPC; ++e)
-                O[e] = 0.f;
-            for (int s = 0; s < a.splits; ++s) {
-                const float *r = recs + (size_t)s * rec;
-                const float w = expf(__ldcg(r) - M);
-                Ls = fmaf(__ldcg(r + 1), w, Ls);
-#pragma unroll
-                for (int e = 0; e < EPC; ++e)
-                    O[e] = fmaf(__ldcg(r + kAttnRec + dc * EPC + e), w, O[e]);
+        if (t == 0)
+            s_last = (atomicAdd(cnt, 1) == C - 1);
+        __syncthreads();
+        if (s_last) {
+            __threadfence();
+            if (t < DH) {
+                float MM = -INFINITY;
+                for (int cc = 0; cc < C; ++cc)
+                    MM = fmaxf(MM, __ldcg(recs + (size_t)cc * rec));
+                float LL = 0.f, OO = 0.f;
+                for (int cc = 0; cc < C; ++cc) {
+                    const float *r = recs + (size_t)cc * rec;
+                    const float w = expf(__ldcg(r) - MM);
+                    LL = fmaf(__ldcg(r + 1), w, LL);
+                    OO = fmaf(__ldcg(r + kAttnRec + t), w, OO);
+                }
+                dst[t] = OO / LL;
             }
-            const float inv = 1.f / Ls;
-#pragma unroll
-            for (int e = 0; e < EPC; ++e)
-                dst[e] = O[e] * inv;
+            if (t == 0)
+                *cnt = 0;
         }
-        if (lane == 0)
-            *cnt = 0;
+        __syncthreads();
     }
+}
+
+template <typename T, int LPK>
+cudaError_t launch_attn_one(const AttnArgs &a, cudaLaunchConfig_t &cfg)
+{
+    auto kern = k_attn<T, LPK>;
+    // shared-memory opt-in once per device (launches may later be captured)
+    static bool configured[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap);
+        if (e != cudaSuccess)
+            return e;
+        configured[dev] = true;
+    }
+    if (cfg.dynamicSmemBytes > kSmemCap)
+        return cudaErrorInvalidValue;
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 template <typename T>
@@ -183,7 +243,7 @@ cudaError_t dispatch_lpk(int lpk, const AttnArgs &a, dim3 grid, cudaStream_t st,
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = a.neuron_final ? neuron_final_smem_bytes(a.ns.N) : 0;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -191,12 +251,12 @@ cudaError_t dispatch_lpk(int lpk, const AttnArgs &a, dim3 grid, cudaStream_t st,
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     switch (lpk) {
-    case 1: return cudaLaunchKernelEx(&cfg, k_attn<T, 1>, a);
-    case 2: return cudaLaunchKernelEx(&cfg, k_attn<T, 2>, a);
-    case 4: return cudaLaunchKernelEx(&cfg, k_attn<T, 4>, a);
-    case 8: return cudaLaunchKernelEx(&cfg, k_attn<T, 8>, a);
-    case 16: return cudaLaunchKernelEx(&cfg, k_attn<T, 16>, a);
-    case 32: return cudaLaunchKernelEx(&cfg, k_attn<T, 32>, a);
+    case 1: return launch_attn_one<T, 1>(a, cfg);
+    case 2: return launch_attn_one<T, 2>(a, cfg);
+    case 4: return launch_attn_one<T, 4>(a, cfg);
+    case 8: return launch_attn_one<T, 8>(a, cfg);
+    case 16: return launch_attn_one<T, 16>(a, cfg);
+    case 32: return launch_attn_one<T, 32>(a, cfg);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -5,193 +5,322 @@
 //          for LLM Inference", "2. Head-Pruned Attention Dispatch": inactive
 //          heads' output-projection weights are never read);
 //   FC2    y[b] = h1[b] + b2 + sum over selected neurons j of a[b][j] * w2T[j][:]
-//          (listing, DejaVuSparseMLP.forward_sparse, steps 3-4: the selected
-//          fc2 columns, kept transposed so each is one contiguous row).
+//          (the guide's listing, DejaVuSparseMLP.forward_sparse, steps 3-4: the
+//          selected fc2 columns, kept transposed so each is one contiguous row).
 //
-// The gathered rows are contiguous, so every warp reads whole 512-byte
-// (binary16) slices of them with 16-byte loads.  Work is split two ways:
-// column slices of 32 x 16 bytes (one per warp) and G groups of rows
-// (split-K).  Each (group, slice) unit accumulates in registers and writes a
-// partial; the last unit of a slice to arrive sums the G partials in group
-// order and adds bias and residual, so the result does not depend on
-// scheduling.
+// Work: the output columns are cut into blocks of CB columns (CB = 32 lanes
+// x P chunks of 16 bytes: 2 KB of a binary16 row).  The (block, row) pieces
+// are dealt to the CTAs of a persistent grid in contiguous, balanced ranges,
+// block-major.  Inside a CTA the warps take the rows of a block round-robin,
+// two batches of rows in flight per warp, each lane accumulating P strided
+// 16-byte chunks (every load instruction reads 512 contiguous bytes, and a
+// warp reads a whole 2 KB piece of a row at once); the 16 warps then reduce
+// in shared memory.  A block covered entirely by one CTA is finished there;
+// a block shared by several CTAs is finished by the last of them to arrive
+// (atomic count of rows), which sums their partials in CTA order -- results
+// do not depend on scheduling.
 #include "dv_common.cuh"
 
 namespace dv {
 namespace {
 
-template <typename T, int NB, int KIND>
+constexpr int kStageRows = 256;  // rows whose offsets and coefficients are staged at once
+constexpr int kMaxCover = 512;   // CTAs that may share one column block
+
+template <int KIND>
+DV_DEV long long row_offset(const ColArgs &a, int i)
+{
+    const int j = (KIND == CK_OPROJ) ? i / a.dh : i;
+    const int h = ld_cg(a.sel + j);
+    if (h < 0 || h >= a.sel_range)
+        return -1;
+    if constexpr (KIND == CK_OPROJ)
+        return ((long long)h * a.dh + (i - j * a.dh)) * a.d;
+    else
+        return (long long)h * a.d;
+}
+
+// CTA whose piece range holds piece p.
+DV_DEV int cta_of(long long total, int nc, long long p)
+{
+    return (int)(((p + 1) * nc - 1) / total);
+}
+DV_DEV long long piece_start(long long total, int nc, int c) { return total * c / nc; }
+
+template <typename T, int NB, int P>
+DV_DEV void write_out(const ColArgs &a, int b0, int col, const float (&v)[NB])
+{
+    if (col >= a.d)
+        return;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        if (b0 + b >= a.B)
+            break;
+        a.out[(size_t)(b0 + b) * a.d + col] =
+            (a.res[(size_t)(b0 + b) * a.d + col] +
+             Elem<T>::load(static_cast<const T *>(a.bias), (size_t)col)) +
+            v[b];
+    }
+}
+
+template <typename T, int NB, int KIND, int P>
 __global__ void __launch_bounds__(kThreads, 1) k_colacc(const ColArgs a)
 {
     constexpr int EPC = Elem<T>::EPC;
-    constexpr int CW = 32 * EPC;  // columns per warp slice
-    constexpr int U = 8;          // rows in flight per lane
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int R = 8 / P;            // rows per batch: 8 loads in flight per lane
+    constexpr int CB = 32 * P * EPC;    // columns per block
+    constexpr int CPT = (CB + kThreads - 1) / kThreads;  // block columns per thread
+    extern __shared__ __align__(16) float red[];         // [kWarpsPerBlock][CB]
+    __shared__ long long soff[kStageRows];
+    __shared__ float scoef[kStageRows * NB];
+    __shared__ int s_last, s_ncover;
+    __shared__ int s_cover[kMaxCover];  // partial slots of the CTAs sharing a block
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
     const int tile = blockIdx.y, b0 = tile * NB;
-    const int ns = min(max(*a.n_sel, 0), a.max_sel);
+    const int ns = min(max(ld_cg(a.n_sel), 0), a.max_sel);
     const int rows = (KIND == CK_OPROJ) ? ns * a.dh : ns;
-    const int S = (a.d + CW - 1) / CW;
-    const int G = a.G;
-    const int rg = (rows + G - 1) / G;
-    const int units = G * S;
+    const int ncb = (a.d + CB - 1) / CB;
+    const int nc = gridDim.x;
+    const long long total = (long long)ncb * rows;
     const T *W = static_cast<const T *>(a.w);
-    const int nw = gridDim.x * kWarpsPerBlock;
 
-    for (int u = blockIdx.x * kWarpsPerBlock + warp; u < units; u += nw) {
-        const int g = u / S, s = u - g * S;
-        const int r0 = min(rows, g * rg), r1 = min(rows, r0 + rg);
-        const int col = s * CW + lane * EPC;
-        const bool colok = col < a.d;
-        float acc[NB][EPC];
+    if (total == 0) {  // nothing selected: out = res + bias
+        pdl_wait();
+        pdl_launch_dependents();
+        for (int col = blockIdx.x * blockDim.x + tid; col < a.d; col += nc * blockDim.x) {
+            float z[NB];
+#pragma unroll
+            for (int b = 0; b < NB; ++b)
+                z[b] = 0.f;
+            write_out<T, NB, P>(a, b0, col, z);
+        }
+        return;
+    }
+
+    const long long p0 = piece_start(total, nc, blockIdx.x);
+    const long long p1 = piece_start(total, nc, blockIdx.x + 1);
+    const int first_cb = (int)(p0 / rows);
+    bool waited = false;  // griddepcontrol.wait done (uniform over the CTA)
+    for (long long pp = p0; pp < p1;) {
+        const int cb = (int)(pp / rows);
+        const int i0 = (int)(pp - (long long)cb * rows);
+        const int i1 = (int)min((long long)rows, i0 + (p1 - pp));
+        pp += i1 - i0;
+        float acc[NB][P * EPC];
 #pragma unroll
         for (int b = 0; b < NB; ++b)
 #pragma unroll
-            for (int e = 0; e < EPC; ++e)
+            for (int e = 0; e < P * EPC; ++e)
                 acc[b][e] = 0.f;
 
-        for (int i0 = r0; i0 < r1; i0 += 32) {
-            const int nr = min(32, r1 - i0);
-            // lane l fetches the metadata of row i0 + l: weight row offset and
-            // the row's coefficient for every batch row of the tile
-            long long off = -1;
-            float cf[NB];
-#pragma unroll
-            for (int b = 0; b < NB; ++b)
-                cf[b] = 0.f;
-            if (lane < nr) {
-                const int i = i0 + lane;
-                int wrow;
-                if constexpr (KIND == CK_OPROJ) {
-                    const int j = i / a.dh, e = i - j * a.dh;
-                    const int h = a.sel[j];
-                    wrow = (h >= 0 && h < a.sel_range) ? h * a.dh + e : -1;
-                } else {
-                    const int j = a.sel[i];
-                    wrow = (j >= 0 && j < a.sel_range) ? j : -1;
+        for (int s0 = i0; s0 < i1; s0 += kStageRows) {
+            const int s1 = min(i1, s0 + kStageRows);
+            __syncthreads();  // the previous stage is consumed
+            for (int i = s0 + tid; i < s1; i += blockDim.x) {
+                const long long off = row_offset<KIND>(a, i);
+                soff[i - s0] = off;
+                if (off < 0)
+                    set_status(a.status, DV_ERR_DEVICE_INDEX);
+            }
+            if (!waited) {
+                // the gather indices come from kernels at least two launches back;
+                // start the first rows toward L2, then wait for the coefficients
+                __syncthreads();
+                if (lane < R) {
+                    const int li = warp + kWarpsPerBlock * lane;
+                    if (s0 + li < s1 && soff[li] >= 0) {
+                        const int ncol = min(CB, a.d - cb * CB);
+                        prefetch_l2(W + soff[li] + (size_t)cb * CB, (unsigned)(ncol * sizeof(T)));
+                    }
                 }
-                if (wrow >= 0) {
-                    off = (long long)wrow * a.d;
+                pdl_wait();
+                pdl_launch_dependents();
+                waited = true;
+            }
+            for (int i = s0 + tid; i < s1; i += blockDim.x) {
+#pragma unroll
+                for (int b = 0; b < NB; ++b)
+                    scoef[(i - s0) * NB + b] =
+                        (b0 + b < a.B) ? a.coef[(size_t)(b0 + b) * a.coef_ld + i] : 0.f;
+            }
+            __syncthreads();
+            // warp w takes rows s0 + w + 16 t; R rows per batch, two batches in flight
+            const int cnt = (s1 - s0 - warp + kWarpsPerBlock - 1) / kWarpsPerBlock;
+            const int nbatch = cnt > 0 ? (cnt + R - 1) / R : 0;
+            auto load = [&](int q, uint4 (&v)[R][P], float (&c)[R][NB]) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const int t = q * R + r;
+                    const int li = warp + kWarpsPerBlock * t;  // row index within the stage
+                    const long long off = (t < cnt) ? soff[li] : -1;
+#pragma unroll
+                    for (int p = 0; p < P; ++p) {
+                        const int col = cb * CB + (lane + 32 * p) * EPC;
+                        v[r][p] = (off >= 0 && col < a.d) ? ld_stream(W + off + col)
+                                                          : make_uint4(0u, 0u, 0u, 0u);
+                    }
 #pragma unroll
                     for (int b = 0; b < NB; ++b)
-                        if (b0 + b < a.B)
-                            cf[b] = a.coef[(size_t)(b0 + b) * a.coef_ld + i];
-                } else {
-                    set_status(a.status, DV_ERR_DEVICE_INDEX);
+                        c[r][b] = (off >= 0) ? scoef[li * NB + b] : 0.f;
                 }
-            }
-            for (int rr = 0; rr < nr; rr += U) {
-                uint4 v[U];
+            };
+            uint4 vc[R][P];
+            float cc[R][NB];
+            load(0, vc, cc);
+            for (int q = 0; q < nbatch; ++q) {
+                uint4 vn[R][P];
+                float cn[R][NB];
+                load(q + 1 < nbatch ? q + 1 : nbatch, vn, cn);
 #pragma unroll
-                for (int q = 0; q < U; ++q) {
-                    const long long o = __shfl_sync(0xffffffffu, off, (rr + q) & 31);
-                    v[q] = (rr + q < nr && o >= 0 && colok)
-                               ? ld_stream(W + (size_t)o + col)
-                               : make_uint4(0u, 0u, 0u, 0u);
-                }
+                for (int r = 0; r < R; ++r)
 #pragma unroll
-                for (int q = 0; q < U; ++q) {
-                    float f[EPC];
-                    Elem<T>::unpack(v[q], f);
+                    for (int p = 0; p < P; ++p) {
+                        float f[EPC];
+                        Elem<T>::unpack(vc[r][p], f);
 #pragma unroll
-                    for (int b = 0; b < NB; ++b) {
-                        const float c = __shfl_sync(0xffffffffu, cf[b], (rr + q) & 31);
+                        for (int b = 0; b < NB; ++b)
 #pragma unroll
-                        for (int e = 0; e < EPC; ++e)
-                            acc[b][e] = fmaf(c, f[e], acc[b][e]);
+                            for (int e = 0; e < EPC; ++e)
+                                acc[b][p * EPC + e] = fmaf(cc[r][b], f[e], acc[b][p * EPC + e]);
                     }
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+#pragma unroll
+                    for (int p = 0; p < P; ++p)
+                        vc[r][p] = vn[r][p];
+#pragma unroll
+                    for (int b = 0; b < NB; ++b)
+                        cc[r][b] = cn[r][b];
                 }
             }
         }
 
-        if (G == 1) {
-            if (colok) {
+        // reduce the warps in shared memory, one batch row at a time
+        const bool whole = (i0 == 0 && i1 == rows);
+        const int slot = (cb == first_cb) ? 0 : 1;
+        float sum[CPT][NB];
 #pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    if (b0 + b >= a.B)
-                        break;
-                    const float *res = a.res + (size_t)(b0 + b) * a.d + col;
-                    float *out = a.out + (size_t)(b0 + b) * a.d + col;
+        for (int b = 0; b < NB; ++b) {
+            __syncthreads();
 #pragma unroll
-                    for (int e = 0; e < EPC; ++e)
-                        out[e] = (res[e] + Elem<T>::load(static_cast<const T *>(a.bias),
-                                                         (size_t)col + e)) +
-                                 acc[b][e];
-                }
-            }
-            continue;
-        }
-        // publish this group's partial, then let the last group of the slice reduce
-        float *pp = a.part + ((size_t)tile * G + g) * NB * a.d;
-        if (colok) {
-#pragma unroll
-            for (int b = 0; b < NB; ++b)
+            for (int p = 0; p < P; ++p)
 #pragma unroll
                 for (int e = 0; e < EPC; e += 4)
-                    *reinterpret_cast<float4 *>(pp + (size_t)b * a.d + col + e) =
-                        make_float4(acc[b][e], acc[b][e + 1], acc[b][e + 2], acc[b][e + 3]);
+                    *reinterpret_cast<float4 *>(red + warp * CB + (lane + 32 * p) * EPC + e) =
+                        make_float4(acc[b][p * EPC + e], acc[b][p * EPC + e + 1],
+                                    acc[b][p * EPC + e + 2], acc[b][p * EPC + e + 3]);
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < CPT; ++k) {
+                const int col = tid + k * kThreads;
+                float s = 0.f;
+                if (col < CB)
+                    for (int w = 0; w < kWarpsPerBlock; ++w)
+                        s += red[w * CB + col];
+                sum[k][b] = s;
+            }
         }
-        __threadfence();
-        __syncwarp();
-        int last = 0;
-        if (lane == 0)
-            last = (atomicAdd(&a.cnt[tile * S + s], 1) == G - 1);
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (!last)
+        if (whole) {
+#pragma unroll
+            for (int k = 0; k < CPT; ++k) {
+                const int col = tid + k * kThreads;
+                if (col < CB)
+                    write_out<T, NB, P>(a, b0, cb * CB + col, sum[k]);
+            }
             continue;
-        __threadfence();
-        if (colok) {
-            float sum[NB][EPC];
+        }
+        // publish this CTA's partial of block cb; the last CTA to finish the block sums them
+        float *pp_out = a.part + (((size_t)tile * nc + blockIdx.x) * 2 + slot) * NB * CB;
 #pragma unroll
-            for (int b = 0; b < NB; ++b)
-#pragma unroll
-                for (int e = 0; e < EPC; ++e)
-                    sum[b][e] = 0.f;
-            const float *base = a.part + (size_t)tile * G * NB * a.d;
-            for (int gg = 0; gg < G; ++gg) {
+        for (int k = 0; k < CPT; ++k) {
+            const int col = tid + k * kThreads;
+            if (col < CB)
 #pragma unroll
                 for (int b = 0; b < NB; ++b)
-#pragma unroll
-                    for (int e = 0; e < EPC; e += 4) {
-                        const float4 p = __ldcg(reinterpret_cast<const float4 *>(
-                            base + ((size_t)gg * NB + b) * a.d + col + e));
-                        sum[b][e] += p.x;
-                        sum[b][e + 1] += p.y;
-                        sum[b][e + 2] += p.z;
-                        sum[b][e + 3] += p.w;
-                    }
-            }
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                if (b0 + b >= a.B)
-                    break;
-                const float *res = a.res + (size_t)(b0 + b) * a.d + col;
-                float *out = a.out + (size_t)(b0 + b) * a.d + col;
-#pragma unroll
-                for (int e = 0; e < EPC; ++e)
-                    out[e] = (res[e] + Elem<T>::load(static_cast<const T *>(a.bias),
-                                                     (size_t)col + e)) +
-                             sum[b][e];
-            }
+                    pp_out[b * CB + col] = sum[k][b];
         }
-        if (lane == 0)
-            a.cnt[tile * S + s] = 0;
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) {
+            int *cntp = a.cnt + (size_t)tile * ncb + cb;
+            s_last = (atomicAdd(cntp, i1 - i0) + (i1 - i0) == rows);
+        }
+        __syncthreads();
+        if (!s_last)
+            continue;
+        __threadfence();
+        // the CTAs covering block cb and the slot each used, in CTA order
+        if (tid < 32) {
+            const int ca = cta_of(total, nc, (long long)cb * rows);
+            const int cz = cta_of(total, nc, (long long)cb * rows + rows - 1);
+            for (int c = ca + tid; c <= cz; c += 32) {
+                const long long st = piece_start(total, nc, c);
+                const bool live = st < piece_start(total, nc, c + 1);
+                const int sl = (st / rows == cb) ? 0 : 1;
+                if (c - ca < kMaxCover)
+                    s_cover[c - ca] = live ? (c * 2 + sl) : -1;
+            }
+            if (tid == 0)
+                s_ncover = min(cz - ca + 1, kMaxCover);
+        }
+        __syncthreads();
+        const int ncover = s_ncover;
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) {
+            const int col = tid + k * kThreads;
+            if (col >= CB)
+                continue;
+            float s[NB];
+#pragma unroll
+            for (int b = 0; b < NB; ++b)
+                s[b] = 0.f;
+            for (int c = 0; c < ncover; ++c) {
+                const int slot = s_cover[c];
+                if (slot < 0)
+                    continue;
+                const float *q = a.part + ((size_t)tile * nc * 2 + slot) * NB * CB;
+#pragma unroll
+                for (int b = 0; b < NB; ++b)
+                    s[b] += __ldcg(q + b * CB + col);
+            }
+            write_out<T, NB, P>(a, b0, cb * CB + col, s);
+        }
+        if (tid == 0)
+            a.cnt[(size_t)tile * ncb + cb] = 0;
     }
 }
 
 template <typename T, int NB, int KIND>
 cudaError_t launch_one(const ColArgs &a, dim3 grid, cudaStream_t st, bool pdl)
 {
+    constexpr int P = colacc_chunks<NB>();
+    constexpr int CB = 32 * P * Elem<T>::EPC;
+    const size_t smem = (size_t)kWarpsPerBlock * CB * sizeof(float);
+    auto kern = k_colacc<T, NB, KIND, P>;
+    static bool configured[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess)
+            return e;
+        configured[dev] = true;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k_colacc<T, NB, KIND>, a);
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 template <typename T, int KIND>
@@ -214,6 +343,14 @@ int colacc_nb(int B)
     while (nb < B && nb < 8)
         nb <<= 1;
     return nb;
+}
+
+int colacc_block_cols(int dtype, int nb)
+{
+    const int epc = dtype == DV_F16 ? 8 : 4;
+    const int p = nb == 1 ? colacc_chunks<1>() : nb == 2 ? colacc_chunks<2>()
+                : nb == 4 ? colacc_chunks<4>() : colacc_chunks<8>();
+    return 32 * p * epc;
 }
 
 cudaError_t launch_colacc(int kind, int dtype, int nb, const ColArgs &a, dim3 grid,

@@ -19,13 +19,21 @@ constexpr int kWarp = 32;
 // Weights and KV rows are read exactly once per call: 16-byte vector loads
 // through the non-coherent path, not allocated in L1, with a 256-byte L2
 // prefetch hint so DRAM sees whole bursts.
+// The asm is volatile so a prefetch is issued where it is written (ahead of
+// the arithmetic on the previous batch), not moved next to its first use.
 DV_DEV uint4 ld_stream(const void *p)
 {
     uint4 r;
-    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
         : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
         : "l"(p));
     return r;
+}
+
+// Ask the TMA engine to bring `bytes` (multiple of 16, 16-byte aligned) into L2.
+DV_DEV void prefetch_l2(const void *p, unsigned bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // Values written by other CTAs of the same kernel: read at L2 (bypass L1).

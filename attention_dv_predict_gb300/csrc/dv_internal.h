@@ -13,9 +13,9 @@ namespace dv {
 constexpr int kThreads = 512;                    // block size of the GEMV kernels
 constexpr int kWarpsPerBlock = kThreads / 32;
 constexpr int kTopkBins = 2048;                  // first radix digit: 11 bits
-constexpr int kMaxSeg = 4;                       // row segments of the row-dot kernel
-constexpr int kMaxColGroups = 64;                // row groups of the column kernel
-constexpr int kAttnMinSplit = 32;                // KV positions per attention split (min)
+constexpr int kMaxWarps = 8192;                  // bound on grid warps (workspace sizing)
+constexpr int kTopkCand = 4096;                  // top-k candidates kept in shared memory
+constexpr int kMaxAttnChunks = 64;               // attention chunks per (batch row, head)
 constexpr int kAttnRec = 4;                      // floats before o[] in a split record
 constexpr size_t kSmemCap = 200 * 1024;          // dynamic shared memory budget
 constexpr int kMaxDevices = 64;
@@ -24,13 +24,47 @@ enum RowKind { RK_PRED1 = 0, RK_PRED2 = 1, RK_QKV = 2, RK_FC1 = 3 };
 enum ColKind { CK_OPROJ = 0, CK_FC2 = 1 };
 
 // ---------------------------------------------------------------------------
+// Neuron top-k state shared by the kernels that compute it (workspace).
+struct NeuronSel {
+    const float *s_n;      // [B][N] scores
+    int B, N, k;
+    int *hist;             // [B][kTopkBins] first-digit histogram (zero at rest)
+    unsigned *rowbits;     // [B][ceil(N/32)] kept-set bitmaps
+    unsigned *cand_key;    // [B][kTopkCand]
+    int *cand_idx;         // [B][kTopkCand]
+    int *cand_cnt;         // [B] (zero at rest)
+    int32_t *idx_n;        // [B][k] outputs
+    int32_t *u_n, *n_u_n;
+    int *status;
+};
+
+struct SelectArgs {
+    const float *s_h;      // [B][H] head scores
+    int H, k_h;
+    int32_t *idx_h, *u_h, *n_u_h;
+    NeuronSel ns;
+};
+
+// ---------------------------------------------------------------------------
 // Row-dot kernel: out_row = dot(W[row], xs) over a list of rows, with an
-// optional norm of the activations, a per-kind epilogue and (predictor kinds)
-// a fused top-k done by the last CTA.
+// optional norm of the activations and a per-kind epilogue.
+//
+// Work geometry (rowdot_geometry): a row has `cpr` 16-byte chunks.  Long rows
+// (cpr >= 32*U) are cut into `nsu` units of `ucr` chunks each ("segment
+// mode"); short rows are packed `rpu` to a unit, one group of 32/rpu lanes per
+// row ("multi-row mode", nsu == 0, ucr == cpr).  Units are dealt to the
+// grid's warps in contiguous, balanced ranges.
+struct RowGeo {
+    int cpr;   // chunks per row
+    int ucr;   // chunks of one row handled by one lane group per unit
+    int nsu;   // units per row (segment mode), 0 in multi-row mode
+    int rpu;   // rows per unit (multi-row mode), 1 in segment mode
+    int U;     // chunks in flight per lane (template parameter of the kernel)
+};
+
 struct RowArgs {
     int K;            // row length in elements
-    int nseg;         // segments per row
-    int seglen;       // K / nseg (multiple of 16 bytes)
+    RowGeo geo;
     int B;            // batch rows
     int max_rows;     // host bound on the number of rows
     const int32_t *n_sel;  // device length of the gather list (QKV, FC1)
@@ -50,14 +84,17 @@ struct RowArgs {
     void *kc, *vc;
     int kv_len, kv_cap;
     float q_scale;
-    float *part;          // segment partials [tiles][max_rows][nseg][NB]
-    int *rowcnt;          // segment arrivals [tiles][max_rows]
-    // fused top-k
-    int topk_n, topk_k;
+    float *part;          // range-boundary partials [tiles][warps][2][NB]
+    int *rowcnt;          // segments accounted per row [tiles][max_rows], zero at rest
     int *hist;            // PRED2: first-digit histogram [B][kTopkBins], zero at rest
-    int32_t *idx_out;     // [B][topk_k]
-    int32_t *u_out, *n_u_out;
-    int *done;            // CTA arrival counter, zero at rest
+    // QKV only: select the heads in the prologue from the head scores
+    int head_sel;
+    const float *s_h;     // [B][H]
+    int k_h;
+    int32_t *idx_h_out, *u_h_out, *n_u_h_out;  // written by CTA 0
+    // QKV only: neuron selection pass over the scores after the main loop
+    int neuron_pass;
+    NeuronSel ns;
     int *status;
 };
 
@@ -77,11 +114,15 @@ struct ColArgs {
     const float *res;     // [B][d]
     const void *bias;     // [d]
     float *out;           // [B][d]
-    int G;                // row groups (split-K)
-    float *part;          // [tiles][G][NB][d]
-    int *cnt;             // [tiles][slices], zero at rest
+    float *part;          // block partials [tiles][CTAs][2][NB][block columns]
+    int *cnt;             // rows accounted per column block [tiles][blocks], zero at rest
     int *status;
 };
+
+// 16-byte chunks per lane of the column kernel (columns per block = 32 * P *
+// elements per chunk); fewer for larger batch tiles to bound registers.
+template <int NB>
+constexpr int colacc_chunks() { return NB == 1 ? 4 : (NB == 2 ? 2 : 1); }
 
 // Split-KV decode attention over the selected heads.
 struct AttnArgs {
@@ -91,17 +132,19 @@ struct AttnArgs {
     const int32_t *sel;
     const float *q;       // [B][max_sel][dh], already scaled
     const void *kc, *vc;  // [B][H][kv_cap][dh]
-    int splits, split_len;
+    int splits, split_len;  // chunks per (batch row, head) and their nominal length
     float *part;          // [B][max_sel][splits][kAttnRec + dh]
     int *cnt;             // [B][max_sel], zero at rest
     float *o;             // [B][max_sel][dh]
+    int neuron_final;     // CTA 0 finishes the neuron selection instead of attending
+    NeuronSel ns;
     int *status;
 };
 
 // ---------------------------------------------------------------------------
 // Workspace layout (byte offsets from the workspace base, 256-byte aligned).
 struct WsLayout {
-    size_t ctl;       // int[64]: [0] status, [1] done(pred1), [2] done(pred2)
+    size_t ctl;       // int[64]: [0] status
     size_t hist;      // int[B][kTopkBins]
     size_t s_h, u, s_n;
     size_t q, attn_part, attn_cnt, o;
@@ -111,6 +154,7 @@ struct WsLayout {
     size_t cpart_o, cpart_2, ccnt_o, ccnt_2;
     size_t stage_x, stage_xp, stage_y;
     size_t sel_idx_h, sel_idx_n, sel_u_h, sel_n_u_h, sel_u_n, sel_n_u_n;
+    size_t nbits, cand_key, cand_idx, cand_cnt;  // neuron selection state
     size_t total;
     int bpad;         // batch rounded up to the largest batch tile (8)
     int attn_splits_max;
@@ -125,11 +169,17 @@ cudaError_t launch_colacc(int kind, int dtype, int nb, const ColArgs &a, dim3 gr
                           cudaStream_t st, bool pdl);
 cudaError_t launch_attn(int dtype, int lanes_per_key, const AttnArgs &a, dim3 grid,
                         cudaStream_t st, bool pdl);
+// Stand-alone selection (dv_predict_topk): head select + neuron pass on `grid`
+// CTAs, then the final neuron step on one CTA.
+cudaError_t launch_select(const SelectArgs &a, int grid, cudaStream_t st);
+size_t select_final_smem(int N);
 cudaError_t launch_copy(void *dst, const void *src, size_t n16, int grid, cudaStream_t st);
 
 // Largest-batch tile each kernel family handles per CTA.
 int rowdot_nb(int B, int K, int kind);
+RowGeo rowdot_geometry(int K, int dtype, int nb);
 int colacc_nb(int B);
-size_t rowdot_smem(int kind, int nb, int K, int topk_n);
+int colacc_block_cols(int dtype, int nb);
+size_t rowdot_smem(int kind, int nb, int K);
 
 }  // namespace dv

@@ -4,43 +4,45 @@
 // product of one weight row with an activation vector:
 //   PRED1  head scores s_h = x_pred . pred_h^T and the low-rank factor
 //          u = x_pred . pred_a^T ("DejaVu Guide: Contextual Sparsity for LLM
-//          Inference", "1. Mathematical Formulation of Lookahead Predictors"),
-//          then the top-k of the heads in the last CTA;
-//   PRED2  neuron scores s_n = u . pred_b^T, then the top-k of the neurons in
-//          the last CTA (the first radix digit's histogram is built on the
-//          way by every CTA);
+//          Inference", "1. Mathematical Formulation of Lookahead Predictors");
+//   PRED2  neuron scores s_n = u . pred_b^T; every CTA adds its scores to the
+//          histogram of the keys' top 11 bits (dv_select.cuh);
 //   QKV    the selected heads' q, k, v rows on LayerNorm(x), bias, q scaling
-//          and the KV append ("2. Head-Pruned Attention Dispatch");
+//          and the KV append ("2. Head-Pruned Attention Dispatch").  In the
+//          fused decode every CTA first selects the heads itself from the
+//          head scores (one warp), and after its rows it runs its share of the
+//          neuron selection pass;
 //   FC1    the selected neurons' fc1 rows on LayerNorm(h1), bias and ReLU
-//          (listing, DejaVuSparseMLP.forward_sparse, steps 1-2).
+//          (the guide's listing, DejaVuSparseMLP.forward_sparse, steps 1-2).
 //
-// Work split: each row is cut into `nseg` equal segments; the (row, segment)
-// units are dealt round-robin to all warps of a persistent grid.  A warp
-// streams its segment with 16-byte non-allocating loads (8 in flight per
-// lane) and dots it with the activations staged once per CTA in shared
-// memory.  When a row has several segments, each writes its partial and the
-// last to arrive (atomic counter) sums them in segment order and runs the
-// epilogue, so results do not depend on scheduling.
+// Streaming: every weight byte is read once with a 16-byte non-allocating
+// load.  Rows are cut into units of at most 32*U chunks (long rows) or packed
+// several to a unit (short rows); the units are dealt to all warps of a
+// persistent grid in contiguous, balanced ranges, and each warp keeps two
+// units in flight (the next unit's loads are issued before the current one is
+// consumed).  The activations are staged once per CTA in shared memory while
+// the first weight loads are in flight.  A row split across two or more warp
+// ranges is combined by the last warp to finish it (an atomic count of the
+// row's units), which sums the partials in warp order: results do not depend
+// on scheduling.
+//
+// Programmatic dependent launch: a kernel issues whatever does not depend on
+// the previous kernel (its first weight loads, QKV's head selection and
+// LayerNorm(x)) before griddepcontrol.wait, and lets the next kernel launch
+// right after its own wait, so data two kernels back is always complete.
 #include "dv_common.cuh"
+#include "dv_select.cuh"
 
 namespace dv {
 namespace {
 
-// Position of activation element c in the staged layout.  For binary16
-// weights a 16-byte chunk holds 8 elements; the staged activations are split
-// into the low and high 4 of every chunk so each lane's two float4 reads hit
-// consecutive addresses across the warp (no bank conflicts).
-template <typename T>
-DV_DEV int xs_index(int c, int K);
-template <>
-DV_DEV int xs_index<float>(int c, int) { return c; }
-template <>
-DV_DEV int xs_index<__half>(int c, int K)
-{
-    const int ch = c >> 3, w = c & 7;
-    return (w < 4) ? (ch << 2) + w : (K >> 1) + (ch << 2) + (w - 4);
-}
+constexpr int kSelStage = 1024;  // gather indices staged in shared memory per CTA
 
+// Staged activation layout: for binary16 weights a 16-byte chunk holds 8
+// elements; the staged activations are split into the low and high 4 of
+// every chunk (two float4 arrays) so each lane's two float4 reads hit
+// consecutive addresses across the warp (no bank conflicts).  For binary32
+// weights the layout is the natural one.
 template <typename T, int NB>
 DV_DEV void fma_chunk(const uint4 &v, const float *xs, int K, int gc, float (&acc)[NB])
 {
@@ -75,129 +77,195 @@ DV_DEV void fma_chunk(const uint4 &v, const float *xs, int K, int gc, float (&ac
     }
 }
 
-// Dot of chunks [c0, c0 + nchunk) of one weight row with the staged
-// activations; lane-partial sums (reduce across the warp afterwards).
-template <typename T, int NB>
-DV_DEV void warp_dot(const T *__restrict__ w, int c0, int nchunk, const float *xs, int K,
-                     float (&acc)[NB], int lane)
+// ---------------------------------------------------------------------------
+// Activation staging: NB rows [b0, b0 + NB), normalised when asked.  A thread
+// owns up to kStageChunks 16-byte chunks of a row (EPC elements each, strided
+// by the block size) and keeps them in registers, so x, the norm gain and the
+// norm bias are each read once with all loads in flight together; the mean
+// and variance come from two block reductions over the registers.
+constexpr int kStageChunks = 4;
+
+template <typename T>
+DV_DEV void stage_chunk_store(float *dst, int K, int c, const float (&v)[Elem<T>::EPC])
 {
-    constexpr int EPC = Elem<T>::EPC;
-    constexpr int U = 8;
-    int c = lane;
-    for (; c + 32 * (U - 1) < nchunk; c += 32 * U) {
-        uint4 v[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            v[u] = ld_stream(w + (size_t)(c0 + c + 32 * u) * EPC);
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            fma_chunk<T, NB>(v[u], xs, K, c0 + c + 32 * u, acc);
-    }
-    if (c < nchunk) {  // fewer than U chunks left for this lane: one guarded batch
-        uint4 v[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            v[u] = (c + 32 * u < nchunk) ? ld_stream(w + (size_t)(c0 + c + 32 * u) * EPC)
-                                         : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (c + 32 * u < nchunk)
-                fma_chunk<T, NB>(v[u], xs, K, c0 + c + 32 * u, acc);
+    if constexpr (Elem<T>::EPC == 8) {
+        reinterpret_cast<float4 *>(dst)[c] = make_float4(v[0], v[1], v[2], v[3]);
+        reinterpret_cast<float4 *>(dst + (K >> 1))[c] = make_float4(v[4], v[5], v[6], v[7]);
+    } else {
+        reinterpret_cast<float4 *>(dst)[c] = make_float4(v[0], v[1], v[2], v[3]);
     }
 }
 
-// Stage NB activation rows [b0, b0 + NB) into shared memory, normalised when
-// the kind asks for it.  Rows past the batch are zero.
 template <typename T, int NB>
 DV_DEV void stage_acts(const RowArgs &a, float *xs, int b0, float *red)
 {
-    const int K = a.K, tid = threadIdx.x, nt = blockDim.x;
+    constexpr int EPC = Elem<T>::EPC;
+    constexpr int CQ = kStageChunks;
+    const int K = a.K, nch = K / EPC, tid = threadIdx.x, nt = blockDim.x;
+    const bool norm = a.norm_g != nullptr;
+    const bool ln = a.norm_kind == DV_LAYERNORM;
     for (int bi = 0; bi < NB; ++bi) {
         const int b = b0 + bi;
         float *dst = xs + (size_t)bi * K;
-        const bool live = b < a.B;
-        const float *src = a.x + (size_t)(live ? b : 0) * a.x_ld;
-        float mean = 0.f, inv = 1.f;
-        if (live && a.norm_g) {
-            if (a.norm_kind == DV_LAYERNORM) {
-                float s = 0.f;
-                for (int c = tid; c < K; c += nt)
-                    s += src[c];
-                mean = block_sum(s, red) / (float)K;
-                float v = 0.f;
-                for (int c = tid; c < K; c += nt) {
-                    const float t = src[c] - mean;
-                    v = fmaf(t, t, v);
-                }
-                inv = rsqrtf(block_sum(v, red) / (float)K + a.eps);
-            } else {
-                float v = 0.f;
-                for (int c = tid; c < K; c += nt)
-                    v = fmaf(src[c], src[c], v);
-                inv = rsqrtf(block_sum(v, red) / (float)K + a.eps);
-            }
+        if (b >= a.B) {
+            for (int c = tid; c < K; c += nt)
+                dst[c] = 0.f;
+            continue;
         }
-        for (int c = tid; c < K; c += nt) {
-            float v = 0.f;
-            if (live) {
-                v = src[c];
-                if (a.norm_g) {
-                    const float g = Elem<T>::load(static_cast<const T *>(a.norm_g), c);
-                    const float bb = (a.norm_kind == DV_LAYERNORM)
-                                         ? Elem<T>::load(static_cast<const T *>(a.norm_b), c)
-                                         : 0.f;
-                    v = (v - mean) * inv * g + bb;
+        const float *src = a.x + (size_t)b * a.x_ld;
+        for (int c0 = 0; c0 < nch; c0 += nt * CQ) {
+            // chunks c0 + tid + q*nt of this row (all of it when nch <= nt*CQ)
+            float v[CQ][EPC];
+            uint4 gv[CQ], bv[CQ];
+#pragma unroll
+            for (int q = 0; q < CQ; ++q) {
+                const int c = c0 + tid + q * nt;
+                const bool in = c < nch;
+#pragma unroll
+                for (int e = 0; e < EPC; e += 4) {
+                    const float4 t = in ? reinterpret_cast<const float4 *>(src + (size_t)c * EPC)[e / 4]
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[q][e] = t.x;
+                    v[q][e + 1] = t.y;
+                    v[q][e + 2] = t.z;
+                    v[q][e + 3] = t.w;
+                }
+                gv[q] = (in && norm) ? reinterpret_cast<const uint4 *>(a.norm_g)[c]
+                                     : make_uint4(0u, 0u, 0u, 0u);
+                bv[q] = (in && norm && ln) ? reinterpret_cast<const uint4 *>(a.norm_b)[c]
+                                           : make_uint4(0u, 0u, 0u, 0u);
+            }
+            float mean = 0.f, inv = 1.f;
+            if (norm) {
+                if (nch > nt * CQ) {
+                    // long rows: statistics over the whole row first (rare)
+                    float s = 0.f, ss = 0.f;
+                    for (int c = tid; c < nch; c += nt)
+                        for (int e = 0; e < EPC; ++e)
+                            s += src[(size_t)c * EPC + e];
+                    mean = ln ? block_sum(s, red) / (float)K : 0.f;
+                    for (int c = tid; c < nch; c += nt)
+                        for (int e = 0; e < EPC; ++e) {
+                            const float d = src[(size_t)c * EPC + e] - mean;
+                            ss = fmaf(d, d, ss);
+                        }
+                    inv = rsqrtf(block_sum(ss, red) / (float)K + a.eps);
+                } else {
+                    float s = 0.f;
+#pragma unroll
+                    for (int q = 0; q < CQ; ++q)
+#pragma unroll
+                        for (int e = 0; e < EPC; ++e)
+                            s += v[q][e];
+                    mean = ln ? block_sum(s, red) / (float)K : 0.f;
+                    float ss = 0.f;
+#pragma unroll
+                    for (int q = 0; q < CQ; ++q) {
+                        if (c0 + tid + q * nt >= nch)
+                            break;
+#pragma unroll
+                        for (int e = 0; e < EPC; ++e) {
+                            const float d = v[q][e] - mean;
+                            ss = fmaf(d, d, ss);
+                        }
+                    }
+                    inv = rsqrtf(block_sum(ss, red) / (float)K + a.eps);
                 }
             }
-            dst[xs_index<T>(c, K)] = v;
+#pragma unroll
+            for (int q = 0; q < CQ; ++q) {
+                const int c = c0 + tid + q * nt;
+                if (c >= nch)
+                    break;
+                if (norm) {
+                    float g[EPC], be[EPC];
+                    Elem<T>::unpack(gv[q], g);
+                    if (ln)
+                        Elem<T>::unpack(bv[q], be);
+#pragma unroll
+                    for (int e = 0; e < EPC; ++e)
+                        v[q][e] = (v[q][e] - mean) * inv * g[e] + (ln ? be[e] : 0.f);
+                }
+                stage_chunk_store<T>(dst, K, c, v[q]);
+            }
         }
     }
     __syncthreads();
 }
 
-struct Meta {
-    bool ok;
-    int t, h, e, j;
+// ---------------------------------------------------------------------------
+// Row addressing.
+struct RowRef {
+    const void *p;  // first element of the row (nullptr: invalid row)
+    int j, t, e, h;
 };
 
-template <typename T, int KIND>
-DV_DEV const T *row_ptr(const RowArgs &a, int row, Meta &m)
+DV_DEV int sel_at(const RowArgs &a, int j, const int *ssel, int sj0, int sn)
 {
-    m.ok = true;
-    m.t = m.h = m.e = m.j = 0;
+    const int o = j - sj0;
+    return (o >= 0 && o < sn) ? ssel[o] : a.sel[j];
+}
+
+template <typename T, int KIND>
+DV_DEV RowRef row_ref(const RowArgs &a, int row, const int *ssel, int sj0, int sn)
+{
+    RowRef r;
+    r.j = r.t = r.e = r.h = 0;
     const T *w0 = static_cast<const T *>(a.w0);
     if constexpr (KIND == RK_PRED1) {
-        if (row < a.split_rows)
-            return w0 + (size_t)row * a.K;
-        return static_cast<const T *>(a.w1) + (size_t)(row - a.split_rows) * a.K;
+        r.p = row < a.split_rows ? (const void *)(w0 + (size_t)row * a.K)
+                                 : (const void *)(static_cast<const T *>(a.w1) +
+                                                  (size_t)(row - a.split_rows) * a.K);
     } else if constexpr (KIND == RK_PRED2) {
-        return w0 + (size_t)row * a.K;
+        r.p = w0 + (size_t)row * a.K;
     } else if constexpr (KIND == RK_QKV) {
         const int per = 3 * a.dh;
-        const int j = row / per, rem = row - j * per;
-        m.j = j;
-        m.t = rem / a.dh;
-        m.e = rem - m.t * a.dh;
-        const int h = a.sel[j];
-        m.h = h;
-        if (h < 0 || h >= a.sel_range) {
-            m.ok = false;
-            return nullptr;
-        }
-        return w0 + (((size_t)m.t * a.H + h) * a.dh + m.e) * a.K;
+        r.j = row / per;
+        const int rem = row - r.j * per;
+        r.t = rem / a.dh;
+        r.e = rem - r.t * a.dh;
+        r.h = sel_at(a, r.j, ssel, sj0, sn);
+        r.p = (r.h >= 0 && r.h < a.sel_range)
+                  ? (const void *)(w0 + (((size_t)r.t * a.H + r.h) * a.dh + r.e) * a.K)
+                  : nullptr;
     } else {
-        const int j = a.sel[row];
-        m.h = j;
-        if (j < 0 || j >= a.sel_range) {
-            m.ok = false;
-            return nullptr;
-        }
-        return w0 + (size_t)j * a.K;
+        r.j = row;
+        r.h = sel_at(a, row, ssel, sj0, sn);
+        r.p = (r.h >= 0 && r.h < a.sel_range) ? (const void *)(w0 + (size_t)r.h * a.K) : nullptr;
+    }
+    return r;
+}
+
+template <typename T, int U>
+DV_DEV void load_unit(const RowRef &r, bool live, int coff, int ucr, int lig, int LG,
+                      uint4 (&v)[U])
+{
+    constexpr int EPC = Elem<T>::EPC;
+    const T *p = static_cast<const T *>(r.p);
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+        const int c = lig + LG * j;
+        v[j] = (live && p && c < ucr) ? ld_stream(p + (size_t)(coff + c) * EPC)
+                                      : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+template <typename T, int NB, int U>
+DV_DEV void consume_unit(const uint4 (&v)[U], bool live, int coff, int ucr, int lig, int LG,
+                         const float *xs, int K, float (&acc)[NB])
+{
+    if (!live)
+        return;
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+        const int c = lig + LG * j;
+        if (c < ucr)
+            fma_chunk<T, NB>(v[j], xs, K, coff + c, acc);
     }
 }
 
 template <typename T, int NB, int KIND>
-DV_DEV void finalize(const RowArgs &a, int row, const Meta &m, const float (&acc)[NB], int b0,
+DV_DEV void finalize(const RowArgs &a, int row, const RowRef &m, const float (&acc)[NB], int b0,
                      int *shist)
 {
 #pragma unroll
@@ -237,111 +305,225 @@ DV_DEV void finalize(const RowArgs &a, int row, const Meta &m, const float (&acc
     }
 }
 
+// Unit range of warp w: [start(w), start(w + 1)).
+DV_DEV int range_start(int units, int W, int w) { return (int)((long long)units * w / W); }
+// The warp whose range holds unit u.
+DV_DEV int warp_of(int units, int W, int u)
+{
+    return (int)((((long long)u + 1) * W - 1) / units);
+}
+
 // ---------------------------------------------------------------------------
-// Block-wide exact top-k of one row of binary32 scores (all threads of the
-// block).  Keys are order-preserving integers (score_key); a three-pass
-// radix select (11, 11, 10 bits) finds the k-th largest key T and how many
-// keys equal to T are kept; the output pass keeps every key > T and the
-// lowest-index keys == T, writing indices in ascending order.
-DV_DEV void find_bin(const int *hist, int nb, int krem, int *scr)
-{
-    const int nt = blockDim.x, tid = threadIdx.x;
-    const int per = (nb + nt - 1) / nt;
-    const int top = nb - 1 - tid * per;
-    int c = 0;
-    for (int q = 0; q < per; ++q) {
-        const int bin = top - q;
-        if (bin >= 0)
-            c += hist[bin];
-    }
-    int tot;
-    const int before = block_excl_scan(c, scr + 4, &tot);
-    if (before < krem && krem <= before + c) {
-        int acc = before;
-        for (int q = 0; q < per; ++q) {
-            const int bin = top - q;
-            if (bin < 0)
-                break;
-            const int h = hist[bin];
-            if (krem <= acc + h) {
-                scr[0] = bin;
-                scr[1] = krem - acc;
-                break;
-            }
-            acc += h;
-        }
-    }
-    __syncthreads();
-}
 
-DV_DEV void block_topk_row(const float *s, int n, int k, int *ghist, int32_t *out,
-                           unsigned *bitmap, int *hist, int *scr)
+template <typename T, int NB, int KIND, int U>
+__global__ void __launch_bounds__(kThreads, 1) k_rowdot(const RowArgs a)
 {
-    const int tid = threadIdx.x, nt = blockDim.x;
-    unsigned prefix = 0u, pmask = 0u;
-    int krem = k;
-    const int shifts[3] = {21, 10, 0};
-    const int widths[3] = {11, 11, 10};
-    for (int pass = 0; pass < 3; ++pass) {
-        const int shift = shifts[pass], nbins = 1 << widths[pass];
-        if (pass == 0 && ghist) {
-            for (int i = tid; i < nbins; i += nt) {
-                hist[i] = ld_cg(ghist + i);
-                ghist[i] = 0;  // leave the global histogram zero for the next call
+    extern __shared__ __align__(16) float smem[];
+    __shared__ float red[34];
+    __shared__ int ssel[kSelStage];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int tile = blockIdx.y, b0 = tile * NB;
+    const RowGeo g = a.geo;
+    float *xs = smem;
+    int *shist = reinterpret_cast<int *>(smem + (size_t)NB * a.K);
+
+    if constexpr (KIND == RK_PRED1) {  // the first kernel of a call: nothing to wait for
+        pdl_wait();
+        pdl_launch_dependents();
+    }
+    int rows = a.max_rows;
+    int sj0 = 0, sn = 0;  // staged gather indices: ssel[i] = sel[sj0 + i], i < sn
+    if constexpr (KIND == RK_QKV) {
+        if (a.head_sel) {
+            // select the heads from the head scores (every CTA, one warp)
+            __shared__ unsigned hbits[2 * kHeadKPL];
+            __shared__ int s_nuh;
+            if (warp == 0) {
+                const int nu = head_select(a.s_h, a.B, a.H, a.k_h, hbits, ssel, blockIdx.x == 0,
+                                           a.idx_h_out, a.u_h_out, a.n_u_h_out, lane);
+                if (lane == 0)
+                    s_nuh = nu;
             }
-        } else {
-            for (int i = tid; i < nbins; i += nt)
-                hist[i] = 0;
             __syncthreads();
-            for (int i = tid; i < n; i += nt) {
-                const unsigned key = score_key(ld_cg(s + i));
-                if ((key & pmask) == prefix)
-                    atomicAdd(&hist[(key >> shift) & (unsigned)(nbins - 1)], 1);
-            }
+            sn = min(s_nuh, a.max_sel);
+            rows = sn * 3 * a.dh;
+        } else {
+            rows = min(max(ld_cg(a.n_sel), 0), a.max_sel) * 3 * a.dh;
         }
-        __syncthreads();
-        find_bin(hist, nbins, krem, scr);
-        prefix |= (unsigned)scr[0] << shift;
-        pmask |= (unsigned)(nbins - 1) << shift;
-        krem = scr[1];
-        __syncthreads();
+    } else if constexpr (KIND == RK_FC1) {
+        rows = min(max(ld_cg(a.n_sel), 0), a.max_sel);
     }
-    const unsigned T = prefix;
-    const int need_eq = krem;
-    const int per = (n + nt - 1) / nt;
-    const int i0 = min(n, tid * per), i1 = min(n, i0 + per);
-    int gt = 0, eq = 0;
-    for (int i = i0; i < i1; ++i) {
-        const unsigned key = score_key(ld_cg(s + i));
-        gt += key > T;
-        eq += key == T;
-    }
-    int tot;
-    const int eq_before = block_excl_scan(eq, scr + 4, &tot);
-    const int take_eq = min(max(need_eq - eq_before, 0), eq);
-    int pos = block_excl_scan(gt + take_eq, scr + 4, &tot);
-    int eq_seen = 0;
-    for (int i = i0; i < i1; ++i) {
-        const unsigned key = score_key(ld_cg(s + i));
-        bool keep = key > T;
-        if (key == T) {
-            keep = eq_seen < take_eq;
-            ++eq_seen;
-        }
-        if (keep) {
-            out[pos++] = i;
-            atomicOr(&bitmap[i >> 5], 1u << (i & 31));
-        }
-    }
-    __syncthreads();
-}
+    const bool seg = g.nsu > 0;
+    const int units = seg ? rows * g.nsu : (rows + g.rpu - 1) / g.rpu;
+    const int Wt = gridDim.x * kWarpsPerBlock;
+    const int gw = blockIdx.x * kWarpsPerBlock + warp;
+    const int ub = range_start(units, Wt, gw), ue = range_start(units, Wt, gw + 1);
+    const int LG = 32 / g.rpu;
+    const int grp = lane / LG, lig = lane - grp * LG;
 
-template <int KIND, int NB>
-DV_DEV void topk_tail(const RowArgs &a, float *smem, int *shist, int b0)
-{
-    __shared__ int s_last;
-    __shared__ int scr[48];
+    // gather indices of the rows this CTA touches, staged in shared memory
+    const bool stage_sel = (KIND == RK_FC1) || (KIND == RK_QKV && !a.head_sel);
+    if (stage_sel) {
+        const int cb = range_start(units, Wt, blockIdx.x * kWarpsPerBlock);
+        const int ce = range_start(units, Wt, (blockIdx.x + 1) * kWarpsPerBlock);
+        if (ce > cb) {
+            const int r0 = seg ? cb / g.nsu : cb * g.rpu;
+            const int r1 = seg ? (ce - 1) / g.nsu : min(rows, ce * g.rpu) - 1;
+            const int j0 = (KIND == RK_QKV) ? r0 / (3 * a.dh) : r0;
+            const int j1 = (KIND == RK_QKV) ? r1 / (3 * a.dh) : r1;
+            sj0 = j0;
+            sn = min(j1 - j0 + 1, kSelStage);
+        }
+    }
+
+    // (row, segment) of the warp's first unit; later units advance incrementally
+    int r = 0, sg = 0;
+    if (ub < ue) {
+        if (seg) {
+            r = ub / g.nsu;
+            sg = ub - r * g.nsu;
+        } else {
+            r = ub * g.rpu + grp;
+        }
+    }
+    // first unit's loads go out before the activations are staged
+    uint4 cur[U];
+    RowRef rcur;
+    rcur.p = nullptr;
+    rcur.j = rcur.t = rcur.e = rcur.h = 0;
+    bool lcur = ub < ue && r < rows;
+    if (lcur)
+        rcur = row_ref<T, KIND>(a, r, ssel, sj0, stage_sel ? 0 : sn);
+    load_unit<T, U>(rcur, lcur, sg * g.ucr, g.ucr, lig, LG, cur);
+    if (stage_sel)
+        for (int i = threadIdx.x; i < sn; i += blockDim.x)
+            ssel[i] = ld_cg(a.sel + sj0 + i);
     if constexpr (KIND == RK_PRED2) {
+        for (int i = threadIdx.x; i < NB * kTopkBins; i += blockDim.x)
+            shist[i] = 0;
+    }
+    if constexpr (KIND == RK_PRED2 || KIND == RK_FC1) {  // activations come from the previous kernel
+        pdl_wait();
+        pdl_launch_dependents();
+    }
+    stage_acts<T, NB>(a, xs, b0, red);
+
+    if (seg) {
+        float acc[NB];
+#pragma unroll
+        for (int b = 0; b < NB; ++b)
+            acc[b] = 0.f;
+        int run_cov = 0;
+        const int first_row = r;
+        for (int u = ub; u < ue; ++u) {
+            const bool more = u + 1 < ue;
+            int rn = r, sgn = sg + 1;
+            if (sgn == g.nsu) {
+                sgn = 0;
+                rn = r + 1;
+            }
+            uint4 nxt[U];
+            RowRef rnext = rcur;
+            if (more && rn != r)
+                rnext = row_ref<T, KIND>(a, rn, ssel, sj0, sn);
+            load_unit<T, U>(rnext, more, sgn * g.ucr, g.ucr, lig, LG, nxt);
+            consume_unit<T, NB, U>(cur, rcur.p != nullptr, sg * g.ucr, g.ucr, lig, LG, xs, a.K,
+                                   acc);
+            ++run_cov;
+            if (!more || rn != r) {
+#pragma unroll
+                for (int b = 0; b < NB; ++b)
+                    acc[b] = warp_sum(acc[b]);
+                if (rcur.p == nullptr && lane == 0)
+                    set_status(a.status, DV_ERR_DEVICE_INDEX);
+                if (run_cov == g.nsu) {
+                    if (lane == 0 && rcur.p)
+                        finalize<T, NB, KIND>(a, r, rcur, acc, b0, shist);
+                } else {
+                    const int slot = (r == first_row) ? 0 : 1;
+                    float *pp = a.part + (((size_t)tile * Wt + gw) * 2 + slot) * NB;
+                    int *cnt = a.rowcnt + (size_t)tile * a.max_rows + r;
+                    int last = 0;
+                    if (lane == 0) {
+#pragma unroll
+                        for (int b = 0; b < NB; ++b)
+                            pp[b] = acc[b];
+                        __threadfence();
+                        last = (atomicAdd(cnt, run_cov) + run_cov == g.nsu);
+                    }
+                    last = __shfl_sync(0xffffffffu, last, 0);
+                    if (last && lane == 0) {
+                        __threadfence();
+                        float s[NB];
+#pragma unroll
+                        for (int b = 0; b < NB; ++b)
+                            s[b] = 0.f;
+                        const int wa = warp_of(units, Wt, r * g.nsu);
+                        const int wb = warp_of(units, Wt, r * g.nsu + g.nsu - 1);
+                        for (int w = wa; w <= wb; ++w) {
+                            const int st = range_start(units, Wt, w);
+                            if (st >= range_start(units, Wt, w + 1))
+                                continue;
+                            const int sl = (st / g.nsu == r) ? 0 : 1;
+                            const float *q = a.part + (((size_t)tile * Wt + w) * 2 + sl) * NB;
+#pragma unroll
+                            for (int b = 0; b < NB; ++b)
+                                s[b] += ld_cg(q + b);
+                        }
+                        if (rcur.p)
+                            finalize<T, NB, KIND>(a, r, rcur, s, b0, shist);
+                        *cnt = 0;
+                    }
+                }
+#pragma unroll
+                for (int b = 0; b < NB; ++b)
+                    acc[b] = 0.f;
+                run_cov = 0;
+            }
+#pragma unroll
+            for (int j = 0; j < U; ++j)
+                cur[j] = nxt[j];
+            rcur = rnext;
+            r = rn;
+            sg = sgn;
+        }
+    } else {
+        for (int u = ub; u < ue; ++u) {
+            const bool more = u + 1 < ue;
+            const int rn = r + g.rpu;
+            uint4 nxt[U];
+            RowRef rnext;
+            rnext.p = nullptr;
+            rnext.j = rnext.t = rnext.e = rnext.h = 0;
+            const bool lnext = more && rn < rows;
+            if (lnext)
+                rnext = row_ref<T, KIND>(a, rn, ssel, sj0, sn);
+            load_unit<T, U>(rnext, lnext, 0, g.ucr, lig, LG, nxt);
+            float acc[NB];
+#pragma unroll
+            for (int b = 0; b < NB; ++b)
+                acc[b] = 0.f;
+            consume_unit<T, NB, U>(cur, lcur && rcur.p != nullptr, 0, g.ucr, lig, LG, xs, a.K,
+                                   acc);
+#pragma unroll
+            for (int b = 0; b < NB; ++b)
+                for (int off = LG >> 1; off > 0; off >>= 1)
+                    acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], off);
+            if (lig == 0 && lcur) {
+                if (rcur.p)
+                    finalize<T, NB, KIND>(a, r, rcur, acc, b0, shist);
+                else
+                    set_status(a.status, DV_ERR_DEVICE_INDEX);
+            }
+#pragma unroll
+            for (int j = 0; j < U; ++j)
+                cur[j] = nxt[j];
+            rcur = rnext;
+            lcur = lnext;
+            r = rn;
+        }
+    }
+    if constexpr (KIND == RK_PRED2) {  // this CTA's scores into the first-digit histogram
         __syncthreads();
         for (int i = threadIdx.x; i < NB * kTopkBins; i += blockDim.x) {
             const int bi = i / kTopkBins;
@@ -350,128 +532,24 @@ DV_DEV void topk_tail(const RowArgs &a, float *smem, int *shist, int b0)
                 atomicAdd(&a.hist[(size_t)(b0 + bi) * kTopkBins + (i - bi * kTopkBins)], v);
         }
     }
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const int total = gridDim.x * gridDim.y;
-        s_last = (atomicAdd(a.done, 1) == total - 1);
-    }
-    __syncthreads();
-    if (!s_last)
-        return;
-    __threadfence();
-    int *hist = reinterpret_cast<int *>(smem);
-    unsigned *bitmap = reinterpret_cast<unsigned *>(hist + kTopkBins);
-    const int n = a.topk_n, k = a.topk_k, W = (n + 31) / 32;
-    for (int i = threadIdx.x; i < W; i += blockDim.x)
-        bitmap[i] = 0u;
-    __syncthreads();
-    for (int b = 0; b < a.B; ++b)
-        block_topk_row(a.out0 + (size_t)b * n, n, k,
-                       KIND == RK_PRED2 ? a.hist + (size_t)b * kTopkBins : nullptr,
-                       a.idx_out + (size_t)b * k, bitmap, hist, scr);
-    // union of the rows, ascending
-    const int nt = blockDim.x, tid = threadIdx.x;
-    const int per = (W + nt - 1) / nt;
-    const int w0 = min(W, tid * per), w1 = min(W, w0 + per);
-    int cnt = 0;
-    for (int w = w0; w < w1; ++w)
-        cnt += __popc(bitmap[w]);
-    int tot;
-    int pos = block_excl_scan(cnt, scr + 4, &tot);
-    for (int w = w0; w < w1; ++w) {
-        unsigned bits = bitmap[w];
-        while (bits) {
-            const int bit = __ffs(bits) - 1;
-            a.u_out[pos++] = w * 32 + bit;
-            bits &= bits - 1u;
+    if constexpr (KIND == RK_QKV) {
+        pdl_wait();  // the neuron scores and their histogram are complete
+        pdl_launch_dependents();
+        if (a.neuron_pass && tile == 0) {
+            __shared__ int sb1[DV_MAX_BATCH];
+            const int W = (a.ns.N + 31) >> 5;
+            const int w0 = (int)((long long)W * blockIdx.x / gridDim.x);
+            const int w1 = (int)((long long)W * (blockIdx.x + 1) / gridDim.x);
+            neuron_pass(a.ns, w0, w1, sb1);
         }
     }
-    if (tid == 0) {
-        *a.n_u_out = tot;
-        *a.done = 0;
-    }
-}
-
-template <typename T, int NB, int KIND>
-__global__ void __launch_bounds__(kThreads, 1) k_rowdot(const RowArgs a)
-{
-    extern __shared__ __align__(16) float smem[];
-    __shared__ float red[34];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int tile = blockIdx.y, b0 = tile * NB;
-    float *xs = smem;
-    int *shist = reinterpret_cast<int *>(smem + (size_t)NB * a.K);
-    if constexpr (KIND == RK_PRED2) {
-        for (int i = threadIdx.x; i < NB * kTopkBins; i += blockDim.x)
-            shist[i] = 0;
-    }
-    stage_acts<T, NB>(a, xs, b0, red);
-
-    int rows = a.max_rows;
-    if constexpr (KIND == RK_QKV || KIND == RK_FC1) {
-        const int ns = min(max(*a.n_sel, 0), a.max_sel);
-        rows = (KIND == RK_QKV) ? ns * 3 * a.dh : ns;
-    }
-    constexpr int EPC = Elem<T>::EPC;
-    const int segc = a.seglen / EPC;
-    const long long units = (long long)rows * a.nseg;
-    const long long nw = (long long)gridDim.x * kWarpsPerBlock;
-    for (long long u = (long long)blockIdx.x * kWarpsPerBlock + warp; u < units; u += nw) {
-        const int row = (int)(u / a.nseg), seg = (int)(u - (long long)row * a.nseg);
-        Meta m;
-        const T *wrow = row_ptr<T, KIND>(a, row, m);
-        float acc[NB];
-#pragma unroll
-        for (int b = 0; b < NB; ++b)
-            acc[b] = 0.f;
-        if (m.ok)
-            warp_dot<T, NB>(wrow, seg * segc, segc, xs, a.K, acc, lane);
-        else if (lane == 0)
-            set_status(a.status, DV_ERR_DEVICE_INDEX);
-#pragma unroll
-        for (int b = 0; b < NB; ++b)
-            acc[b] = warp_sum(acc[b]);
-        if (a.nseg == 1) {
-            if (m.ok && lane == 0)
-                finalize<T, NB, KIND>(a, row, m, acc, b0, shist);
-            continue;
-        }
-        const size_t slot = (size_t)tile * a.max_rows + row;
-        float *pp = a.part + (slot * a.nseg + seg) * NB;
-        int last = 0;
-        if (lane == 0) {
-#pragma unroll
-            for (int b = 0; b < NB; ++b)
-                pp[b] = acc[b];
-            __threadfence();
-            last = (atomicAdd(&a.rowcnt[slot], 1) == a.nseg - 1);
-        }
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last && lane == 0) {
-            __threadfence();
-            float s[NB];
-#pragma unroll
-            for (int b = 0; b < NB; ++b)
-                s[b] = 0.f;
-            const float *base = a.part + slot * a.nseg * NB;
-            for (int sg = 0; sg < a.nseg; ++sg)
-#pragma unroll
-                for (int b = 0; b < NB; ++b)
-                    s[b] += ld_cg(base + sg * NB + b);
-            if (m.ok)
-                finalize<T, NB, KIND>(a, row, m, s, b0, shist);
-            a.rowcnt[slot] = 0;
-        }
-    }
-    if constexpr (KIND == RK_PRED1 || KIND == RK_PRED2)
-        topk_tail<KIND, NB>(a, smem, shist, b0);
 }
 
 template <typename T, int NB, int KIND>
 cudaError_t launch_one(const RowArgs &a, dim3 grid, size_t smem, cudaStream_t st, bool pdl)
 {
-    auto kern = k_rowdot<T, NB, KIND>;
+    constexpr int U = NB <= 2 ? 8 : 4;
+    auto kern = k_rowdot<T, NB, KIND, U>;
     // Opt in to the shared-memory budget once per device (not per launch, so
     // later launches may be captured into a CUDA graph).
     static bool configured[kMaxDevices] = {};
@@ -488,7 +566,7 @@ cudaError_t launch_one(const RowArgs &a, dim3 grid, size_t smem, cudaStream_t st
             return e;
         configured[dev] = true;
     }
-    if (smem > kSmemCap)
+    if (smem > kSmemCap || a.geo.U != U)
         return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -531,6 +609,32 @@ cudaError_t dispatch_kind(int kind, int nb, const RowArgs &a, dim3 grid, size_t 
 
 }  // namespace
 
+RowGeo rowdot_geometry(int K, int dtype, int nb)
+{
+    RowGeo g;
+    const int epc = dtype == DV_F16 ? 8 : 4;
+    g.U = nb <= 2 ? 8 : 4;
+    const int lim = 32 * g.U;  // chunks one warp has in flight per unit
+    g.cpr = K / epc;
+    if (g.cpr >= lim) {
+        // segment mode: the largest divisor of cpr not above lim
+        int uc = lim;
+        while (uc > 1 && g.cpr % uc != 0)
+            --uc;
+        g.ucr = uc;
+        g.nsu = g.cpr / uc;
+        g.rpu = 1;
+    } else {
+        int rpu = 1;
+        while (rpu < 4 && g.cpr * rpu * 2 <= lim)
+            rpu <<= 1;
+        g.rpu = rpu;
+        g.ucr = g.cpr;
+        g.nsu = 0;
+    }
+    return g;
+}
+
 int rowdot_nb(int B, int K, int kind)
 {
     int nb = 1;
@@ -542,13 +646,9 @@ int rowdot_nb(int B, int K, int kind)
     return nb;
 }
 
-size_t rowdot_smem(int kind, int nb, int K, int topk_n)
+size_t rowdot_smem(int kind, int nb, int K)
 {
-    size_t main = (size_t)nb * K * 4 + (kind == RK_PRED2 ? (size_t)nb * kTopkBins * 4 : 0);
-    size_t tail = 0;
-    if (kind == RK_PRED1 || kind == RK_PRED2)
-        tail = ((size_t)kTopkBins + (size_t)(topk_n + 31) / 32) * 4;
-    return main > tail ? main : tail;
+    return (size_t)nb * K * 4 + (kind == RK_PRED2 ? (size_t)nb * kTopkBins * 4 : 0);
 }
 
 cudaError_t launch_rowdot(int kind, int dtype, int nb, const RowArgs &a, dim3 grid, size_t smem,

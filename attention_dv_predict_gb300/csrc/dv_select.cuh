@@ -1,0 +1,408 @@
+// dv_select.cuh -- exact top-k selection of the predictor scores, split so
+// that it never sits on the critical path of the layer decode.
+//
+// The selection rule ("DejaVu Guide: Contextual Sparsity for LLM Inference",
+// "1. Mathematical Formulation of Lookahead Predictors": Top-k of the scores;
+// the guide's listing returns the kept indices sorted): keep the k largest
+// binary32 scores of a row, ties to the lower index, indices ascending; then
+// the union over the batch rows.
+//
+// Scores are compared through order-preserving integer keys (score_key).
+//  * Heads (n <= 256): one warp runs a bitwise radix select (head_select).
+//  * Neurons: every CTA of the scoring kernel adds its scores to a histogram
+//    of the key's top 11 bits.  In a later kernel each CTA reads that
+//    histogram, finds the bin b1 holding the k-th largest key, and scans its
+//    own slice of the scores (neuron_pass): keys above b1 go straight into
+//    the row's bitmap, keys inside b1 go to a candidate list.  One CTA of the
+//    following kernel finishes the row (neuron_final): a radix select over
+//    the candidates' low 21 bits gives the k-th key T; keys > T are kept and,
+//    among keys == T, the lowest indices; the bitmaps are compacted into
+//    ascending index lists and their union.
+#pragma once
+
+#include "dv_common.cuh"
+
+namespace dv {
+
+constexpr int kHeadTopkMax = 256;   // head select handles n <= 256 (8 keys per lane)
+constexpr int kHeadKPL = kHeadTopkMax / 32;
+
+// Bitmap words (bits[q] for elements q*32 + lane) of the k largest of
+// s[0..n), ties to the lower index.  One warp; n <= kHeadTopkMax.
+DV_DEV void warp_topk_bits(const float *s, int n, int k, unsigned *bits, int lane)
+{
+    unsigned key[kHeadKPL];
+#pragma unroll
+    for (int q = 0; q < kHeadKPL; ++q) {
+        const int i = q * 32 + lane;
+        key[q] = i < n ? score_key(ld_cg(s + i)) : 0u;
+    }
+    unsigned T = 0u;
+    for (int bit = 31; bit >= 0; --bit) {
+        const unsigned cand = T | (1u << bit);
+        unsigned c = 0;
+#pragma unroll
+        for (int q = 0; q < kHeadKPL; ++q)
+            c += (q * 32 + lane < n && key[q] >= cand) ? 1u : 0u;
+        if ((int)__reduce_add_sync(0xffffffffu, c) >= k)
+            T = cand;
+    }
+    unsigned gt = 0;
+#pragma unroll
+    for (int q = 0; q < kHeadKPL; ++q)
+        gt += (q * 32 + lane < n && key[q] > T) ? 1u : 0u;
+    const int need_eq = k - (int)__reduce_add_sync(0xffffffffu, gt);
+    int seen = 0;
+#pragma unroll
+    for (int q = 0; q < kHeadKPL; ++q) {
+        const bool valid = q * 32 + lane < n;
+        const bool eq = valid && key[q] == T;
+        const unsigned m = __ballot_sync(0xffffffffu, eq);
+        const int rank = seen + __popc(m & ((1u << lane) - 1u));
+        const bool keep = valid && (key[q] > T || (eq && rank < need_eq));
+        const unsigned w = __ballot_sync(0xffffffffu, keep);
+        if (lane == 0 && q * 32 < n)
+            bits[q] = w;
+        seen += __popc(m);
+    }
+    __syncwarp();
+}
+
+// Ascending indices of the set bits of bits[0..W) written to out (one warp);
+// returns their number.
+DV_DEV int warp_compact_bits(const unsigned *bits, int W, int32_t *out, int lane)
+{
+    int off = 0;
+    for (int q = 0; q < W; ++q) {
+        const unsigned b = bits[q];
+        if (out && ((b >> lane) & 1u))
+            out[off + __popc(b & ((1u << lane) - 1u))] = q * 32 + lane;
+        off += __popc(b);
+    }
+    return off;
+}
+
+// Head selection of all B rows by one warp.  The union goes to su[] (shared
+// memory, ascending) and its length is returned.  When `write` is set the
+// per-row lists, the union and its length are also written to global memory.
+DV_DEV int head_select(const float *s_h, int B, int H, int k, unsigned *sbits, int32_t *su,
+                       bool write, int32_t *idx_h, int32_t *u_h, int32_t *n_u_h, int lane)
+{
+    const int W = (H + 31) >> 5;
+    unsigned *rowbits = sbits, *ubits = sbits + kHeadKPL;
+    if (lane < kHeadKPL)
+        ubits[lane] = 0u;
+    __syncwarp();
+    for (int b = 0; b < B; ++b) {
+        warp_topk_bits(s_h + (size_t)b * H, H, k, rowbits, lane);
+        if (lane < W)
+            ubits[lane] |= rowbits[lane];
+        __syncwarp();
+        if (write)
+            warp_compact_bits(rowbits, W, idx_h + (size_t)b * k, lane);
+        __syncwarp();
+    }
+    const int nu = warp_compact_bits(ubits, W, su, lane);
+    if (write) {
+        warp_compact_bits(ubits, W, u_h, lane);
+        if (lane == 0)
+            *n_u_h = nu;
+    }
+    __syncwarp();
+    return nu;
+}
+
+// ---------------------------------------------------------------------------
+// Neuron selection (state: NeuronSel in the workspace).
+
+// Bin of the k-th largest key and the rank left inside it, from a histogram
+// (one warp; bins scanned from the top).
+DV_DEV void warp_find_bin(const int *hist, int k, int lane, int *bin_out, int *krem_out)
+{
+    constexpr int PER = kTopkBins / 32;  // bins per lane, lane 0 owns the top ones
+    int c = 0;
+    const int top = kTopkBins - 1 - lane * PER;
+#pragma unroll 8
+    for (int q = 0; q < PER; ++q)
+        c += ld_cg(hist + top - q);
+    const int incl = warp_incl_scan(c, lane);
+    const int before = incl - c;
+    int bin = -1, krem = 0;
+    if (before < k && k <= incl) {
+        int acc = before;
+        for (int q = 0; q < PER; ++q) {
+            const int h = ld_cg(hist + top - q);
+            if (k <= acc + h) {
+                bin = top - q;
+                krem = k - acc;
+                break;
+            }
+            acc += h;
+        }
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, bin >= 0);
+    const int src = m ? __ffs(m) - 1 : 0;
+    *bin_out = __shfl_sync(0xffffffffu, bin, src);
+    *krem_out = __shfl_sync(0xffffffffu, krem, src);
+}
+
+// The pass of one CTA over bitmap words [w0, w1) of every row (all threads
+// of the CTA).  Words are whole: each belongs to exactly one CTA.
+DV_DEV void neuron_pass(const NeuronSel &ns, int w0, int w1, int *sb1 /* smem [B] */)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int W = (ns.N + 31) >> 5;
+    if (warp == 0) {
+        for (int b = 0; b < ns.B; ++b) {
+            int bin, krem;
+            warp_find_bin(ns.hist + (size_t)b * kTopkBins, ns.k, lane, &bin, &krem);
+            if (lane == 0)
+                sb1[b] = bin;
+        }
+    }
+    __syncthreads();
+    for (int b = 0; b < ns.B; ++b) {
+        const unsigned b1 = (unsigned)sb1[b];
+        const float *s = ns.s_n + (size_t)b * ns.N;
+        for (int wd = w0 + warp; wd < w1; wd += nw) {
+            const int i = wd * 32 + lane;
+            const bool in = i < ns.N;
+            const unsigned key = in ? score_key(ld_cg(s + i)) : 0u;
+            const unsigned d = key >> 21;
+            const unsigned above = __ballot_sync(0xffffffffu, in && d > b1);
+            const unsigned cand = __ballot_sync(0xffffffffu, in && d == b1);
+            if (lane == 0)
+                ns.rowbits[(size_t)b * W + wd] = above;
+            if (cand) {
+                int base = 0;
+                if (lane == 0)
+                    base = atomicAdd(ns.cand_cnt + b, __popc(cand));
+                base = __shfl_sync(0xffffffffu, base, 0);
+                if (in && d == b1) {
+                    const int pos = base + __popc(cand & ((1u << lane) - 1u));
+                    if (pos < kTopkCand) {
+                        ns.cand_key[(size_t)b * kTopkCand + pos] = key;
+                        ns.cand_idx[(size_t)b * kTopkCand + pos] = i;
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Shared-memory layout of neuron_final.
+struct FinalSmem {
+    int *hist;          // [kTopkBins]
+    unsigned *rowbits;  // [W]
+    unsigned *ubits;    // [W]
+    unsigned *ckey;     // [kTopkCand]
+    int *cidx;          // [kTopkCand]
+    int *scr;           // [48]
+};
+
+__host__ __device__ inline size_t neuron_final_smem_bytes(int N)
+{
+    const int W = (N + 31) >> 5;
+    return ((size_t)kTopkBins + 2 * (size_t)W + 2 * (size_t)kTopkCand) * 4;
+}
+
+// Block-wide: bin of the krem-th largest key of a histogram of nb bins.
+DV_DEV void block_find_bin(const int *hist, int nb, int krem, int *scr)
+{
+    const int nt = blockDim.x, tid = threadIdx.x;
+    const int per = (nb + nt - 1) / nt;
+    const int top = nb - 1 - tid * per;
+    int c = 0;
+    for (int q = 0; q < per; ++q) {
+        const int bin = top - q;
+        if (bin >= 0)
+            c += hist[bin];
+    }
+    int tot;
+    const int before = block_excl_scan(c, scr + 4, &tot);
+    if (before < krem && krem <= before + c) {
+        int acc = before;
+        for (int q = 0; q < per; ++q) {
+            const int bin = top - q;
+            if (bin < 0)
+                break;
+            const int h = hist[bin];
+            if (krem <= acc + h) {
+                scr[0] = bin;
+                scr[1] = krem - acc;
+                break;
+            }
+            acc += h;
+        }
+    }
+    __syncthreads();
+}
+
+// Ascending indices of the set bits of bits[0..W), block-wide.
+DV_DEV int block_compact_bits(const unsigned *bits, int W, int32_t *out, int *scr)
+{
+    const int nt = blockDim.x, tid = threadIdx.x;
+    const int per = (W + nt - 1) / nt;
+    const int w0 = min(W, tid * per), w1 = min(W, w0 + per);
+    int cnt = 0;
+    for (int w = w0; w < w1; ++w)
+        cnt += __popc(bits[w]);
+    int tot;
+    int pos = block_excl_scan(cnt, scr + 4, &tot);
+    for (int w = w0; w < w1; ++w) {
+        unsigned b = bits[w];
+        while (b) {
+            const int bit = __ffs(b) - 1;
+            out[pos++] = w * 32 + bit;
+            b &= b - 1u;
+        }
+    }
+    return tot;
+}
+
+// Candidates beyond the capacity (many keys share the k-th key's top 11
+// bits): finish exactly with passes over the global scores.  Slow, rare.
+DV_DEV void neuron_overflow(const float *s, int N, unsigned prefix, int krem, const FinalSmem &sm)
+{
+    const int tid = threadIdx.x, nt = blockDim.x;
+    unsigned pmask = 0xffe00000u;
+    const int shifts[2] = {10, 0};
+    const int widths[2] = {11, 10};
+    for (int pass = 0; pass < 2; ++pass) {
+        const int shift = shifts[pass], nbins = 1 << widths[pass];
+        for (int i = tid; i < nbins; i += nt)
+            sm.hist[i] = 0;
+        __syncthreads();
+        for (int i = tid; i < N; i += nt) {
+            const unsigned key = score_key(ld_cg(s + i));
+            if ((key & pmask) == prefix)
+                atomicAdd(&sm.hist[(key >> shift) & (unsigned)(nbins - 1)], 1);
+        }
+        __syncthreads();
+        block_find_bin(sm.hist, nbins, krem, sm.scr);
+        prefix |= (unsigned)sm.scr[0] << shift;
+        pmask |= (unsigned)(nbins - 1) << shift;
+        krem = sm.scr[1];
+        __syncthreads();
+    }
+    const unsigned T = prefix;
+    int seen = 0;
+    for (int base = 0; base < N; base += nt) {
+        const int i = base + tid;
+        const unsigned key = i < N ? score_key(ld_cg(s + i)) : 0u;
+        const int eq = (i < N && key == T) ? 1 : 0;
+        int tot;
+        const int rank = block_excl_scan(eq, sm.scr + 4, &tot);
+        if (i < N && (key > T || (eq && seen + rank < krem)))
+            atomicOr(&sm.rowbits[i >> 5], 1u << (i & 31));
+        seen += tot;
+    }
+    __syncthreads();
+}
+
+// Finish the selection of every row and write idx_n, u_n, n_u_n; leave the
+// histogram and candidate counts zero.  One whole CTA; smem as FinalSmem.
+DV_DEV void neuron_final(const NeuronSel &ns, const FinalSmem &sm)
+{
+    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
+    const int W = (ns.N + 31) >> 5;
+    for (int i = tid; i < W; i += nt)
+        sm.ubits[i] = 0u;
+    for (int b = 0; b < ns.B; ++b) {
+        int *ghist = ns.hist + (size_t)b * kTopkBins;
+        if (warp == 0) {
+            int bin, krem;
+            warp_find_bin(ghist, ns.k, lane, &bin, &krem);
+            if (lane == 0) {
+                sm.scr[40] = bin;
+                sm.scr[41] = krem;
+            }
+        }
+        const unsigned *gbits = ns.rowbits + (size_t)b * W;
+        for (int i = tid; i < W; i += nt)
+            sm.rowbits[i] = __ldcg(gbits + i);
+        __syncthreads();
+        const unsigned b1 = (unsigned)sm.scr[40];
+        const int krem = sm.scr[41];
+        const int ncand = __ldcg(ns.cand_cnt + b);
+        if (ncand > kTopkCand) {
+            neuron_overflow(ns.s_n + (size_t)b * ns.N, ns.N, b1 << 21, krem, sm);
+        } else {
+            for (int i = tid; i < ncand; i += nt) {
+                sm.ckey[i] = __ldcg(ns.cand_key + (size_t)b * kTopkCand + i);
+                sm.cidx[i] = __ldcg(ns.cand_idx + (size_t)b * kTopkCand + i);
+            }
+            unsigned prefix = b1 << 21, pmask = 0xffe00000u;
+            int kr = krem;
+            const int shifts[2] = {10, 0};
+            const int widths[2] = {11, 10};
+            for (int pass = 0; pass < 2; ++pass) {
+                const int shift = shifts[pass], nbins = 1 << widths[pass];
+                for (int i = tid; i < nbins; i += nt)
+                    sm.hist[i] = 0;
+                __syncthreads();
+                for (int i = tid; i < ncand; i += nt) {
+                    const unsigned key = sm.ckey[i];
+                    if ((key & pmask) == prefix)
+                        atomicAdd(&sm.hist[(key >> shift) & (unsigned)(nbins - 1)], 1);
+                }
+                __syncthreads();
+                block_find_bin(sm.hist, nbins, kr, sm.scr);
+                prefix |= (unsigned)sm.scr[0] << shift;
+                pmask |= (unsigned)(nbins - 1) << shift;
+                kr = sm.scr[1];
+                __syncthreads();
+            }
+            const unsigned T = prefix;
+            const int need_eq = kr;
+            const int n_eq = sm.hist[T & 1023u];  // candidates equal to T
+            for (int i = tid; i < ncand; i += nt) {
+                const unsigned key = sm.ckey[i];
+                bool keep = key > T;
+                if (key == T) {
+                    if (n_eq == need_eq) {
+                        keep = true;
+                    } else {
+                        const int idx = sm.cidx[i];
+                        int rank = 0;
+                        for (int q = 0; q < ncand; ++q)
+                            rank += (sm.ckey[q] == T && sm.cidx[q] < idx);
+                        keep = rank < need_eq;
+                    }
+                }
+                if (keep) {
+                    const int idx = sm.cidx[i];
+                    atomicOr(&sm.rowbits[idx >> 5], 1u << (idx & 31));
+                }
+            }
+            __syncthreads();
+        }
+        for (int i = tid; i < W; i += nt)
+            sm.ubits[i] |= sm.rowbits[i];
+        block_compact_bits(sm.rowbits, W, ns.idx_n + (size_t)b * ns.k, sm.scr);
+        // leave this row's shared state zero for the next call
+        for (int i = tid; i < kTopkBins; i += nt)
+            ghist[i] = 0;
+        if (tid == 0)
+            ns.cand_cnt[b] = 0;
+        __syncthreads();
+    }
+    const int tot = block_compact_bits(sm.ubits, W, ns.u_n, sm.scr);
+    if (tid == 0)
+        *ns.n_u_n = tot;
+}
+
+DV_DEV FinalSmem final_smem(void *base, int N, int *scr)
+{
+    const int W = (N + 31) >> 5;
+    FinalSmem sm;
+    sm.hist = static_cast<int *>(base);
+    sm.rowbits = reinterpret_cast<unsigned *>(sm.hist + kTopkBins);
+    sm.ubits = sm.rowbits + W;
+    sm.ckey = sm.ubits + W;
+    sm.cidx = reinterpret_cast<int *>(sm.ckey + kTopkCand);
+    sm.scr = scr;
+    return sm;
+}
+
+}  // namespace dv

@@ -244,6 +244,10 @@ def dv_layer_decode_traced(layer: Layer, x: torch.Tensor, k_heads: int, k_neuron
                            x_pred: Optional[torch.Tensor] = None,
                            h1: Optional[torch.Tensor] = None, stream=None):
     B = x.shape[0]
+    s = stream if stream is not None else torch.cuda.current_stream()
+    for e in events:  # torch creates the CUDA event on its first record
+        if e.cuda_event == 0:
+            e.record(s)
     arr = (C.c_void_p * len(events))(*[C.c_void_p(e.cuda_event) for e in events])
     _check("dv_layer_decode_traced", _lib.dv_layer_decode_traced(
         C.byref(layer.desc), C.byref(layer.c), _ptr(x), _ptr(x_pred), B, k_heads, k_neurons,

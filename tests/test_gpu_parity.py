@@ -262,3 +262,47 @@ def test_opt175b_full(dv):
     out = check_layer_parity(case, g)
     assert g["u_n"].size == 2458 and g["u_h"].size == 20
     print("opt175b parity", out)
+
+
+def _predict_only(dv, case):
+    desc = dv.desc_from_config(case.cfg, case.kv_cap)
+    layer = dv.Layer(desc, case.w_dev)
+    sel = dv.SelectionBuffers(desc, case.B, case.k_h, case.k_n)
+    ws = dv.Workspace(desc, case.B)
+    x = torch.from_numpy(case.x).cuda()
+    sn = torch.empty((case.B, case.cfg.d_ffn), device="cuda")
+    dv.dv_predict_topk(layer, x, case.k_h, case.k_n, sel, ws, None, sn)
+    torch.cuda.synchronize()
+    assert dv.dv_check(ws) == dv.DV_OK
+    return sel, sn
+
+
+def test_topk_all_scores_equal_takes_lowest_indices(dv):
+    """Every score ties (zero predictors): more candidates than the kernel keeps
+    in shared memory, so the exact fallback path runs; the k lowest indices win."""
+    cfg = dv_inputs.LayerConfig("ties", 264, 6, 64, 9000, 40, 5, 2, "f16",
+                                dv_inputs.Fraction(1, 18), k_heads_fixed=4)
+    case = make_case(cfg, B=2, seed=12)
+    for key in ("pred_h", "pred_b"):
+        case.w_host[key][:] = 0
+        case.w_dev[key].zero_()
+    sel, _ = _predict_only(dv, case)
+    k_n, k_h = case.k_n, case.k_h
+    assert np.array_equal(sel.idx_n.cpu().numpy(), np.tile(np.arange(k_n), (2, 1)))
+    assert np.array_equal(sel.idx_h.cpu().numpy(), np.tile(np.arange(k_h), (2, 1)))
+    u_h, u_n = sel.unions()
+    assert np.array_equal(u_n.cpu().numpy(), np.arange(k_n))
+    assert np.array_equal(u_h.cpu().numpy(), np.arange(k_h))
+
+
+@pytest.mark.parametrize("N", [1003, 4099])
+def test_topk_row_lengths_not_multiple_of_four(dv, N):
+    cfg = dv_inputs.LayerConfig("oddN", 264, 6, 64, N, 40, 5, 3, "f16",
+                                dv_inputs.Fraction(1, 10), k_heads_fixed=2)
+    case = make_case(cfg, B=3, seed=N)
+    sel, sn = _predict_only(dv, case)
+    D = oracle.desc_from_config(case.cfg, case.kv_cap)
+    p = oracle.predict(D, case.w_host, case.x, case.k_h, case.k_n)
+    assert_close(sn.cpu().numpy(), p["s_n"], "neuron scores", 1e-4, 1e-5)
+    check_topk_rows(sel.idx_n.cpu().numpy(), p["idx_n"], p["s_n"], case.k_n, "neurons")
+    check_topk_rows(sel.idx_h.cpu().numpy(), p["idx_h"], p["s_h"], case.k_h, "heads")

@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "dv_internal.h"
 
@@ -522,6 +523,8 @@ const char *dv_status_string(int status)
     case DV_ERR_TIMEOUT: return "device wait timed out";
     case DV_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case DV_ERR_DEVICE_INDEX: return "a kernel met an index outside its range";
+    case DV_ERR_SCRATCH_LIMIT:
+        return "shape and batch need more scratch than dv_predict_topk_noalloc holds";
     default: return "unknown status";
     }
 }
@@ -727,6 +730,127 @@ int dv_hbm_copy(void *dst, const void *src, size_t bytes, void *stream)
     if (s)
         return s;
     return cuda_status(launch_copy(dst, src, bytes / 16, lc.nsm * 4, lc.st));
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// dv_predict_topk_noalloc: the predictor and top-k with their scratch in a
+// fixed device array of this library instead of a caller workspace.
+//
+// Some callers cannot hand the library device memory when they predict: a
+// serving loop whose memory pool has already given all free HBM to its KV
+// cache arena, or code that must not call an allocator at that point because
+// cudaMalloc/cudaFree synchronise the device.  This entry point allocates
+// nothing: its scratch is a static device array, one per device, whose
+// address is looked up once per device.
+
+namespace {
+
+constexpr size_t kNoallocScratch = DV_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratch];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_base[kMaxDevices];
+
+// Layout inside the scratch.  The fields the kernels require to start at
+// zero (status word, first-digit histograms, candidate counters, row
+// counters) come first, in [0, *zero_bytes); every other field is written
+// before it is read.
+size_t noalloc_layout(const dv_layer_desc &D, int B, WsLayout *L, size_t *zero_bytes)
+{
+    const size_t H = D.n_heads, N = D.d_ffn, r = D.pred_rank;
+    const size_t bp = (size_t)batch_pad(B);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes, 256);
+        return o;
+    };
+    std::memset(L, 0, sizeof(*L));
+    L->ctl = take(64 * 4);
+    L->hist = take((size_t)B * kTopkBins * 4);
+    L->cand_cnt = take((size_t)B * 4);
+    L->cnt_pred1 = take(bp * (H + r > N ? H + r : N) * 4);
+    *zero_bytes = off;
+    L->s_h = take((size_t)B * H * 4);
+    L->u = take((size_t)B * r * 4);
+    L->s_n = take((size_t)B * N * 4);
+    L->part_pred1 = take(bp * kMaxWarps * 2 * 4);
+    L->nbits = take((size_t)B * ((N + 31) / 32) * 4);
+    L->cand_key = take((size_t)B * kTopkCand * 4);
+    L->cand_idx = take((size_t)B * kTopkCand * 4);
+    L->total = off;
+    L->bpad = (int)bp;
+    return off;
+}
+
+// Device address of the scratch on the current device.  The first call per
+// device looks it up (this may load the library's device code).
+dv_status noalloc_base(void **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return DV_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices)
+        return DV_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> guard(g_noalloc_mu);
+    if (!g_noalloc_base[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
+            return DV_ERR_CUDA;
+        if (reinterpret_cast<uintptr_t>(p) & 255u)
+            return DV_ERR_WORKSPACE;
+        g_noalloc_base[dev] = p;
+    }
+    *out = g_noalloc_base[dev];
+    return DV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dv_predict_topk_noalloc(const dv_layer_desc *desc, const dv_layer_weights *w,
+                            const float *x_pred, int batch, int k_heads, int k_neurons,
+                            const dv_selection *sel, float *scores_h, float *scores_n,
+                            void *stream)
+{
+    dv_status s = check_desc(desc);
+    if (s)
+        return s;
+    if (!w || !ptr_ok(w->pred_h) || !ptr_ok(w->pred_a) || !ptr_ok(w->pred_b))
+        return DV_ERR_INVALID_ARG;
+    const dv_layer_desc &D = *desc;
+    if (batch < 1 || batch > DV_MAX_BATCH || k_heads < 1 || k_heads > D.n_heads ||
+        k_neurons < 1 || k_neurons > D.d_ffn || !ptr_ok(x_pred) || !sel_ok(sel))
+        return DV_ERR_INVALID_ARG;
+    WsLayout L;
+    size_t zero_bytes = 0;
+    if (noalloc_layout(D, batch, &L, &zero_bytes) > kNoallocScratch)
+        return DV_ERR_SCRATCH_LIMIT;
+    void *ws = nullptr;
+    if ((s = noalloc_base(&ws)))
+        return s;
+    Launch lc;
+    if ((s = make_launch(stream, nullptr, 0, &lc)))
+        return s;
+    if (cudaMemsetAsync(ws, 0, zero_bytes, lc.st) != cudaSuccess)
+        return DV_ERR_CUDA;
+    if ((s = run_scores(D, *w, x_pred, batch, scores_h, scores_n, ws, L, lc)))
+        return s;
+    SelectArgs sa;
+    std::memset(&sa, 0, sizeof(sa));
+    sa.s_h = at<float>(ws, L.s_h);
+    sa.H = D.n_heads;
+    sa.k_h = k_heads;
+    sa.idx_h = sel->idx_h;
+    sa.u_h = sel->u_h;
+    sa.n_u_h = sel->n_u_h;
+    sa.ns = make_neuron_sel(D, batch, k_neurons, *sel, ws, L);
+    if (launch_select(sa, lc.nsm, lc.st) != cudaSuccess)
+        return DV_ERR_CUDA;
+    return cuda_status(cudaGetLastError());
 }
 
 }  // extern "C"

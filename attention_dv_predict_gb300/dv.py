@@ -25,7 +25,7 @@ if not os.path.exists(LIB_PATH):
 _lib = C.CDLL(LIB_PATH)
 
 DV_OK, DV_ERR_INVALID_ARG, DV_ERR_UNSUPPORTED, DV_ERR_CUDA = 0, 1, 2, 3
-DV_ERR_TIMEOUT, DV_ERR_WORKSPACE, DV_ERR_DEVICE_INDEX = 4, 5, 6
+DV_ERR_TIMEOUT, DV_ERR_WORKSPACE, DV_ERR_DEVICE_INDEX, DV_ERR_SCRATCH_LIMIT = 4, 5, 6, 7
 DV_F32, DV_F16 = 0, 1
 DV_LAYERNORM, DV_RMSNORM = 0, 1
 DV_MAX_BATCH = 32
@@ -63,6 +63,7 @@ _SIGS = {
     "dv_check": ([_P, _SZ, _P], _I),
     "dv_layer_decode_launches": ([_D, _I], _I),
     "dv_predict_topk": ([_D, _W, _P, _I, _I, _I, _S, _P, _P, _P, _SZ, _P], _I),
+    "dv_predict_topk_noalloc": ([_D, _W, _P, _I, _I, _I, _S, _P, _P, _P], _I),
     "dv_sparse_attn": ([_D, _W, _P, _I, _P, _P, _I, _P, _P, _I, _P, _P, _SZ, _P], _I),
     "dv_sparse_mlp": ([_D, _W, _P, _I, _P, _P, _I, _P, _P, _SZ, _P], _I),
     "dv_layer_decode": ([_D, _W, _P, _P, _I, _I, _I, _P, _P, _I, _S, _P, _P, _P, _SZ, _P], _I),
@@ -204,6 +205,15 @@ def dv_predict_topk(layer: Layer, x_pred: torch.Tensor, k_heads: int, k_neurons:
     _check("dv_predict_topk", _lib.dv_predict_topk(
         C.byref(layer.desc), C.byref(layer.c), _ptr(x_pred), B, k_heads, k_neurons,
         C.byref(sel.c), _ptr(scores_h), _ptr(scores_n), ws.cptr, ws.nbytes, _stream(stream)))
+
+
+def dv_predict_topk_noalloc(layer: Layer, x_pred: torch.Tensor, k_heads: int, k_neurons: int,
+                            sel: SelectionBuffers, scores_h: Optional[torch.Tensor] = None,
+                            scores_n: Optional[torch.Tensor] = None, stream=None):
+    B = x_pred.shape[0]
+    _check("dv_predict_topk_noalloc", _lib.dv_predict_topk_noalloc(
+        C.byref(layer.desc), C.byref(layer.c), _ptr(x_pred), B, k_heads, k_neurons,
+        C.byref(sel.c), _ptr(scores_h), _ptr(scores_n), _stream(stream)))
 
 
 def dv_sparse_attn(layer: Layer, x: torch.Tensor, u_h: torch.Tensor, n_u_h: torch.Tensor,

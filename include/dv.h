@@ -69,7 +69,8 @@ typedef enum {
     DV_ERR_CUDA = 3,         /* a CUDA runtime call failed */
     DV_ERR_TIMEOUT = 4,      /* a bounded device-side wait gave up */
     DV_ERR_WORKSPACE = 5,    /* workspace missing, misaligned or too small */
-    DV_ERR_DEVICE_INDEX = 6  /* a kernel met an index outside its range (skipped) */
+    DV_ERR_DEVICE_INDEX = 6, /* a kernel met an index outside its range (skipped) */
+    DV_ERR_SCRATCH_LIMIT = 7 /* dv_predict_topk_noalloc: shape needs more than its scratch */
 } dv_status;
 
 typedef enum { DV_F32 = 0, DV_F16 = 1 } dv_dtype;
@@ -228,6 +229,43 @@ int dv_layer_decode_host(const dv_layer_desc *desc, const dv_layer_weights *w, c
  * measure the copy bandwidth that serves as the roofline denominator.
  */
 int dv_hbm_copy(void *dst, const void *src, size_t bytes, void *stream);
+
+/*
+ * dv_predict_topk_noalloc -- dv_predict_topk without a caller workspace.
+ * This entry point is an addition of this library; the DejaVu pages have no
+ * counterpart.  It is for callers that cannot provide device memory at the
+ * point of prediction: a serving loop whose pool has already given all free
+ * HBM to its KV cache, or code that must not call an allocator there because
+ * cudaMalloc / cudaFree synchronise the device.  It allocates nothing.
+ *
+ * Computes exactly what dv_predict_topk computes (same kernels, same
+ * arguments apart from the workspace).
+ *
+ * Scratch: a static device array of DV_NOALLOC_SCRATCH_BYTES inside this
+ * library, one per device per process -- the exception to the "no state
+ * outside the caller's workspace" convention above.  A shape and batch whose
+ * scratch (status word, histograms, row counters, scores, partial sums,
+ * bitmaps, candidates) does not fit is rejected with DV_ERR_SCRATCH_LIMIT and
+ * nothing is launched; at the OPT-175B shape (N = 49152, r = 1000) the limit
+ * is reached above batch 16.
+ * Set-up: the first call on a device, with that device current, looks up the
+ * scratch's device address (which may load the library's device code); make
+ * that first call before any stream capture begins.
+ * Zeroing: every call first zeroes, on `stream`, the part of the scratch
+ * that the kernels require to start at zero (status word, first-digit
+ * histograms, candidate counters, row counters); everything else is written
+ * before it is read.
+ * Concurrency: calls whose execution overlaps on one device (different
+ * streams, or different host threads) share the scratch and race; the
+ * results are then wrong.  Serialise them.  Device-side faults recorded in
+ * the scratch status word are not reported.
+ */
+#define DV_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+
+int dv_predict_topk_noalloc(const dv_layer_desc *desc, const dv_layer_weights *w,
+                            const float *x_pred, int batch, int k_heads, int k_neurons,
+                            const dv_selection *sel, float *scores_h, float *scores_n,
+                            void *stream);
 
 #ifdef __cplusplus
 }

@@ -26,6 +26,7 @@ namespace {
 
 constexpr int kStageRows = 256;  // rows whose offsets and coefficients are staged at once
 constexpr int kMaxCover = 512;   // CTAs that may share one column block
+constexpr int kCoverBatch = 8;   // partials loaded together by the combining CTA
 
 template <int KIND>
 DV_DEV long long row_offset(const ColArgs &a, int i)
@@ -274,14 +275,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_colacc(const ColArgs a)
 #pragma unroll
             for (int b = 0; b < NB; ++b)
                 s[b] = 0.f;
-            for (int c = 0; c < ncover; ++c) {
-                const int slot = s_cover[c];
-                if (slot < 0)
-                    continue;
-                const float *q = a.part + ((size_t)tile * nc * 2 + slot) * NB * CB;
+            // kCoverBatch partials loaded at once, then added in CTA order
+            for (int c0 = 0; c0 < ncover; c0 += kCoverBatch) {
+                float v[kCoverBatch][NB];
+                unsigned live = 0u;
 #pragma unroll
-                for (int b = 0; b < NB; ++b)
-                    s[b] += __ldcg(q + b * CB + col);
+                for (int u = 0; u < kCoverBatch; ++u) {
+                    const int slot = (c0 + u < ncover) ? s_cover[c0 + u] : -1;
+                    const float *q =
+                        a.part + ((size_t)tile * nc * 2 + (slot < 0 ? 0 : slot)) * NB * CB;
+                    live |= (slot >= 0 ? 1u : 0u) << u;
+#pragma unroll
+                    for (int b = 0; b < NB; ++b)
+                        v[u][b] = slot >= 0 ? __ldcg(q + b * CB + col) : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < kCoverBatch; ++u)
+                    if ((live >> u) & 1u)
+#pragma unroll
+                        for (int b = 0; b < NB; ++b)
+                            s[b] += v[u][b];
             }
             write_out<T, NB, P>(a, b0, cb * CB + col, s);
         }

@@ -537,10 +537,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot(const RowArgs a)
         pdl_launch_dependents();
         if (a.neuron_pass && tile == 0) {
             __shared__ int sb1[DV_MAX_BATCH];
+            __shared__ int hbuf[kTopkBins];
+            __shared__ int nscr[48];
             const int W = (a.ns.N + 31) >> 5;
             const int w0 = (int)((long long)W * blockIdx.x / gridDim.x);
             const int w1 = (int)((long long)W * (blockIdx.x + 1) / gridDim.x);
-            neuron_pass(a.ns, w0, w1, sb1);
+            neuron_pass(a.ns, w0, w1, sb1, hbuf, nscr);
         }
     }
 }

@@ -12,6 +12,8 @@ __global__ void __launch_bounds__(kThreads) k_select_pass(const SelectArgs a)
     __shared__ unsigned hbits[2 * kHeadKPL];
     __shared__ int32_t hsel[kHeadTopkMax];
     __shared__ int sb1[DV_MAX_BATCH];
+    __shared__ int hbuf[kTopkBins];
+    __shared__ int scr[48];
     pdl_wait();  // the scores come from the previous kernels
     pdl_launch_dependents();
     if (blockIdx.x == 0 && threadIdx.x < 32)
@@ -20,7 +22,7 @@ __global__ void __launch_bounds__(kThreads) k_select_pass(const SelectArgs a)
     const int W = (a.ns.N + 31) >> 5;
     const int w0 = (int)((long long)W * blockIdx.x / gridDim.x);
     const int w1 = (int)((long long)W * (blockIdx.x + 1) / gridDim.x);
-    neuron_pass(a.ns, w0, w1, sb1);
+    neuron_pass(a.ns, w0, w1, sb1, hbuf, scr);
 }
 
 __global__ void __launch_bounds__(kThreads) k_select_final(const SelectArgs a)

@@ -115,50 +115,55 @@ DV_DEV int head_select(const float *s_h, int B, int H, int k, unsigned *sbits, i
 // ---------------------------------------------------------------------------
 // Neuron selection (state: NeuronSel in the workspace).
 
-// Bin of the k-th largest key and the rank left inside it, from a histogram
-// (one warp; bins scanned from the top).
-DV_DEV void warp_find_bin(const int *hist, int k, int lane, int *bin_out, int *krem_out)
+// Block-wide: bin of the krem-th largest key of a histogram of nb bins.
+DV_DEV void block_find_bin(const int *hist, int nb, int krem, int *scr)
 {
-    constexpr int PER = kTopkBins / 32;  // bins per lane, lane 0 owns the top ones
+    const int nt = blockDim.x, tid = threadIdx.x;
+    const int per = (nb + nt - 1) / nt;
+    const int top = nb - 1 - tid * per;
     int c = 0;
-    const int top = kTopkBins - 1 - lane * PER;
-#pragma unroll 8
-    for (int q = 0; q < PER; ++q)
-        c += ld_cg(hist + top - q);
-    const int incl = warp_incl_scan(c, lane);
-    const int before = incl - c;
-    int bin = -1, krem = 0;
-    if (before < k && k <= incl) {
+    for (int q = 0; q < per; ++q) {
+        const int bin = top - q;
+        if (bin >= 0)
+            c += hist[bin];
+    }
+    int tot;
+    const int before = block_excl_scan(c, scr + 4, &tot);
+    if (before < krem && krem <= before + c) {
         int acc = before;
-        for (int q = 0; q < PER; ++q) {
-            const int h = ld_cg(hist + top - q);
-            if (k <= acc + h) {
-                bin = top - q;
-                krem = k - acc;
+        for (int q = 0; q < per; ++q) {
+            const int bin = top - q;
+            if (bin < 0)
+                break;
+            const int h = hist[bin];
+            if (krem <= acc + h) {
+                scr[0] = bin;
+                scr[1] = krem - acc;
                 break;
             }
             acc += h;
         }
     }
-    const unsigned m = __ballot_sync(0xffffffffu, bin >= 0);
-    const int src = m ? __ffs(m) - 1 : 0;
-    *bin_out = __shfl_sync(0xffffffffu, bin, src);
-    *krem_out = __shfl_sync(0xffffffffu, krem, src);
+    __syncthreads();
 }
 
 // The pass of one CTA over bitmap words [w0, w1) of every row (all threads
-// of the CTA).  Words are whole: each belongs to exactly one CTA.
-DV_DEV void neuron_pass(const NeuronSel &ns, int w0, int w1, int *sb1 /* smem [B] */)
+// of the CTA).  Words are whole: each belongs to exactly one CTA.  hbuf:
+// shared [kTopkBins]; scr: shared [48]; sb1: shared [B].
+DV_DEV void neuron_pass(const NeuronSel &ns, int w0, int w1, int *sb1, int *hbuf, int *scr)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
     const int W = (ns.N + 31) >> 5;
-    if (warp == 0) {
-        for (int b = 0; b < ns.B; ++b) {
-            int bin, krem;
-            warp_find_bin(ns.hist + (size_t)b * kTopkBins, ns.k, lane, &bin, &krem);
-            if (lane == 0)
-                sb1[b] = bin;
-        }
+    for (int b = 0; b < ns.B; ++b) {
+        // the row's first-digit histogram, staged with independent loads
+        const int *gh = ns.hist + (size_t)b * kTopkBins;
+        for (int i = tid; i < kTopkBins; i += nt)
+            hbuf[i] = ld_cg(gh + i);
+        __syncthreads();
+        block_find_bin(hbuf, kTopkBins, ns.k, scr);
+        if (tid == 0)
+            sb1[b] = scr[0];
     }
     __syncthreads();
     for (int b = 0; b < ns.B; ++b) {
@@ -204,38 +209,6 @@ __host__ __device__ inline size_t neuron_final_smem_bytes(int N)
 {
     const int W = (N + 31) >> 5;
     return ((size_t)kTopkBins + 2 * (size_t)W + 2 * (size_t)kTopkCand) * 4;
-}
-
-// Block-wide: bin of the krem-th largest key of a histogram of nb bins.
-DV_DEV void block_find_bin(const int *hist, int nb, int krem, int *scr)
-{
-    const int nt = blockDim.x, tid = threadIdx.x;
-    const int per = (nb + nt - 1) / nt;
-    const int top = nb - 1 - tid * per;
-    int c = 0;
-    for (int q = 0; q < per; ++q) {
-        const int bin = top - q;
-        if (bin >= 0)
-            c += hist[bin];
-    }
-    int tot;
-    const int before = block_excl_scan(c, scr + 4, &tot);
-    if (before < krem && krem <= before + c) {
-        int acc = before;
-        for (int q = 0; q < per; ++q) {
-            const int bin = top - q;
-            if (bin < 0)
-                break;
-            const int h = hist[bin];
-            if (krem <= acc + h) {
-                scr[0] = bin;
-                scr[1] = krem - acc;
-                break;
-            }
-            acc += h;
-        }
-    }
-    __syncthreads();
 }
 
 // Ascending indices of the set bits of bits[0..W), block-wide.
@@ -304,26 +277,22 @@ DV_DEV void neuron_overflow(const float *s, int N, unsigned prefix, int krem, co
 // histogram and candidate counts zero.  One whole CTA; smem as FinalSmem.
 DV_DEV void neuron_final(const NeuronSel &ns, const FinalSmem &sm)
 {
-    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x, nt = blockDim.x;
     const int W = (ns.N + 31) >> 5;
     for (int i = tid; i < W; i += nt)
         sm.ubits[i] = 0u;
     for (int b = 0; b < ns.B; ++b) {
         int *ghist = ns.hist + (size_t)b * kTopkBins;
-        if (warp == 0) {
-            int bin, krem;
-            warp_find_bin(ghist, ns.k, lane, &bin, &krem);
-            if (lane == 0) {
-                sm.scr[40] = bin;
-                sm.scr[41] = krem;
-            }
-        }
+        for (int i = tid; i < kTopkBins; i += nt)
+            sm.hist[i] = __ldcg(ghist + i);
         const unsigned *gbits = ns.rowbits + (size_t)b * W;
         for (int i = tid; i < W; i += nt)
             sm.rowbits[i] = __ldcg(gbits + i);
         __syncthreads();
-        const unsigned b1 = (unsigned)sm.scr[40];
-        const int krem = sm.scr[41];
+        block_find_bin(sm.hist, kTopkBins, ns.k, sm.scr);
+        const unsigned b1 = (unsigned)sm.scr[0];
+        const int krem = sm.scr[1];
+        __syncthreads();  // every thread holds b1, krem before scr is reused
         const int ncand = __ldcg(ns.cand_cnt + b);
         if (ncand > kTopkCand) {
             neuron_overflow(ns.s_n + (size_t)b * ns.N, ns.N, b1 << 21, krem, sm);

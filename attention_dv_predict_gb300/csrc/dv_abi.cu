@@ -13,6 +13,7 @@ using namespace dv;
 namespace {
 
 constexpr int kLayerLaunches = 7;
+constexpr int kSideFlagWord = 1;  // workspace control word of the side-work flag
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -147,7 +148,8 @@ NeuronSel make_neuron_sel(const dv_layer_desc &D, int B, int kn, const dv_select
 // PRED1 (head scores, low-rank factor u) and PRED2 (neuron scores +
 // first-digit histogram).  PRED1 is the first launch of the call.
 dv_status run_scores(const dv_layer_desc &D, const dv_layer_weights &w, const float *xp, int B,
-                     float *sh_user, float *sn_user, void *ws, const WsLayout &L, Launch &lc)
+                     float *sh_user, float *sn_user, void *ws, const WsLayout &L, Launch &lc,
+                     const PredSide *side = nullptr)
 {
     const int d = D.d_model, H = D.n_heads, N = D.d_ffn, r = D.pred_rank;
     int *ctl = at<int>(ws, L.ctl);
@@ -170,6 +172,8 @@ dv_status run_scores(const dv_layer_desc &D, const dv_layer_weights &w, const fl
     a.part = at<float>(ws, L.part_pred1);
     a.rowcnt = at<int>(ws, L.cnt_pred1);
     a.status = ctl;
+    if (side)
+        a.side_flag = ctl + kSideFlagWord;
     dim3 grid(lc.nsm, ceil_div(B, nb));
     dv_status s = lc.mark();
     if (s)
@@ -194,6 +198,11 @@ dv_status run_scores(const dv_layer_desc &D, const dv_layer_weights &w, const fl
     b2.part = at<float>(ws, L.part_pred1);
     b2.rowcnt = at<int>(ws, L.cnt_pred1);
     b2.status = ctl;
+    if (side) {
+        b2.side_cta = 1;
+        b2.side = *side;
+        b2.side_flag = ctl + kSideFlagWord;
+    }
     grid = dim3(lc.nsm, ceil_div(B, nb));
     if ((s = lc.mark()))
         return s;
@@ -203,13 +212,14 @@ dv_status run_scores(const dv_layer_desc &D, const dv_layer_weights &w, const fl
     return DV_OK;
 }
 
-// Attention block.  Fused mode (fused != nullptr): the QKV kernel selects the
-// heads itself and runs the neuron pass; the attention kernel's CTA 0
-// finishes the neuron selection.  first: this is the call's first launch.
+// Attention block.  Fused mode (ns != nullptr): the head union and norm(x)
+// come from the stage-2 predictor's side CTA, the QKV kernel runs the
+// neuron pass after its rows and the attention kernel's CTA 0 finishes the
+// neuron selection.  first: this is the call's first launch.
 dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const float *x, int B,
                    const int32_t *u_h, const int32_t *n_u_h, int max_u_h, void *kc, void *vc,
                    int kv_len, float *h1, void *ws, const WsLayout &L, Launch &lc, bool first,
-                   const dv_selection *fused, int k_heads, const NeuronSel *ns)
+                   const NeuronSel *ns)
 {
     const int d = D.d_model, H = D.n_heads, dh = D.head_dim;
     int *ctl = at<int>(ws, L.ctl);
@@ -244,15 +254,14 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     a.part = at<float>(ws, L.part_qkv);
     a.rowcnt = at<int>(ws, L.cnt_qkv);
     a.status = ctl;
-    if (fused) {
-        a.head_sel = 1;
-        a.s_h = at<float>(ws, L.s_h);
-        a.k_h = k_heads;
-        a.idx_h_out = fused->idx_h;
-        a.u_h_out = fused->u_h;
-        a.n_u_h_out = fused->n_u_h;
+    if (ns) {
+        // heads and norm(x) come from the stage-2 predictor kernel's side CTA
+        a.x = at<float>(ws, L.xn);
+        a.norm_g = nullptr;
+        a.norm_b = nullptr;
         a.neuron_pass = 1;
         a.ns = *ns;
+        a.side_flag = ctl + kSideFlagWord;
     }
     dim3 grid(lc.nsm, ceil_div(B, nb));
     dv_status s = lc.mark();
@@ -276,7 +285,7 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     t.kc = kc;
     t.vc = vc;
     const int L1 = kv_len + 1;
-    const int attn_ctas = fused ? lc.nsm - 1 : lc.nsm;
+    const int attn_ctas = ns ? lc.nsm - 1 : lc.nsm;
     // chunks per (batch row, head): enough CTAs to cover the SMs once
     int chunks = attn_ctas / (B * max_u_h);
     if (chunks < 1)
@@ -291,7 +300,7 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     t.cnt = at<int>(ws, L.attn_cnt);
     t.o = at<float>(ws, L.o);
     t.status = ctl;
-    if (fused) {
+    if (ns) {
         t.neuron_final = 1;
         t.ns = *ns;
     }
@@ -436,10 +445,26 @@ dv_status layer_decode_impl(const dv_layer_desc *desc, const dv_layer_weights *w
     const int max_u_h = batch * k_heads < D.n_heads ? batch * k_heads : D.n_heads;
     const int max_u_n = batch * k_neurons < D.d_ffn ? batch * k_neurons : D.d_ffn;
     const NeuronSel ns = make_neuron_sel(D, batch, k_neurons, *sel, ws, L);
-    if ((s = run_scores(D, *w, x_pred ? x_pred : x, batch, nullptr, nullptr, ws, L, lc)))
+    PredSide side;
+    std::memset(&side, 0, sizeof(side));
+    side.s_h = at<float>(ws, L.s_h);
+    side.H = D.n_heads;
+    side.k_h = k_heads;
+    side.idx_h = sel->idx_h;
+    side.u_h = sel->u_h;
+    side.n_u_h = sel->n_u_h;
+    side.x = x;
+    side.x_ld = D.d_model;
+    side.d = D.d_model;
+    side.g = w->ln1_g;
+    side.beta = w->ln1_b;
+    side.norm_kind = D.norm;
+    side.eps = D.ln_eps;
+    side.xn = at<float>(ws, L.xn);
+    if ((s = run_scores(D, *w, x_pred ? x_pred : x, batch, nullptr, nullptr, ws, L, lc, &side)))
         return s;
     if ((s = run_attn(D, *w, x, batch, sel->u_h, sel->n_u_h, max_u_h, kc, vc, kv_len, h1p, ws, L,
-                      lc, false, sel, k_heads, &ns)))
+                      lc, false, &ns)))
         return s;
     if ((s = run_mlp(D, *w, h1p, batch, sel->u_n, sel->n_u_n, max_u_n, y, ws, L, lc, false)))
         return s;
@@ -503,6 +528,7 @@ bool ws_layout(const dv_layer_desc &D, int B, WsLayout *L)
     L->cand_key = take((size_t)B * kTopkCand * 4);
     L->cand_idx = take((size_t)B * kTopkCand * 4);
     L->cand_cnt = take((size_t)B * 4);
+    L->xn = take((size_t)B * d * 4);
     L->total = off;
     L->bpad = (int)bp;
     L->attn_splits_max = (int)splits;
@@ -626,7 +652,7 @@ int dv_sparse_attn(const dv_layer_desc *desc, const dv_layer_weights *w, const f
     if ((s = make_launch(stream, nullptr, 0, &lc)))
         return s;
     if ((s = run_attn(D, *w, x, batch, u_h, n_u_h, max_u_h, k_cache, v_cache, kv_len, h1, ws, L,
-                      lc, true, nullptr, 0, nullptr)))
+                      lc, true, nullptr)))
         return s;
     return cuda_status(cudaGetLastError());
 }

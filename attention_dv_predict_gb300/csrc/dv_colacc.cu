@@ -124,16 +124,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_colacc(const ColArgs a)
                     set_status(a.status, DV_ERR_DEVICE_INDEX);
             }
             if (!waited) {
-                // the gather indices come from kernels at least two launches back;
-                // start the first rows toward L2, then wait for the coefficients
-                __syncthreads();
-                if (lane < R) {
-                    const int li = warp + kWarpsPerBlock * lane;
-                    if (s0 + li < s1 && soff[li] >= 0) {
-                        const int ncol = min(CB, a.d - cb * CB);
-                        prefetch_l2(W + soff[li] + (size_t)cb * CB, (unsigned)(ncol * sizeof(T)));
-                    }
-                }
+                // the gather indices come from kernels at least two launches
+                // back; the coefficients from the previous one
                 pdl_wait();
                 pdl_launch_dependents();
                 waited = true;

@@ -30,12 +30,6 @@ DV_DEV uint4 ld_stream(const void *p)
     return r;
 }
 
-// Ask the TMA engine to bring `bytes` (multiple of 16, 16-byte aligned) into L2.
-DV_DEV void prefetch_l2(const void *p, unsigned bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // Values written by other CTAs of the same kernel: read at L2 (bypass L1).
 DV_DEV float ld_cg(const float *p) { return __ldcg(p); }
 DV_DEV int ld_cg(const int *p) { return __ldcg(p); }
@@ -170,6 +164,20 @@ DV_DEV unsigned score_key(float s)
     if (u == 0x80000000u)
         u = 0u;
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Flag hand-off between kernels of one call: the writer publishes its data,
+// then stores the flag with release semantics; a reader that sees the flag
+// with acquire semantics also sees the data.
+DV_DEV int ld_acquire_gpu(const int *p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+DV_DEV void st_release_gpu(int *p, int v)
+{
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // ---------------------------------------------------------------------------

@@ -62,6 +62,24 @@ struct RowGeo {
     int U;     // chunks in flight per lane (template parameter of the kernel)
 };
 
+// Side work of the stage-2 predictor kernel in the fused decode (one CTA):
+// head selection and the normalised input of the attention block.
+struct PredSide {
+    const float *s_h;     // head scores [B][H]
+    int H, k_h;
+    int32_t *idx_h, *u_h, *n_u_h;
+    const float *x;       // layer input [B][x_ld]
+    int x_ld, d;
+    const void *g, *beta; // norm parameters (dtype of the weights)
+    int norm_kind;
+    float eps;
+    float *xn;            // out: norm(x) [B][d]
+};
+
+// Polls of the side-work flag before the QKV kernel falls back to waiting
+// for the whole stage-2 predictor grid.
+constexpr int kSideSpin = 20000;
+
 struct RowArgs {
     int K;            // row length in elements
     RowGeo geo;
@@ -87,11 +105,12 @@ struct RowArgs {
     float *part;          // range-boundary partials [tiles][warps][2][NB]
     int *rowcnt;          // segments accounted per row [tiles][max_rows], zero at rest
     int *hist;            // PRED2: first-digit histogram [B][kTopkBins], zero at rest
-    // QKV only: select the heads in the prologue from the head scores
-    int head_sel;
-    const float *s_h;     // [B][H]
-    int k_h;
-    int32_t *idx_h_out, *u_h_out, *n_u_h_out;  // written by CTA 0
+    // PRED2 only: the last CTA column does the side work (PredSide) instead of rows
+    int side_cta;
+    PredSide side;
+    // fused decode: PRED1 clears it, PRED2's side CTA sets it once its results
+    // are published, the QKV kernel starts on it instead of the grid dependency
+    int *side_flag;
     // QKV only: neuron selection pass over the scores after the main loop
     int neuron_pass;
     NeuronSel ns;
@@ -155,6 +174,7 @@ struct WsLayout {
     size_t stage_x, stage_xp, stage_y;
     size_t sel_idx_h, sel_idx_n, sel_u_h, sel_n_u_h, sel_u_n, sel_n_u_n;
     size_t nbits, cand_key, cand_idx, cand_cnt;  // neuron selection state
+    size_t xn;  // normalised input of the attention block (fused decode)
     size_t total;
     int bpad;         // batch rounded up to the largest batch tile (8)
     int attn_splits_max;

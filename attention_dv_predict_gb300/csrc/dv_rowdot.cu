@@ -96,101 +96,140 @@ DV_DEV void stage_chunk_store(float *dst, int K, int c, const float (&v)[Elem<T>
     }
 }
 
-template <typename T, int NB>
-DV_DEV void stage_acts(const RowArgs &a, float *xs, int b0, float *red)
+// One activation row src[0..K), normalised when g != nullptr, handed chunk
+// by chunk to store(c, v) (c = chunk index, v = its EPC values).  Every
+// thread of the block calls it; barriers inside.
+template <typename T, typename Store>
+DV_DEV void norm_row(const float *src, int K, const void *g_, const void *b_, int norm_kind,
+                     float eps, float *red, Store store)
 {
     constexpr int EPC = Elem<T>::EPC;
     constexpr int CQ = kStageChunks;
-    const int K = a.K, nch = K / EPC, tid = threadIdx.x, nt = blockDim.x;
-    const bool norm = a.norm_g != nullptr;
-    const bool ln = a.norm_kind == DV_LAYERNORM;
+    const int nch = K / EPC, tid = threadIdx.x, nt = blockDim.x;
+    const bool norm = g_ != nullptr;
+    const bool ln = norm_kind == DV_LAYERNORM;
+    for (int c0 = 0; c0 < nch; c0 += nt * CQ) {
+        // chunks c0 + tid + q*nt of this row (all of it when nch <= nt*CQ)
+        float v[CQ][EPC];
+        uint4 gv[CQ], bv[CQ];
+#pragma unroll
+        for (int q = 0; q < CQ; ++q) {
+            const int c = c0 + tid + q * nt;
+            const bool in = c < nch;
+#pragma unroll
+            for (int e = 0; e < EPC; e += 4) {
+                const float4 t = in ? reinterpret_cast<const float4 *>(src + (size_t)c * EPC)[e / 4]
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[q][e] = t.x;
+                v[q][e + 1] = t.y;
+                v[q][e + 2] = t.z;
+                v[q][e + 3] = t.w;
+            }
+            gv[q] = (in && norm) ? reinterpret_cast<const uint4 *>(g_)[c]
+                                 : make_uint4(0u, 0u, 0u, 0u);
+            bv[q] = (in && norm && ln) ? reinterpret_cast<const uint4 *>(b_)[c]
+                                       : make_uint4(0u, 0u, 0u, 0u);
+        }
+        float mean = 0.f, inv = 1.f;
+        if (norm) {
+            if (nch > nt * CQ) {
+                // long rows: statistics over the whole row first (rare)
+                float s = 0.f, ss = 0.f;
+                for (int c = tid; c < nch; c += nt)
+                    for (int e = 0; e < EPC; ++e)
+                        s += src[(size_t)c * EPC + e];
+                mean = ln ? block_sum(s, red) / (float)K : 0.f;
+                for (int c = tid; c < nch; c += nt)
+                    for (int e = 0; e < EPC; ++e) {
+                        const float d = src[(size_t)c * EPC + e] - mean;
+                        ss = fmaf(d, d, ss);
+                    }
+                inv = rsqrtf(block_sum(ss, red) / (float)K + eps);
+            } else {
+                float s = 0.f;
+#pragma unroll
+                for (int q = 0; q < CQ; ++q)
+#pragma unroll
+                    for (int e = 0; e < EPC; ++e)
+                        s += v[q][e];
+                mean = ln ? block_sum(s, red) / (float)K : 0.f;
+                float ss = 0.f;
+#pragma unroll
+                for (int q = 0; q < CQ; ++q) {
+                    if (c0 + tid + q * nt >= nch)
+                        break;
+#pragma unroll
+                    for (int e = 0; e < EPC; ++e) {
+                        const float d = v[q][e] - mean;
+                        ss = fmaf(d, d, ss);
+                    }
+                }
+                inv = rsqrtf(block_sum(ss, red) / (float)K + eps);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < CQ; ++q) {
+            const int c = c0 + tid + q * nt;
+            if (c >= nch)
+                break;
+            if (norm) {
+                float g[EPC], be[EPC];
+                Elem<T>::unpack(gv[q], g);
+                if (ln)
+                    Elem<T>::unpack(bv[q], be);
+#pragma unroll
+                for (int e = 0; e < EPC; ++e)
+                    v[q][e] = (v[q][e] - mean) * inv * g[e] + (ln ? be[e] : 0.f);
+            }
+            store(c, v[q]);
+        }
+    }
+}
+
+template <typename T, int NB>
+DV_DEV void stage_acts(const RowArgs &a, float *xs, int b0, float *red)
+{
+    const int K = a.K;
     for (int bi = 0; bi < NB; ++bi) {
         const int b = b0 + bi;
         float *dst = xs + (size_t)bi * K;
         if (b >= a.B) {
-            for (int c = tid; c < K; c += nt)
+            for (int c = threadIdx.x; c < K; c += blockDim.x)
                 dst[c] = 0.f;
             continue;
         }
-        const float *src = a.x + (size_t)b * a.x_ld;
-        for (int c0 = 0; c0 < nch; c0 += nt * CQ) {
-            // chunks c0 + tid + q*nt of this row (all of it when nch <= nt*CQ)
-            float v[CQ][EPC];
-            uint4 gv[CQ], bv[CQ];
-#pragma unroll
-            for (int q = 0; q < CQ; ++q) {
-                const int c = c0 + tid + q * nt;
-                const bool in = c < nch;
-#pragma unroll
-                for (int e = 0; e < EPC; e += 4) {
-                    const float4 t = in ? reinterpret_cast<const float4 *>(src + (size_t)c * EPC)[e / 4]
-                                        : make_float4(0.f, 0.f, 0.f, 0.f);
-                    v[q][e] = t.x;
-                    v[q][e + 1] = t.y;
-                    v[q][e + 2] = t.z;
-                    v[q][e + 3] = t.w;
-                }
-                gv[q] = (in && norm) ? reinterpret_cast<const uint4 *>(a.norm_g)[c]
-                                     : make_uint4(0u, 0u, 0u, 0u);
-                bv[q] = (in && norm && ln) ? reinterpret_cast<const uint4 *>(a.norm_b)[c]
-                                           : make_uint4(0u, 0u, 0u, 0u);
-            }
-            float mean = 0.f, inv = 1.f;
-            if (norm) {
-                if (nch > nt * CQ) {
-                    // long rows: statistics over the whole row first (rare)
-                    float s = 0.f, ss = 0.f;
-                    for (int c = tid; c < nch; c += nt)
-                        for (int e = 0; e < EPC; ++e)
-                            s += src[(size_t)c * EPC + e];
-                    mean = ln ? block_sum(s, red) / (float)K : 0.f;
-                    for (int c = tid; c < nch; c += nt)
-                        for (int e = 0; e < EPC; ++e) {
-                            const float d = src[(size_t)c * EPC + e] - mean;
-                            ss = fmaf(d, d, ss);
-                        }
-                    inv = rsqrtf(block_sum(ss, red) / (float)K + a.eps);
-                } else {
-                    float s = 0.f;
-#pragma unroll
-                    for (int q = 0; q < CQ; ++q)
-#pragma unroll
-                        for (int e = 0; e < EPC; ++e)
-                            s += v[q][e];
-                    mean = ln ? block_sum(s, red) / (float)K : 0.f;
-                    float ss = 0.f;
-#pragma unroll
-                    for (int q = 0; q < CQ; ++q) {
-                        if (c0 + tid + q * nt >= nch)
-                            break;
-#pragma unroll
-                        for (int e = 0; e < EPC; ++e) {
-                            const float d = v[q][e] - mean;
-                            ss = fmaf(d, d, ss);
-                        }
-                    }
-                    inv = rsqrtf(block_sum(ss, red) / (float)K + a.eps);
-                }
-            }
-#pragma unroll
-            for (int q = 0; q < CQ; ++q) {
-                const int c = c0 + tid + q * nt;
-                if (c >= nch)
-                    break;
-                if (norm) {
-                    float g[EPC], be[EPC];
-                    Elem<T>::unpack(gv[q], g);
-                    if (ln)
-                        Elem<T>::unpack(bv[q], be);
-#pragma unroll
-                    for (int e = 0; e < EPC; ++e)
-                        v[q][e] = (v[q][e] - mean) * inv * g[e] + (ln ? be[e] : 0.f);
-                }
-                stage_chunk_store<T>(dst, K, c, v[q]);
-            }
-        }
+        norm_row<T>(a.x + (size_t)b * a.x_ld, K, a.norm_g, a.norm_b, a.norm_kind, a.eps, red,
+                    [&](int c, const float(&v)[Elem<T>::EPC]) {
+                        stage_chunk_store<T>(dst, K, c, v);
+                    });
     }
     __syncthreads();
+}
+
+// Side work of one CTA of the stage-2 predictor kernel in the fused decode:
+// select the heads (the head scores come from the previous kernel) and
+// write the attention block's normalised input xn = norm(x) to global
+// memory, both for the QKV kernel that follows.
+template <typename T>
+__device__ __noinline__ void pred2_side(const RowArgs &a, float *red)
+{
+    __shared__ unsigned hbits[2 * kHeadKPL];
+    __shared__ int32_t hsel[kHeadTopkMax];
+    const PredSide &p = a.side;
+    if (threadIdx.x < 32)
+        head_select(p.s_h, a.B, p.H, p.k_h, hbits, hsel, true, p.idx_h, p.u_h, p.n_u_h,
+                    threadIdx.x);
+    constexpr int EPC = Elem<T>::EPC;
+    for (int b = 0; b < a.B; ++b) {
+        float *dst = p.xn + (size_t)b * p.d;
+        norm_row<T>(p.x + (size_t)b * p.x_ld, p.d, p.g, p.beta, p.norm_kind, p.eps, red,
+                    [&](int c, const float(&v)[EPC]) {
+#pragma unroll
+                        for (int e = 0; e < EPC; e += 4)
+                            *reinterpret_cast<float4 *>(dst + (size_t)c * EPC + e) =
+                                make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+                    });
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -330,39 +369,66 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot(const RowArgs a)
     if constexpr (KIND == RK_PRED1) {  // the first kernel of a call: nothing to wait for
         pdl_wait();
         pdl_launch_dependents();
+        if (a.side_flag && blockIdx.x == 0 && tile == 0 && threadIdx.x == 0)
+            *a.side_flag = 0;
+    }
+    int ncta = gridDim.x;  // CTAs that share the rows
+    if constexpr (KIND == RK_PRED2) {
+        if (a.side_cta) {
+            ncta = gridDim.x - 1;
+            if (blockIdx.x == ncta) {  // the last CTA does the side work instead
+                pdl_wait();
+                pdl_launch_dependents();
+                if (tile == 0) {
+                    pred2_side<T>(a, red);
+                    __threadfence();
+                    __syncthreads();
+                    if (threadIdx.x == 0 && a.side_flag)
+                        st_release_gpu(a.side_flag, 1);
+                }
+                return;
+            }
+        }
+    }
+    if constexpr (KIND == RK_QKV) {
+        if (a.side_flag) {
+            // the head union and norm(x) come from the previous kernel's side
+            // CTA: start as soon as it has published them (bounded polling,
+            // then the grid dependency)
+            __shared__ int s_ready;
+            if (threadIdx.x == 0) {
+                int ok = 0;
+                for (int it = 0; it < kSideSpin && !ok; ++it) {
+                    ok = ld_acquire_gpu(a.side_flag);
+                    if (!ok)
+                        __nanosleep(128);
+                }
+                s_ready = ok;
+            }
+            __syncthreads();
+            if (!s_ready)
+                pdl_wait();
+        } else {  // the head union was given by the caller
+            pdl_wait();
+            pdl_launch_dependents();
+        }
     }
     int rows = a.max_rows;
     int sj0 = 0, sn = 0;  // staged gather indices: ssel[i] = sel[sj0 + i], i < sn
-    if constexpr (KIND == RK_QKV) {
-        if (a.head_sel) {
-            // select the heads from the head scores (every CTA, one warp)
-            __shared__ unsigned hbits[2 * kHeadKPL];
-            __shared__ int s_nuh;
-            if (warp == 0) {
-                const int nu = head_select(a.s_h, a.B, a.H, a.k_h, hbits, ssel, blockIdx.x == 0,
-                                           a.idx_h_out, a.u_h_out, a.n_u_h_out, lane);
-                if (lane == 0)
-                    s_nuh = nu;
-            }
-            __syncthreads();
-            sn = min(s_nuh, a.max_sel);
-            rows = sn * 3 * a.dh;
-        } else {
-            rows = min(max(ld_cg(a.n_sel), 0), a.max_sel) * 3 * a.dh;
-        }
-    } else if constexpr (KIND == RK_FC1) {
+    if constexpr (KIND == RK_QKV)
+        rows = min(max(ld_cg(a.n_sel), 0), a.max_sel) * 3 * a.dh;
+    else if constexpr (KIND == RK_FC1)
         rows = min(max(ld_cg(a.n_sel), 0), a.max_sel);
-    }
     const bool seg = g.nsu > 0;
     const int units = seg ? rows * g.nsu : (rows + g.rpu - 1) / g.rpu;
-    const int Wt = gridDim.x * kWarpsPerBlock;
+    const int Wt = ncta * kWarpsPerBlock;
     const int gw = blockIdx.x * kWarpsPerBlock + warp;
     const int ub = range_start(units, Wt, gw), ue = range_start(units, Wt, gw + 1);
     const int LG = 32 / g.rpu;
     const int grp = lane / LG, lig = lane - grp * LG;
 
     // gather indices of the rows this CTA touches, staged in shared memory
-    const bool stage_sel = (KIND == RK_FC1) || (KIND == RK_QKV && !a.head_sel);
+    const bool stage_sel = (KIND == RK_FC1) || (KIND == RK_QKV);
     if (stage_sel) {
         const int cb = range_start(units, Wt, blockIdx.x * kWarpsPerBlock);
         const int ce = range_start(units, Wt, (blockIdx.x + 1) * kWarpsPerBlock);
@@ -533,8 +599,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot(const RowArgs a)
         }
     }
     if constexpr (KIND == RK_QKV) {
-        pdl_wait();  // the neuron scores and their histogram are complete
-        pdl_launch_dependents();
+        if (a.side_flag) {  // the neuron scores and their histogram: the whole grid
+            pdl_wait();
+            pdl_launch_dependents();
+        }
         if (a.neuron_pass && tile == 0) {
             __shared__ int sb1[DV_MAX_BATCH];
             __shared__ int hbuf[kTopkBins];

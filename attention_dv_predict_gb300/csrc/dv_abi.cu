@@ -254,21 +254,25 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     a.part = at<float>(ws, L.part_qkv);
     a.rowcnt = at<int>(ws, L.cnt_qkv);
     a.status = ctl;
+    size_t smem = rowdot_smem(RK_QKV, nb, d);
     if (ns) {
-        // heads and norm(x) come from the stage-2 predictor kernel's side CTA
+        // heads and norm(x) come from the stage-2 predictor kernel's side CTA;
+        // the last CTA of this kernel selects the neurons
         a.x = at<float>(ws, L.xn);
         a.norm_g = nullptr;
         a.norm_b = nullptr;
-        a.neuron_pass = 1;
+        a.side_cta = 1;
         a.ns = *ns;
         a.side_flag = ctl + kSideFlagWord;
+        const size_t fs = select_final_smem(D.d_ffn);
+        if (fs > smem)
+            smem = fs;
     }
     dim3 grid(lc.nsm, ceil_div(B, nb));
     dv_status s = lc.mark();
     if (s)
         return s;
-    if (launch_rowdot(RK_QKV, D.dtype, nb, a, grid, rowdot_smem(RK_QKV, nb, d), lc.st, !first) !=
-        cudaSuccess)
+    if (launch_rowdot(RK_QKV, D.dtype, nb, a, grid, smem, lc.st, !first) != cudaSuccess)
         return DV_ERR_CUDA;
 
     AttnArgs t;
@@ -285,9 +289,8 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     t.kc = kc;
     t.vc = vc;
     const int L1 = kv_len + 1;
-    const int attn_ctas = ns ? lc.nsm - 1 : lc.nsm;
     // chunks per (batch row, head): enough CTAs to cover the SMs once
-    int chunks = attn_ctas / (B * max_u_h);
+    int chunks = lc.nsm / (B * max_u_h);
     if (chunks < 1)
         chunks = 1;
     if (chunks > L1)
@@ -295,15 +298,10 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     if (chunks > kMaxAttnChunks)
         chunks = kMaxAttnChunks;
     t.splits = chunks;
-    t.split_len = ceil_div(L1, chunks);
     t.part = at<float>(ws, L.attn_part);
-    t.cnt = at<int>(ws, L.attn_cnt);
-    t.o = at<float>(ws, L.o);
     t.status = ctl;
-    if (ns) {
-        t.neuron_final = 1;
-        t.ns = *ns;
-    }
+    if (ns)
+        t.side_flag = ctl + kSideFlagWord;
     const int lpk = (int)((size_t)dh * esize(D.dtype) / 16);
     if ((s = lc.mark()))
         return s;
@@ -320,8 +318,8 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     c.sel_range = H;
     c.dh = dh;
     c.w = w.w_oT;
-    c.coef = at<float>(ws, L.o);
-    c.coef_ld = max_u_h * dh;
+    c.attn_rec = at<float>(ws, L.attn_part);
+    c.attn_C = chunks;
     c.res = x;
     c.bias = w.b_o;
     c.out = h1;
@@ -499,8 +497,6 @@ bool ws_layout(const dv_layer_desc &D, int B, WsLayout *L)
     L->s_n = take((size_t)B * N * 4);
     L->q = take((size_t)B * H * dh * 4);
     L->attn_part = take((size_t)B * H * splits * (kAttnRec + dh) * 4);
-    L->attn_cnt = take((size_t)B * H * 4);
-    L->o = take((size_t)B * H * dh * 4);
     L->h1 = take((size_t)B * d * 4);
     L->act = take((size_t)B * N * 4);
     L->part_pred1 = take(bp * kMaxWarps * 2 * 4);

@@ -13,15 +13,16 @@
 // warp scores 32/group keys per step (two batches of steps in flight),
 // reduces each dot product with xor shuffles inside its group and keeps a
 // running max / sum / weighted V (online softmax) per group.  Groups merge by
-// butterfly shuffles, the warps of the CTA merge in shared memory, and the
-// last chunk of a (batch row, head) to arrive combines the C chunk records in
-// chunk order.
+// butterfly shuffles and the warps of the CTA merge in shared memory into one
+// chunk record (max m, weight sum l, weighted V, not yet divided); the
+// out-projection kernel merges the C records of a head while it stages its
+// coefficients.
 //
-// In the fused decode, CTA 0 instead finishes the neuron selection
-// (dv_select.cuh, neuron_final): the selected neurons are needed only by the
-// fc1 kernel two launches later, so the selection overlaps the attention.
+// Only position kv_len (appended by the QKV kernel) and q depend on the
+// previous kernel; the head list was published before it (flag) or given by
+// the caller, and older positions of the cache are inputs.  So the first two
+// batches of K/V loads go out before the grid dependency is waited for.
 #include "dv_common.cuh"
-#include "dv_select.cuh"
 
 namespace dv {
 namespace {
@@ -35,26 +36,36 @@ __global__ void __launch_bounds__(kThreads) k_attn(const AttnArgs a)
     constexpr int DH = LPK * EPC;  // head dimension
     __shared__ float wm[kWarpsPerBlock], wl[kWarpsPerBlock];
     __shared__ __align__(16) float wo[kWarpsPerBlock][DH];
-    __shared__ int s_last;
+    __shared__ int s_ready;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int ks = lane / LPK, dc = lane % LPK;
     const int C = a.splits;  // chunks per (row, head)
     const int L1 = a.kv_len + 1;
     const T *Kc = static_cast<const T *>(a.kc);
     const T *Vc = static_cast<const T *>(a.vc);
-    pdl_wait();  // q, the appended K/V and the head union come from the previous kernel
-    pdl_launch_dependents();
+    bool waited = false;
+    if (a.side_flag) {
+        // the head union is published by the stage-2 predictor's side CTA
+        if (threadIdx.x == 0) {
+            int ok = 0;
+            for (int it = 0; it < kSideSpin && !ok; ++it) {
+                ok = ld_acquire_gpu(a.side_flag);
+                if (!ok)
+                    __nanosleep(128);
+            }
+            s_ready = ok;
+        }
+        __syncthreads();
+        if (!s_ready) {
+            pdl_wait();
+            pdl_launch_dependents();
+            waited = true;
+        }
+    }
     const int ns = min(max(ld_cg(a.n_sel), 0), a.max_sel);
     const int units = a.B * ns * C;
-    if (a.neuron_final && blockIdx.x == 0) {
-        extern __shared__ __align__(16) int fsm[];
-        __shared__ int fscr[48];
-        neuron_final(a.ns, final_smem(fsm, a.ns.N, fscr));
-        return;
-    }
-    const int cta0 = a.neuron_final ? 1 : 0;  // CTAs [cta0, gridDim.x) attend
 
-    for (int cu = blockIdx.x - cta0; cu < units; cu += gridDim.x - cta0) {
+    for (int cu = blockIdx.x; cu < units; cu += gridDim.x) {
         const int per_b = ns * C;
         const int b = cu / per_b, rem = cu - b * per_b;
         const int j = rem / C, c = rem - j * C;
@@ -67,41 +78,61 @@ __global__ void __launch_bounds__(kThreads) k_attn(const AttnArgs a)
         const int c0 = (int)((long long)L1 * c / C), c1 = (int)((long long)L1 * (c + 1) / C);
         const int p0 = c0 + (int)((long long)(c1 - c0) * warp / kWarpsPerBlock);
         const int p1 = c0 + (int)((long long)(c1 - c0) * (warp + 1) / kWarpsPerBlock);
+        const size_t base = ((size_t)b * a.H + h) * (size_t)a.kv_cap * DH + (size_t)dc * EPC;
+        // positions this lane loads before the wait: the cache's older ones
+        const int pre = waited ? p1 : min(p1, a.kv_len);
+        const int nbatch = (p1 - p0 + KPW * UK - 1) / (KPW * UK);
+        uint4 kc[UK], vc[UK], kn[UK], vn[UK];
+#pragma unroll
+        for (int uu = 0; uu < UK; ++uu) {
+            const int p = p0 + uu * KPW + ks;
+            kc[uu] = p < pre ? ld_stream(Kc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
+            vc[uu] = p < pre ? ld_stream(Vc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int uu = 0; uu < UK; ++uu) {
+            const int p = p0 + (UK + uu) * KPW + ks;
+            kn[uu] = p < pre ? ld_stream(Kc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
+            vn[uu] = p < pre ? ld_stream(Vc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (!waited) {
+            pdl_wait();  // q and the appended K/V come from the previous kernel
+            pdl_launch_dependents();
+            waited = true;
+            // the appended position, if it falls in the first two batches
+#pragma unroll
+            for (int uu = 0; uu < UK; ++uu) {
+                const int p = p0 + uu * KPW + ks;
+                if (p == a.kv_len && p < p1) {
+                    kc[uu] = ld_stream(Kc + base + (size_t)p * DH);
+                    vc[uu] = ld_stream(Vc + base + (size_t)p * DH);
+                }
+                const int pn = p0 + (UK + uu) * KPW + ks;
+                if (pn == a.kv_len && pn < p1) {
+                    kn[uu] = ld_stream(Kc + base + (size_t)pn * DH);
+                    vn[uu] = ld_stream(Vc + base + (size_t)pn * DH);
+                }
+            }
+        }
         float q[EPC];
         {
             const float *qp = a.q + ((size_t)b * a.max_sel + j) * DH + dc * EPC;
 #pragma unroll
             for (int e = 0; e < EPC; e += 4) {
-                const float4 t = *reinterpret_cast<const float4 *>(qp + e);
+                const float4 t = __ldcg(reinterpret_cast<const float4 *>(qp + e));
                 q[e] = t.x;
                 q[e + 1] = t.y;
                 q[e + 2] = t.z;
                 q[e + 3] = t.w;
             }
         }
-        const size_t base = ((size_t)b * a.H + h) * (size_t)a.kv_cap * DH + (size_t)dc * EPC;
         float m = -INFINITY, l = 0.f, o[EPC];
 #pragma unroll
         for (int e = 0; e < EPC; ++e)
             o[e] = 0.f;
 
-        const int nbatch = (p1 - p0 + KPW * UK - 1) / (KPW * UK);
-        uint4 kc[UK], vc[UK];
-#pragma unroll
-        for (int uu = 0; uu < UK; ++uu) {
-            const int p = p0 + uu * KPW + ks;
-            kc[uu] = p < p1 ? ld_stream(Kc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
-            vc[uu] = p < p1 ? ld_stream(Vc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
-        }
         for (int bt = 0; bt < nbatch; ++bt) {
             const int pb = p0 + bt * KPW * UK;
-            uint4 kn[UK], vn[UK];
-#pragma unroll
-            for (int uu = 0; uu < UK; ++uu) {
-                const int p = pb + KPW * UK + uu * KPW + ks;
-                kn[uu] = p < p1 ? ld_stream(Kc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
-                vn[uu] = p < p1 ? ld_stream(Vc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
-            }
 #pragma unroll
             for (int uu = 0; uu < UK; ++uu) {
                 const int p = pb + uu * KPW + ks;
@@ -127,10 +158,15 @@ __global__ void __launch_bounds__(kThreads) k_attn(const AttnArgs a)
                     m = mn;
                 }
             }
+            // the next batch moves up; the one after it is loaded (the waited
+            // state holds here, so every position may be read)
 #pragma unroll
             for (int uu = 0; uu < UK; ++uu) {
                 kc[uu] = kn[uu];
                 vc[uu] = vn[uu];
+                const int p = pb + 2 * KPW * UK + uu * KPW + ks;
+                kn[uu] = p < p1 ? ld_stream(Kc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
+                vn[uu] = p < p1 ? ld_stream(Vc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
             }
         }
         // merge the key groups of the warp (butterfly: every lane ends with the total)
@@ -159,7 +195,7 @@ __global__ void __launch_bounds__(kThreads) k_attn(const AttnArgs a)
             wl[warp] = l;
         }
         __syncthreads();
-        // combine the warps of the CTA (thread t owns dimension t)
+        // combine the warps of the CTA (thread t owns dimension t) into the record
         float M = -INFINITY;
         for (int w = 0; w < kWarpsPerBlock; ++w)
             M = fmaxf(M, wm[w]);
@@ -171,70 +207,26 @@ __global__ void __launch_bounds__(kThreads) k_attn(const AttnArgs a)
         if (t < DH)
             for (int w = 0; w < kWarpsPerBlock; ++w)
                 Ot += (wm[w] == -INFINITY) ? 0.f : wo[w][t] * expf(wm[w] - M);
-        float *dst = a.o + ((size_t)b * a.max_sel + j) * DH;
-        if (C == 1) {
-            if (t < DH)
-                dst[t] = Ot / Ls;
-            __syncthreads();
-            continue;
-        }
         const int rec = kAttnRec + DH;
-        float *recs = a.part + ((size_t)b * a.max_sel + j) * C * rec;
+        float *r = a.part + (((size_t)b * a.max_sel + j) * C + c) * rec;
         if (t < DH)
-            recs[(size_t)c * rec + kAttnRec + t] = Ot;
+            r[kAttnRec + t] = Ot;
         if (t == 0) {
-            recs[(size_t)c * rec] = M;
-            recs[(size_t)c * rec + 1] = Ls;
-        }
-        __threadfence();
-        __syncthreads();
-        int *cnt = a.cnt + (size_t)b * a.max_sel + j;
-        if (t == 0)
-            s_last = (atomicAdd(cnt, 1) == C - 1);
-        __syncthreads();
-        if (s_last) {
-            __threadfence();
-            if (t < DH) {
-                float MM = -INFINITY;
-                for (int cc = 0; cc < C; ++cc)
-                    MM = fmaxf(MM, __ldcg(recs + (size_t)cc * rec));
-                float LL = 0.f, OO = 0.f;
-                for (int cc = 0; cc < C; ++cc) {
-                    const float *r = recs + (size_t)cc * rec;
-                    const float w = expf(__ldcg(r) - MM);
-                    LL = fmaf(__ldcg(r + 1), w, LL);
-                    OO = fmaf(__ldcg(r + kAttnRec + t), w, OO);
-                }
-                dst[t] = OO / LL;
-            }
-            if (t == 0)
-                *cnt = 0;
+            r[0] = M;
+            r[1] = Ls;
         }
         __syncthreads();
+    }
+    if (!waited) {  // no unit: still order this grid after the previous one
+        pdl_wait();
+        pdl_launch_dependents();
     }
 }
 
 template <typename T, int LPK>
 cudaError_t launch_attn_one(const AttnArgs &a, cudaLaunchConfig_t &cfg)
 {
-    auto kern = k_attn<T, LPK>;
-    // shared-memory opt-in once per device (launches may later be captured)
-    static bool configured[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return e;
-    if (dev < 0 || dev >= kMaxDevices)
-        return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap);
-        if (e != cudaSuccess)
-            return e;
-        configured[dev] = true;
-    }
-    if (cfg.dynamicSmemBytes > kSmemCap)
-        return cudaErrorInvalidValue;
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    return cudaLaunchKernelEx(&cfg, k_attn<T, LPK>, a);
 }
 
 template <typename T>
@@ -243,7 +235,7 @@ cudaError_t dispatch_lpk(int lpk, const AttnArgs &a, dim3 grid, cudaStream_t st,
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = a.neuron_final ? neuron_final_smem_bytes(a.ns.N) : 0;
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

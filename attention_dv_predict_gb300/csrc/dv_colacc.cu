@@ -27,6 +27,7 @@ namespace {
 constexpr int kStageRows = 256;  // rows whose offsets and coefficients are staged at once
 constexpr int kMaxCover = 512;   // CTAs that may share one column block
 constexpr int kCoverBatch = 8;   // partials loaded together by the combining CTA
+constexpr int kRecBatch = 8;     // attention chunk records loaded together
 
 template <int KIND>
 DV_DEV long long row_offset(const ColArgs &a, int i)
@@ -39,6 +40,55 @@ DV_DEV long long row_offset(const ColArgs &a, int i)
         return ((long long)h * a.dh + (i - j * a.dh)) * a.d;
     else
         return (long long)h * a.d;
+}
+
+// Coefficient of row i for batch row b.  FC2: the fc1 activation.  OPROJ:
+// attention output o[b][j][e] (i = j*dh + e), merged from the attention
+// kernel's C chunk records (m, l, weighted V) of head slot j:
+//   o = sum_c exp(m_c - M) V_c[e] / sum_c exp(m_c - M) l_c,  M = max_c m_c.
+template <int KIND>
+DV_DEV float coef_at(const ColArgs &a, int b, int i)
+{
+    if constexpr (KIND == CK_OPROJ) {
+        // the records were written by the previous kernel (read at L2); loads
+        // in batches of kRecBatch chunks
+        const int j = i / a.dh, e = i - j * a.dh;
+        const int C = a.attn_C, rec = kAttnRec + a.dh;
+        const float *r = a.attn_rec + ((size_t)b * a.max_sel + j) * C * rec;
+        float MM = -INFINITY;
+        for (int c0 = 0; c0 < C; c0 += kRecBatch) {
+            float m[kRecBatch];
+#pragma unroll
+            for (int u = 0; u < kRecBatch; ++u)
+                m[u] = c0 + u < C ? __ldcg(r + (size_t)(c0 + u) * rec) : -INFINITY;
+#pragma unroll
+            for (int u = 0; u < kRecBatch; ++u)
+                MM = fmaxf(MM, m[u]);
+        }
+        float LL = 0.f, OO = 0.f;
+        for (int c0 = 0; c0 < C; c0 += kRecBatch) {
+            float m[kRecBatch], l[kRecBatch], o[kRecBatch];
+#pragma unroll
+            for (int u = 0; u < kRecBatch; ++u) {
+                const float *rc = r + (size_t)(c0 + u) * rec;
+                const bool in = c0 + u < C;
+                m[u] = in ? __ldcg(rc) : 0.f;
+                l[u] = in ? __ldcg(rc + 1) : 0.f;
+                o[u] = in ? __ldcg(rc + kAttnRec + e) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < kRecBatch; ++u) {
+                if (c0 + u >= C)
+                    break;
+                const float w = expf(m[u] - MM);
+                LL = fmaf(l[u], w, LL);
+                OO = fmaf(o[u], w, OO);
+            }
+        }
+        return OO / LL;
+    } else {
+        return a.coef[(size_t)b * a.coef_ld + i];
+    }
 }
 
 // CTA whose piece range holds piece p.
@@ -134,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_colacc(const ColArgs a)
 #pragma unroll
                 for (int b = 0; b < NB; ++b)
                     scoef[(i - s0) * NB + b] =
-                        (b0 + b < a.B) ? a.coef[(size_t)(b0 + b) * a.coef_ld + i] : 0.f;
+                        (b0 + b < a.B) ? coef_at<KIND>(a, b0 + b, i) : 0.f;
             }
             __syncthreads();
             // warp w takes rows s0 + w + 16 t; R rows per batch, two batches in flight

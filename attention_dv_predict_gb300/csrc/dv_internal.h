@@ -105,15 +105,15 @@ struct RowArgs {
     float *part;          // range-boundary partials [tiles][warps][2][NB]
     int *rowcnt;          // segments accounted per row [tiles][max_rows], zero at rest
     int *hist;            // PRED2: first-digit histogram [B][kTopkBins], zero at rest
-    // PRED2 only: the last CTA column does the side work (PredSide) instead of rows
+    // Fused decode only: the last CTA column does side work instead of rows --
+    // PRED2: head selection and norm(x) (PredSide); QKV: the whole neuron
+    // selection (NeuronSel), after waiting for the stage-2 grid.
     int side_cta;
     PredSide side;
-    // fused decode: PRED1 clears it, PRED2's side CTA sets it once its results
-    // are published, the QKV kernel starts on it instead of the grid dependency
-    int *side_flag;
-    // QKV only: neuron selection pass over the scores after the main loop
-    int neuron_pass;
     NeuronSel ns;
+    // fused decode: PRED1 clears it, PRED2's side CTA sets it once its results
+    // are published; the QKV kernel starts on it instead of the grid dependency
+    int *side_flag;
     int *status;
 };
 
@@ -128,8 +128,12 @@ struct ColArgs {
     int sel_range;
     int dh;
     const void *w;        // w_oT or w2T
-    const float *coef;    // [B][coef_ld]
+    const float *coef;    // FC2: [B][coef_ld]
     int coef_ld;
+    // OPROJ: the attention kernel's chunk records [B][max_sel][attn_C][kAttnRec + dh]
+    // (running max, sum of weights, weighted V), merged into the coefficients
+    const float *attn_rec;
+    int attn_C;
     const float *res;     // [B][d]
     const void *bias;     // [d]
     float *out;           // [B][d]
@@ -151,12 +155,9 @@ struct AttnArgs {
     const int32_t *sel;
     const float *q;       // [B][max_sel][dh], already scaled
     const void *kc, *vc;  // [B][H][kv_cap][dh]
-    int splits, split_len;  // chunks per (batch row, head) and their nominal length
-    float *part;          // [B][max_sel][splits][kAttnRec + dh]
-    int *cnt;             // [B][max_sel], zero at rest
-    float *o;             // [B][max_sel][dh]
-    int neuron_final;     // CTA 0 finishes the neuron selection instead of attending
-    NeuronSel ns;
+    int splits;           // chunks per (batch row, head)
+    float *part;          // out: chunk records [B][max_sel][splits][kAttnRec + dh]
+    const int *side_flag; // fused decode: set once the head union is published
     int *status;
 };
 
@@ -166,7 +167,7 @@ struct WsLayout {
     size_t ctl;       // int[64]: [0] status
     size_t hist;      // int[B][kTopkBins]
     size_t s_h, u, s_n;
-    size_t q, attn_part, attn_cnt, o;
+    size_t q, attn_part;  // attention chunk records [B][H][splits][kAttnRec + dh]
     size_t h1, act;
     size_t part_pred1, part_qkv, part_fc1;
     size_t cnt_pred1, cnt_qkv, cnt_fc1;

@@ -391,10 +391,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot(const RowArgs a)
         }
     }
     if constexpr (KIND == RK_QKV) {
+        if (a.side_cta) {
+            ncta = gridDim.x - 1;
+            if (blockIdx.x == ncta) {
+                // the last CTA selects the neurons instead: it needs the whole
+                // stage-2 grid (scores and histogram)
+                pdl_wait();
+                pdl_launch_dependents();
+                if (tile == 0) {
+                    __shared__ int nscr[48];
+                    neuron_select_cta(a.ns, final_smem(smem, a.ns.N, nscr));
+                }
+                return;
+            }
+        }
         if (a.side_flag) {
             // the head union and norm(x) come from the previous kernel's side
             // CTA: start as soon as it has published them (bounded polling,
-            // then the grid dependency)
+            // then the grid dependency).  The dependents may launch now: the
+            // attention kernel reads only flag-published data before its wait.
             __shared__ int s_ready;
             if (threadIdx.x == 0) {
                 int ok = 0;
@@ -408,6 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot(const RowArgs a)
             __syncthreads();
             if (!s_ready)
                 pdl_wait();
+            pdl_launch_dependents();
         } else {  // the head union was given by the caller
             pdl_wait();
             pdl_launch_dependents();
@@ -596,21 +612,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot(const RowArgs a)
             const int v = shist[i];
             if (v && b0 + bi < a.B)
                 atomicAdd(&a.hist[(size_t)(b0 + bi) * kTopkBins + (i - bi * kTopkBins)], v);
-        }
-    }
-    if constexpr (KIND == RK_QKV) {
-        if (a.side_flag) {  // the neuron scores and their histogram: the whole grid
-            pdl_wait();
-            pdl_launch_dependents();
-        }
-        if (a.neuron_pass && tile == 0) {
-            __shared__ int sb1[DV_MAX_BATCH];
-            __shared__ int hbuf[kTopkBins];
-            __shared__ int nscr[48];
-            const int W = (a.ns.N + 31) >> 5;
-            const int w0 = (int)((long long)W * blockIdx.x / gridDim.x);
-            const int w1 = (int)((long long)W * (blockIdx.x + 1) / gridDim.x);
-            neuron_pass(a.ns, w0, w1, sb1, hbuf, nscr);
         }
     }
 }

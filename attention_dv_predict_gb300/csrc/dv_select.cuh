@@ -26,6 +26,7 @@ namespace dv {
 
 constexpr int kHeadTopkMax = 256;   // head select handles n <= 256 (8 keys per lane)
 constexpr int kHeadKPL = kHeadTopkMax / 32;
+constexpr int kScanBatch = 8;    // 16-byte score loads per thread in flight in neuron_select_cta
 
 // Bitmap words (bits[q] for elements q*32 + lane) of the k largest of
 // s[0..n), ties to the lower index.  One warp; n <= kHeadTopkMax.
@@ -273,7 +274,96 @@ DV_DEV void neuron_overflow(const float *s, int N, unsigned prefix, int krem, co
     __syncthreads();
 }
 
-// Finish the selection of every row and write idx_n, u_n, n_u_n; leave the
+// Finish row b: sm.rowbits holds the keys above bin b1, sm.ckey / sm.cidx the
+// ncand keys inside it (all of them when ncand <= kTopkCand; else the row is
+// finished from the global scores).  Selects the krem largest candidates
+// (ties to the lower index), adds the row to sm.ubits and writes idx_n[b].
+DV_DEV void neuron_row_finish(const NeuronSel &ns, int b, unsigned b1, int krem, int ncand,
+                              const FinalSmem &sm)
+{
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int W = (ns.N + 31) >> 5;
+    if (ncand > kTopkCand) {
+        neuron_overflow(ns.s_n + (size_t)b * ns.N, ns.N, b1 << 21, krem, sm);
+    } else {
+        unsigned prefix = b1 << 21, pmask = 0xffe00000u;
+        int kr = krem;
+        const int shifts[2] = {10, 0};
+        const int widths[2] = {11, 10};
+        for (int pass = 0; pass < 2; ++pass) {
+            const int shift = shifts[pass], nbins = 1 << widths[pass];
+            for (int i = tid; i < nbins; i += nt)
+                sm.hist[i] = 0;
+            __syncthreads();
+            for (int i = tid; i < ncand; i += nt) {
+                const unsigned key = sm.ckey[i];
+                if ((key & pmask) == prefix)
+                    atomicAdd(&sm.hist[(key >> shift) & (unsigned)(nbins - 1)], 1);
+            }
+            __syncthreads();
+            block_find_bin(sm.hist, nbins, kr, sm.scr);
+            prefix |= (unsigned)sm.scr[0] << shift;
+            pmask |= (unsigned)(nbins - 1) << shift;
+            kr = sm.scr[1];
+            __syncthreads();
+        }
+        const unsigned T = prefix;
+        const int need_eq = kr;
+        const int n_eq = sm.hist[T & 1023u];  // candidates equal to T
+        for (int i = tid; i < ncand; i += nt) {
+            const unsigned key = sm.ckey[i];
+            bool keep = key > T;
+            if (key == T) {
+                if (n_eq == need_eq) {
+                    keep = true;
+                } else {
+                    const int idx = sm.cidx[i];
+                    int rank = 0;
+                    for (int q = 0; q < ncand; ++q)
+                        rank += (sm.ckey[q] == T && sm.cidx[q] < idx);
+                    keep = rank < need_eq;
+                }
+            }
+            if (keep) {
+                const int idx = sm.cidx[i];
+                atomicOr(&sm.rowbits[idx >> 5], 1u << (idx & 31));
+            }
+        }
+        __syncthreads();
+    }
+    for (int i = tid; i < W; i += nt)
+        sm.ubits[i] |= sm.rowbits[i];
+    block_compact_bits(sm.rowbits, W, ns.idx_n + (size_t)b * ns.k, sm.scr);
+}
+
+// Union of the rows (sm.ubits) to u_n / n_u_n.
+DV_DEV void neuron_union_out(const NeuronSel &ns, const FinalSmem &sm)
+{
+    const int W = (ns.N + 31) >> 5;
+    __syncthreads();
+    const int tot = block_compact_bits(sm.ubits, W, ns.u_n, sm.scr);
+    if (threadIdx.x == 0)
+        *ns.n_u_n = tot;
+}
+
+// Bin b1 of the k-th largest key of row b and the rank krem left inside it,
+// from the row's global first-digit histogram (staged in sm.hist).
+DV_DEV void neuron_row_bin(const NeuronSel &ns, int b, const FinalSmem &sm, unsigned *b1,
+                           int *krem)
+{
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int *ghist = ns.hist + (size_t)b * kTopkBins;
+    for (int i = tid; i < kTopkBins; i += nt)
+        sm.hist[i] = __ldcg(ghist + i);
+    __syncthreads();
+    block_find_bin(sm.hist, kTopkBins, ns.k, sm.scr);
+    *b1 = (unsigned)sm.scr[0];
+    *krem = sm.scr[1];
+    __syncthreads();  // every thread holds b1, krem before scr is reused
+}
+
+// Finish the selection of every row from the bitmaps and candidate lists of
+// the distributed pass (neuron_pass) and write idx_n, u_n, n_u_n; leave the
 // histogram and candidate counts zero.  One whole CTA; smem as FinalSmem.
 DV_DEV void neuron_final(const NeuronSel &ns, const FinalSmem &sm)
 {
@@ -282,83 +372,109 @@ DV_DEV void neuron_final(const NeuronSel &ns, const FinalSmem &sm)
     for (int i = tid; i < W; i += nt)
         sm.ubits[i] = 0u;
     for (int b = 0; b < ns.B; ++b) {
-        int *ghist = ns.hist + (size_t)b * kTopkBins;
-        for (int i = tid; i < kTopkBins; i += nt)
-            sm.hist[i] = __ldcg(ghist + i);
         const unsigned *gbits = ns.rowbits + (size_t)b * W;
         for (int i = tid; i < W; i += nt)
             sm.rowbits[i] = __ldcg(gbits + i);
-        __syncthreads();
-        block_find_bin(sm.hist, kTopkBins, ns.k, sm.scr);
-        const unsigned b1 = (unsigned)sm.scr[0];
-        const int krem = sm.scr[1];
-        __syncthreads();  // every thread holds b1, krem before scr is reused
+        unsigned b1;
+        int krem;
+        neuron_row_bin(ns, b, sm, &b1, &krem);
         const int ncand = __ldcg(ns.cand_cnt + b);
-        if (ncand > kTopkCand) {
-            neuron_overflow(ns.s_n + (size_t)b * ns.N, ns.N, b1 << 21, krem, sm);
-        } else {
+        if (ncand <= kTopkCand)
             for (int i = tid; i < ncand; i += nt) {
                 sm.ckey[i] = __ldcg(ns.cand_key + (size_t)b * kTopkCand + i);
                 sm.cidx[i] = __ldcg(ns.cand_idx + (size_t)b * kTopkCand + i);
             }
-            unsigned prefix = b1 << 21, pmask = 0xffe00000u;
-            int kr = krem;
-            const int shifts[2] = {10, 0};
-            const int widths[2] = {11, 10};
-            for (int pass = 0; pass < 2; ++pass) {
-                const int shift = shifts[pass], nbins = 1 << widths[pass];
-                for (int i = tid; i < nbins; i += nt)
-                    sm.hist[i] = 0;
-                __syncthreads();
-                for (int i = tid; i < ncand; i += nt) {
-                    const unsigned key = sm.ckey[i];
-                    if ((key & pmask) == prefix)
-                        atomicAdd(&sm.hist[(key >> shift) & (unsigned)(nbins - 1)], 1);
-                }
-                __syncthreads();
-                block_find_bin(sm.hist, nbins, kr, sm.scr);
-                prefix |= (unsigned)sm.scr[0] << shift;
-                pmask |= (unsigned)(nbins - 1) << shift;
-                kr = sm.scr[1];
-                __syncthreads();
-            }
-            const unsigned T = prefix;
-            const int need_eq = kr;
-            const int n_eq = sm.hist[T & 1023u];  // candidates equal to T
-            for (int i = tid; i < ncand; i += nt) {
-                const unsigned key = sm.ckey[i];
-                bool keep = key > T;
-                if (key == T) {
-                    if (n_eq == need_eq) {
-                        keep = true;
-                    } else {
-                        const int idx = sm.cidx[i];
-                        int rank = 0;
-                        for (int q = 0; q < ncand; ++q)
-                            rank += (sm.ckey[q] == T && sm.cidx[q] < idx);
-                        keep = rank < need_eq;
-                    }
-                }
-                if (keep) {
-                    const int idx = sm.cidx[i];
-                    atomicOr(&sm.rowbits[idx >> 5], 1u << (idx & 31));
-                }
-            }
-            __syncthreads();
-        }
-        for (int i = tid; i < W; i += nt)
-            sm.ubits[i] |= sm.rowbits[i];
-        block_compact_bits(sm.rowbits, W, ns.idx_n + (size_t)b * ns.k, sm.scr);
+        neuron_row_finish(ns, b, b1, krem, ncand, sm);
         // leave this row's shared state zero for the next call
+        int *ghist = ns.hist + (size_t)b * kTopkBins;
         for (int i = tid; i < kTopkBins; i += nt)
             ghist[i] = 0;
         if (tid == 0)
             ns.cand_cnt[b] = 0;
         __syncthreads();
     }
-    const int tot = block_compact_bits(sm.ubits, W, ns.u_n, sm.scr);
-    if (tid == 0)
-        *ns.n_u_n = tot;
+    neuron_union_out(ns, sm);
+}
+
+// The whole neuron selection in one CTA: for every row, the bin of the k-th
+// key from the global histogram, one pass over the row's scores into
+// shared-memory bitmaps and candidates, then the finish.  Leaves the global
+// histogram zero.  smem as FinalSmem.  Each thread reads 4 consecutive
+// scores per load (16 bytes when the row is 16-byte aligned) and kScanBatch
+// such groups at a time, so few requests carry the row even when the memory
+// system is busy.
+static __device__ __noinline__ void neuron_select_cta(const NeuronSel &ns, const FinalSmem &sm)
+{
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int W = (ns.N + 31) >> 5;
+    const int G = (ns.N + 3) >> 2;  // groups of 4 scores
+    const bool vec = (ns.N & 3) == 0;
+    for (int i = tid; i < W; i += nt)
+        sm.ubits[i] = 0u;
+    for (int b = 0; b < ns.B; ++b) {
+        const float *s = ns.s_n + (size_t)b * ns.N;
+        // the row's histogram first (one 16-byte load per thread), then the bin
+        const int4 *gh4 = reinterpret_cast<const int4 *>(ns.hist + (size_t)b * kTopkBins);
+        for (int i = tid; i < kTopkBins / 4; i += nt)
+            reinterpret_cast<int4 *>(sm.hist)[i] = __ldcg(gh4 + i);
+        for (int i = tid; i < W; i += nt)
+            sm.rowbits[i] = 0u;
+        if (tid == 0)
+            sm.scr[44] = 0;  // candidate count
+        __syncthreads();
+        block_find_bin(sm.hist, kTopkBins, ns.k, sm.scr);
+        const unsigned b1 = (unsigned)sm.scr[0];
+        const int krem = sm.scr[1];
+        __syncthreads();
+        for (int g0 = tid; g0 < G; g0 += nt * kScanBatch) {
+            float v[kScanBatch][4];
+#pragma unroll
+            for (int u = 0; u < kScanBatch; ++u) {
+                const int g = g0 + u * nt;
+                if (vec) {
+                    const float4 t = g < G ? __ldcg(reinterpret_cast<const float4 *>(s) + g)
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[u][0] = t.x;
+                    v[u][1] = t.y;
+                    v[u][2] = t.z;
+                    v[u][3] = t.w;
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        v[u][q] = 4 * g + q < ns.N ? ld_cg(s + 4 * g + q) : 0.f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kScanBatch; ++u) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int i = 4 * (g0 + u * nt) + q;
+                    if (i >= ns.N)
+                        continue;
+                    const unsigned key = score_key(v[u][q]);
+                    const unsigned d = key >> 21;
+                    if (d > b1) {
+                        atomicOr(&sm.rowbits[i >> 5], 1u << (i & 31));
+                    } else if (d == b1) {
+                        const int pos = atomicAdd(&sm.scr[44], 1);
+                        if (pos < kTopkCand) {
+                            sm.ckey[pos] = key;
+                            sm.cidx[pos] = i;
+                        }
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        const int ncand = sm.scr[44];
+        __syncthreads();
+        neuron_row_finish(ns, b, b1, krem, ncand, sm);
+        int *ghist = ns.hist + (size_t)b * kTopkBins;
+        for (int i = tid; i < kTopkBins; i += nt)
+            ghist[i] = 0;
+        __syncthreads();
+    }
+    neuron_union_out(ns, sm);
 }
 
 DV_DEV FinalSmem final_smem(void *base, int N, int *scr)

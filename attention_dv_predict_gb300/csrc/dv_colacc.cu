@@ -91,12 +91,27 @@ DV_DEV float coef_at(const ColArgs &a, int b, int i)
     }
 }
 
-// CTA whose piece range holds piece p.
-DV_DEV int cta_of(long long total, int nc, long long p)
+// Work split.  Pieces are (column block, row); CTA c takes pieces [p0, p1).
+// With no more column blocks than CTAs, block cb is shared by CTAs
+// [first_cta(cb), first_cta(cb + 1)), which split its rows evenly, so no
+// CTA straddles two blocks; otherwise every CTA takes whole blocks.
+DV_DEV int first_cta(int cb, int nc, int ncb)
 {
-    return (int)(((p + 1) * nc - 1) / total);
+    return (int)(((long long)cb * nc + ncb - 1) / ncb);
 }
-DV_DEV long long piece_start(long long total, int nc, int c) { return total * c / nc; }
+DV_DEV void cta_pieces(int c, int nc, int ncb, int rows, long long *p0, long long *p1)
+{
+    if (ncb <= nc) {
+        const int cb = (int)((long long)c * ncb / nc);
+        const int f = first_cta(cb, nc, ncb), m = first_cta(cb + 1, nc, ncb) - f;
+        const int r = c - f;
+        *p0 = (long long)cb * rows + (long long)rows * r / m;
+        *p1 = (long long)cb * rows + (long long)rows * (r + 1) / m;
+    } else {
+        *p0 = (long long)((long long)c * ncb / nc) * rows;
+        *p1 = (long long)((long long)(c + 1) * ncb / nc) * rows;
+    }
+}
 
 template <typename T, int NB, int P>
 DV_DEV void write_out(const ColArgs &a, int b0, int col, const float (&v)[NB])
@@ -148,9 +163,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_colacc(const ColArgs a)
         return;
     }
 
-    const long long p0 = piece_start(total, nc, blockIdx.x);
-    const long long p1 = piece_start(total, nc, blockIdx.x + 1);
+    long long p0, p1;
+    cta_pieces(blockIdx.x, nc, ncb, rows, &p0, &p1);
     const int first_cb = (int)(p0 / rows);
+    const int last_cb = p1 > p0 ? (int)((p1 - 1) / rows) : first_cb;
+    // residual + bias of the columns of this CTA's first and last column
+    // blocks (the ones it may have to finish), read before the grid wait:
+    // both are inputs or come from kernels at least two launches back
+    float rb0[CPT][NB], rb1[CPT][NB];
+#pragma unroll
+    for (int k = 0; k < CPT; ++k) {
+        const int bc = tid + k * kThreads;
+        const int c0 = first_cb * CB + bc, c1 = last_cb * CB + bc;
+        const bool in0 = p1 > p0 && bc < CB && c0 < a.d;
+        const bool in1 = p1 > p0 && bc < CB && c1 < a.d;
+        const float bias0 = in0 ? Elem<T>::load(static_cast<const T *>(a.bias), (size_t)c0) : 0.f;
+        const float bias1 = in1 ? Elem<T>::load(static_cast<const T *>(a.bias), (size_t)c1) : 0.f;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const bool bin = b0 + b < a.B;
+            rb0[k][b] = (in0 && bin) ? a.res[(size_t)(b0 + b) * a.d + c0] + bias0 : 0.f;
+            rb1[k][b] = (in1 && bin) ? a.res[(size_t)(b0 + b) * a.d + c1] + bias1 : 0.f;
+        }
+    }
     bool waited = false;  // griddepcontrol.wait done (uniform over the CTA)
     for (long long pp = p0; pp < p1;) {
         const int cb = (int)(pp / rows);
@@ -292,16 +327,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_colacc(const ColArgs a)
         if (!s_last)
             continue;
         __threadfence();
-        // the CTAs covering block cb and the slot each used, in CTA order
+        // the CTAs sharing block cb (each used its slot 0), in CTA order
         if (tid < 32) {
-            const int ca = cta_of(total, nc, (long long)cb * rows);
-            const int cz = cta_of(total, nc, (long long)cb * rows + rows - 1);
+            const int ca = first_cta(cb, nc, ncb), cz = first_cta(cb + 1, nc, ncb) - 1;
             for (int c = ca + tid; c <= cz; c += 32) {
-                const long long st = piece_start(total, nc, c);
-                const bool live = st < piece_start(total, nc, c + 1);
-                const int sl = (st / rows == cb) ? 0 : 1;
+                long long q0, q1;
+                cta_pieces(c, nc, ncb, rows, &q0, &q1);
                 if (c - ca < kMaxCover)
-                    s_cover[c - ca] = live ? (c * 2 + sl) : -1;
+                    s_cover[c - ca] = q1 > q0 ? c * 2 : -1;
             }
             if (tid == 0)
                 s_ncover = min(cz - ca + 1, kMaxCover);
@@ -338,7 +371,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_colacc(const ColArgs a)
                         for (int b = 0; b < NB; ++b)
                             s[b] += v[u][b];
             }
-            write_out<T, NB, P>(a, b0, cb * CB + col, s);
+            const int oc = cb * CB + col;
+            if (oc < a.d) {
+#pragma unroll
+                for (int b = 0; b < NB; ++b)
+                    if (b0 + b < a.B)
+                        a.out[(size_t)(b0 + b) * a.d + oc] =
+                            (cb == first_cb ? rb0[k][b] : rb1[k][b]) + s[b];
+            }
         }
         if (tid == 0)
             a.cnt[(size_t)tile * ncb + cb] = 0;

@@ -146,10 +146,13 @@ NeuronSel make_neuron_sel(const dv_layer_desc &D, int B, int kn, const dv_select
 }
 
 // PRED1 (head scores, low-rank factor u) and PRED2 (neuron scores +
-// first-digit histogram).  PRED1 is the first launch of the call.
+// first-digit histogram).  pdl_first: PRED1 is launched as a programmatic
+// dependent of the previous kernel on the stream and reads its weight rows
+// before its grid wait (the weights must not be written by a preceding kernel
+// that triggers its dependents early; no kernel of this library writes them).
 dv_status run_scores(const dv_layer_desc &D, const dv_layer_weights &w, const float *xp, int B,
                      float *sh_user, float *sn_user, void *ws, const WsLayout &L, Launch &lc,
-                     const PredSide *side = nullptr)
+                     const PredSide *side = nullptr, bool pdl_first = false)
 {
     const int d = D.d_model, H = D.n_heads, N = D.d_ffn, r = D.pred_rank;
     int *ctl = at<int>(ws, L.ctl);
@@ -179,7 +182,7 @@ dv_status run_scores(const dv_layer_desc &D, const dv_layer_weights &w, const fl
     if (s)
         return s;
     if (launch_rowdot(RK_PRED1, D.dtype, nb, a, grid, rowdot_smem(RK_PRED1, nb, d), lc.st,
-                      false) != cudaSuccess)
+                      pdl_first) != cudaSuccess)
         return DV_ERR_CUDA;
 
     RowArgs b2;
@@ -417,7 +420,7 @@ dv_status layer_decode_impl(const dv_layer_desc *desc, const dv_layer_weights *w
                             const float *x_pred, int batch, int k_heads, int k_neurons, void *kc,
                             void *vc, int kv_len, const dv_selection *sel, float *h1, float *y,
                             void *ws, size_t ws_bytes, void *const *events, int n_events,
-                            void *stream)
+                            void *stream, bool pdl_first)
 {
     dv_status s = check_desc(desc);
     if (s)
@@ -459,7 +462,8 @@ dv_status layer_decode_impl(const dv_layer_desc *desc, const dv_layer_weights *w
     side.norm_kind = D.norm;
     side.eps = D.ln_eps;
     side.xn = at<float>(ws, L.xn);
-    if ((s = run_scores(D, *w, x_pred ? x_pred : x, batch, nullptr, nullptr, ws, L, lc, &side)))
+    if ((s = run_scores(D, *w, x_pred ? x_pred : x, batch, nullptr, nullptr, ws, L, lc, &side,
+                        pdl_first)))
         return s;
     if ((s = run_attn(D, *w, x, batch, sel->u_h, sel->n_u_h, max_u_h, kc, vc, kv_len, h1p, ws, L,
                       lc, false, &ns)))
@@ -611,7 +615,7 @@ int dv_predict_topk(const dv_layer_desc *desc, const dv_layer_weights *w, const 
     Launch lc;
     if ((s = make_launch(stream, nullptr, 0, &lc)))
         return s;
-    if ((s = run_scores(D, *w, x_pred, batch, scores_h, scores_n, ws, L, lc)))
+    if ((s = run_scores(D, *w, x_pred, batch, scores_h, scores_n, ws, L, lc, nullptr, true)))
         return s;
     SelectArgs sa;
     std::memset(&sa, 0, sizeof(sa));
@@ -683,7 +687,7 @@ int dv_layer_decode(const dv_layer_desc *desc, const dv_layer_weights *w, const 
                     void *ws, size_t ws_bytes, void *stream)
 {
     return layer_decode_impl(desc, w, x, x_pred, batch, k_heads, k_neurons, k_cache, v_cache,
-                             kv_len, sel, h1, y, ws, ws_bytes, nullptr, 0, stream);
+                             kv_len, sel, h1, y, ws, ws_bytes, nullptr, 0, stream, true);
 }
 
 int dv_layer_decode_traced(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x,
@@ -698,7 +702,7 @@ int dv_layer_decode_traced(const dv_layer_desc *desc, const dv_layer_weights *w,
         if (!events[i])
             return DV_ERR_INVALID_ARG;
     return layer_decode_impl(desc, w, x, x_pred, batch, k_heads, k_neurons, k_cache, v_cache,
-                             kv_len, sel, h1, y, ws, ws_bytes, events, n_events, stream);
+                             kv_len, sel, h1, y, ws, ws_bytes, events, n_events, stream, false);
 }
 
 int dv_layer_decode_host(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x_host,
@@ -735,7 +739,7 @@ int dv_layer_decode_host(const dv_layer_desc *desc, const dv_layer_weights *w, c
         sel = &own;
     }
     s = layer_decode_impl(desc, w, x_dev, xp_dev, batch, k_heads, k_neurons, k_cache, v_cache,
-                          kv_len, sel, nullptr, y_dev, ws, ws_bytes, nullptr, 0, stream);
+                          kv_len, sel, nullptr, y_dev, ws, ws_bytes, nullptr, 0, stream, false);
     if (s)
         return s;
     if (cudaMemcpyAsync(y_host, y_dev, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)

@@ -366,12 +366,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot(const RowArgs a)
     float *xs = smem;
     int *shist = reinterpret_cast<int *>(smem + (size_t)NB * a.K);
 
-    if constexpr (KIND == RK_PRED1) {  // the first kernel of a call: nothing to wait for
-        pdl_wait();
-        pdl_launch_dependents();
-        if (a.side_flag && blockIdx.x == 0 && tile == 0 && threadIdx.x == 0)
-            *a.side_flag = 0;
-    }
     int ncta = gridDim.x;  // CTAs that share the rows
     if constexpr (KIND == RK_PRED2) {
         if (a.side_cta) {
@@ -484,9 +478,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot(const RowArgs a)
         for (int i = threadIdx.x; i < NB * kTopkBins; i += blockDim.x)
             shist[i] = 0;
     }
-    if constexpr (KIND == RK_PRED2 || KIND == RK_FC1) {  // activations come from the previous kernel
+    if constexpr (KIND == RK_PRED1 || KIND == RK_PRED2 || KIND == RK_FC1) {
+        // activations come from the previous kernel (PRED1: from whatever ran
+        // before the call; only its weight rows are read before this point)
         pdl_wait();
         pdl_launch_dependents();
+        if constexpr (KIND == RK_PRED1) {
+            if (a.side_flag && blockIdx.x == 0 && tile == 0 && threadIdx.x == 0)
+                *a.side_flag = 0;
+        }
     }
     stage_acts<T, NB>(a, xs, b0, red);
 

@@ -17,6 +17,13 @@
  *    state between calls other than what lives in the caller's workspace.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
  *    stream) and returns without synchronising, except where stated.
+ *    dv_layer_decode and dv_predict_topk launch their first kernel as a
+ *    programmatic dependent of the previous kernel on the stream: it may
+ *    read the predictor weights (pred_h, pred_a) before that kernel has
+ *    finished, everything else only after.  So do not write those weights
+ *    from a kernel that signals early completion to its dependents
+ *    (griddepcontrol.launch_dependents) right before the call; kernels that
+ *    do not, and copies, are waited for in full.
  *    Index counts stay on the device; no call reads device memory on the
  *    host, so a call can be captured in a CUDA graph.
  *  - Arguments are checked on the host before anything is launched; a bad

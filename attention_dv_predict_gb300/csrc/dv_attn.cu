@@ -18,10 +18,10 @@
 // out-projection kernel merges the C records of a head while it stages its
 // coefficients.
 //
-// Only position kv_len (appended by the QKV kernel) and q depend on the
-// previous kernel; the head list was published before it (flag) or given by
-// the caller, and older positions of the cache are inputs.  So the first two
-// batches of K/V loads go out before the grid dependency is waited for.
+// The head list was published before the previous kernel ran (flag) or
+// given by the caller, so the CTAs read it and place their work before the
+// grid wait; q and the appended position come from the QKV kernel, so all
+// K/V loads follow the wait.
 #include "dv_common.cuh"
 
 namespace dv {
@@ -79,40 +79,27 @@ __global__ void __launch_bounds__(kThreads) k_attn(const AttnArgs a)
         const int p0 = c0 + (int)((long long)(c1 - c0) * warp / kWarpsPerBlock);
         const int p1 = c0 + (int)((long long)(c1 - c0) * (warp + 1) / kWarpsPerBlock);
         const size_t base = ((size_t)b * a.H + h) * (size_t)a.kv_cap * DH + (size_t)dc * EPC;
-        // positions this lane loads before the wait: the cache's older ones
-        const int pre = waited ? p1 : min(p1, a.kv_len);
+        if (!waited) {
+            // q and the appended K/V come from the previous kernel.  (Loading
+            // the older positions before this wait was measured: the extra
+            // traffic beside the QKV kernel's tail made the step slower.)
+            pdl_wait();
+            pdl_launch_dependents();
+            waited = true;
+        }
         const int nbatch = (p1 - p0 + KPW * UK - 1) / (KPW * UK);
         uint4 kc[UK], vc[UK], kn[UK], vn[UK];
 #pragma unroll
         for (int uu = 0; uu < UK; ++uu) {
             const int p = p0 + uu * KPW + ks;
-            kc[uu] = p < pre ? ld_stream(Kc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
-            vc[uu] = p < pre ? ld_stream(Vc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
+            kc[uu] = p < p1 ? ld_stream(Kc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
+            vc[uu] = p < p1 ? ld_stream(Vc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int uu = 0; uu < UK; ++uu) {
             const int p = p0 + (UK + uu) * KPW + ks;
-            kn[uu] = p < pre ? ld_stream(Kc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
-            vn[uu] = p < pre ? ld_stream(Vc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
-        }
-        if (!waited) {
-            pdl_wait();  // q and the appended K/V come from the previous kernel
-            pdl_launch_dependents();
-            waited = true;
-            // the appended position, if it falls in the first two batches
-#pragma unroll
-            for (int uu = 0; uu < UK; ++uu) {
-                const int p = p0 + uu * KPW + ks;
-                if (p == a.kv_len && p < p1) {
-                    kc[uu] = ld_stream(Kc + base + (size_t)p * DH);
-                    vc[uu] = ld_stream(Vc + base + (size_t)p * DH);
-                }
-                const int pn = p0 + (UK + uu) * KPW + ks;
-                if (pn == a.kv_len && pn < p1) {
-                    kn[uu] = ld_stream(Kc + base + (size_t)pn * DH);
-                    vn[uu] = ld_stream(Vc + base + (size_t)pn * DH);
-                }
-            }
+            kn[uu] = p < p1 ? ld_stream(Kc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
+            vn[uu] = p < p1 ? ld_stream(Vc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
         }
         float q[EPC];
         {

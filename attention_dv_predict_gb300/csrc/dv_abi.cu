@@ -146,10 +146,11 @@ NeuronSel make_neuron_sel(const dv_layer_desc &D, int B, int kn, const dv_select
 }
 
 // PRED1 (head scores, low-rank factor u) and PRED2 (neuron scores +
-// first-digit histogram).  pdl_first: PRED1 is launched as a programmatic
-// dependent of the previous kernel on the stream and reads its weight rows
-// before its grid wait (the weights must not be written by a preceding kernel
-// that triggers its dependents early; no kernel of this library writes them).
+// first-digit histogram).  pdl_first: launch PRED1 as a programmatic
+// dependent of the previous kernel on the stream.  No entry point does: a
+// cross-stream event wait before the call is not covered by PRED1's grid
+// wait (a lookahead predictor on a second stream then overwrote a selection
+// still in use), and the gain measured was within noise.
 dv_status run_scores(const dv_layer_desc &D, const dv_layer_weights &w, const float *xp, int B,
                      float *sh_user, float *sn_user, void *ws, const WsLayout &L, Launch &lc,
                      const PredSide *side = nullptr, bool pdl_first = false)
@@ -615,7 +616,7 @@ int dv_predict_topk(const dv_layer_desc *desc, const dv_layer_weights *w, const 
     Launch lc;
     if ((s = make_launch(stream, nullptr, 0, &lc)))
         return s;
-    if ((s = run_scores(D, *w, x_pred, batch, scores_h, scores_n, ws, L, lc, nullptr, true)))
+    if ((s = run_scores(D, *w, x_pred, batch, scores_h, scores_n, ws, L, lc)))
         return s;
     SelectArgs sa;
     std::memset(&sa, 0, sizeof(sa));
@@ -681,13 +682,45 @@ int dv_sparse_mlp(const dv_layer_desc *desc, const dv_layer_weights *w, const fl
     return cuda_status(cudaGetLastError());
 }
 
+int dv_layer_decode_presel(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x,
+                           int batch, const int32_t *u_h, const int32_t *n_u_h, int max_u_h,
+                           const int32_t *u_n, const int32_t *n_u_n, int max_u_n, void *k_cache,
+                           void *v_cache, int kv_len, float *h1, float *y, void *ws,
+                           size_t ws_bytes, void *stream)
+{
+    dv_status s = check_desc(desc);
+    if (s)
+        return s;
+    if ((s = check_weights(w)))
+        return s;
+    const dv_layer_desc &D = *desc;
+    if (batch < 1 || batch > DV_MAX_BATCH || max_u_h < 1 || max_u_h > D.n_heads || max_u_n < 1 ||
+        max_u_n > D.d_ffn || kv_len < 0 || kv_len >= D.kv_cap || !ptr_ok(x) || !ptr_ok(y) ||
+        (h1 && !ptr_ok(h1)) || !u_h || !n_u_h || !u_n || !n_u_n || !ptr_ok(k_cache) ||
+        !ptr_ok(v_cache) || x == y || x == h1 || (h1 && h1 == y))
+        return DV_ERR_INVALID_ARG;
+    WsLayout L;
+    if ((s = check_ws(D, batch, ws, ws_bytes, &L)))
+        return s;
+    Launch lc;
+    if ((s = make_launch(stream, nullptr, 0, &lc)))
+        return s;
+    float *h1p = h1 ? h1 : at<float>(ws, L.h1);
+    if ((s = run_attn(D, *w, x, batch, u_h, n_u_h, max_u_h, k_cache, v_cache, kv_len, h1p, ws, L,
+                      lc, true, nullptr)))
+        return s;
+    if ((s = run_mlp(D, *w, h1p, batch, u_n, n_u_n, max_u_n, y, ws, L, lc, false)))
+        return s;
+    return cuda_status(cudaGetLastError());
+}
+
 int dv_layer_decode(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x,
                     const float *x_pred, int batch, int k_heads, int k_neurons, void *k_cache,
                     void *v_cache, int kv_len, const dv_selection *sel, float *h1, float *y,
                     void *ws, size_t ws_bytes, void *stream)
 {
     return layer_decode_impl(desc, w, x, x_pred, batch, k_heads, k_neurons, k_cache, v_cache,
-                             kv_len, sel, h1, y, ws, ws_bytes, nullptr, 0, stream, true);
+                             kv_len, sel, h1, y, ws, ws_bytes, nullptr, 0, stream, false);
 }
 
 int dv_layer_decode_traced(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x,

@@ -27,6 +27,13 @@
 namespace dv {
 namespace {
 
+// K/V rows are streamed through the non-coherent path: the cache's older
+// positions are inputs, never written while this kernel runs.  Position
+// kv_len was just written by the QKV kernel, which may still have been running
+// when this grid started (programmatic dependent launch), and reading it
+// through the non-coherent path returned stale data in about 1 of 25
+// decodes; the warp whose range holds it reads all its rows at L2 instead.
+
 template <typename T, int LPK>
 __global__ void __launch_bounds__(kThreads) k_attn(const AttnArgs a)
 {
@@ -88,18 +95,21 @@ __global__ void __launch_bounds__(kThreads) k_attn(const AttnArgs a)
             waited = true;
         }
         const int nbatch = (p1 - p0 + KPW * UK - 1) / (KPW * UK);
+        // the warp whose range holds position kv_len reads all its rows at L2
+        const bool coh = p0 <= a.kv_len && a.kv_len < p1;  // uniform over the warp
+        auto ldkv = [&](const T *row) { return coh ? ld_stream_coherent(row) : ld_stream(row); };
         uint4 kc[UK], vc[UK], kn[UK], vn[UK];
 #pragma unroll
         for (int uu = 0; uu < UK; ++uu) {
             const int p = p0 + uu * KPW + ks;
-            kc[uu] = p < p1 ? ld_stream(Kc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
-            vc[uu] = p < p1 ? ld_stream(Vc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
+            kc[uu] = p < p1 ? ldkv(Kc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
+            vc[uu] = p < p1 ? ldkv(Vc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int uu = 0; uu < UK; ++uu) {
             const int p = p0 + (UK + uu) * KPW + ks;
-            kn[uu] = p < p1 ? ld_stream(Kc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
-            vn[uu] = p < p1 ? ld_stream(Vc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
+            kn[uu] = p < p1 ? ldkv(Kc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
+            vn[uu] = p < p1 ? ldkv(Vc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
         }
         float q[EPC];
         {
@@ -152,8 +162,8 @@ __global__ void __launch_bounds__(kThreads) k_attn(const AttnArgs a)
                 kc[uu] = kn[uu];
                 vc[uu] = vn[uu];
                 const int p = pb + 2 * KPW * UK + uu * KPW + ks;
-                kn[uu] = p < p1 ? ld_stream(Kc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
-                vn[uu] = p < p1 ? ld_stream(Vc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
+                kn[uu] = p < p1 ? ldkv(Kc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
+                vn[uu] = p < p1 ? ldkv(Vc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
             }
         }
         // merge the key groups of the warp (butterfly: every lane ends with the total)

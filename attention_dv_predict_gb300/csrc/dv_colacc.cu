@@ -87,7 +87,7 @@ DV_DEV float coef_at(const ColArgs &a, int b, int i)
         }
         return OO / LL;
     } else {
-        return a.coef[(size_t)b * a.coef_ld + i];
+        return __ldcg(a.coef + (size_t)b * a.coef_ld + i);
     }
 }
 

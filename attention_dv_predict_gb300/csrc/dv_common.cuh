@@ -16,9 +16,9 @@ constexpr int kWarp = 32;
 // ---------------------------------------------------------------------------
 // Global-memory access.
 //
-// Weights and KV rows are read exactly once per call: 16-byte vector loads
-// through the non-coherent path, not allocated in L1, with a 256-byte L2
-// prefetch hint so DRAM sees whole bursts.
+// Weights are read exactly once per call and never written: 16-byte vector
+// loads through the non-coherent path, not allocated in L1, with a 256-byte
+// L2 prefetch hint so DRAM sees whole bursts.
 // The asm is volatile so a prefetch is issued where it is written (ahead of
 // the arithmetic on the previous batch), not moved next to its first use.
 DV_DEV uint4 ld_stream(const void *p)
@@ -27,6 +27,19 @@ DV_DEV uint4 ld_stream(const void *p)
     asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
         : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
         : "l"(p));
+    return r;
+}
+
+// Data that a preceding kernel writes while this one may already be resident
+// (programmatic dependent launch: the KV cache's appended slot): 16-byte loads
+// at L2, never through the non-coherent read-only path, which is only valid
+// for data that no grid writes during the reading kernel's lifetime.
+DV_DEV uint4 ld_stream_coherent(const void *p)
+{
+    uint4 r;
+    asm volatile("ld.global.cg.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
     return r;
 }
 

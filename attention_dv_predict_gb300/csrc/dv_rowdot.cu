@@ -242,7 +242,7 @@ struct RowRef {
 DV_DEV int sel_at(const RowArgs &a, int j, const int *ssel, int sj0, int sn)
 {
     const int o = j - sj0;
-    return (o >= 0 && o < sn) ? ssel[o] : a.sel[j];
+    return (o >= 0 && o < sn) ? ssel[o] : ld_cg(a.sel + j);
 }
 
 template <typename T, int KIND>

@@ -67,6 +67,8 @@ _SIGS = {
     "dv_sparse_attn": ([_D, _W, _P, _I, _P, _P, _I, _P, _P, _I, _P, _P, _SZ, _P], _I),
     "dv_sparse_mlp": ([_D, _W, _P, _I, _P, _P, _I, _P, _P, _SZ, _P], _I),
     "dv_layer_decode": ([_D, _W, _P, _P, _I, _I, _I, _P, _P, _I, _S, _P, _P, _P, _SZ, _P], _I),
+    "dv_layer_decode_presel": ([_D, _W, _P, _I, _P, _P, _I, _P, _P, _I, _P, _P, _I, _P, _P, _P,
+                                _SZ, _P], _I),
     "dv_layer_decode_traced": ([_D, _W, _P, _P, _I, _I, _I, _P, _P, _I, _S, _P, _P, _P, _SZ,
                                 C.POINTER(_P), _I, _P], _I),
     "dv_layer_decode_host": ([_D, _W, _P, _P, _I, _I, _I, _P, _P, _I, _S, _P, _P, _SZ, _P], _I),
@@ -245,6 +247,18 @@ def dv_layer_decode(layer: Layer, x: torch.Tensor, k_heads: int, k_neurons: int,
         C.byref(layer.desc), C.byref(layer.c), _ptr(x), _ptr(x_pred), B, k_heads, k_neurons,
         _ptr(k_cache), _ptr(v_cache), kv_len, C.byref(sel.c), _ptr(h1), _ptr(y), ws.cptr,
         ws.nbytes, _stream(stream)))
+
+
+def dv_layer_decode_presel(layer: Layer, x: torch.Tensor, sel: SelectionBuffers,
+                           k_cache: torch.Tensor, v_cache: torch.Tensor, kv_len: int,
+                           y: torch.Tensor, ws: Workspace, h1: Optional[torch.Tensor] = None,
+                           stream=None):
+    """Layer decode on the unions already in ``sel`` (e.g. from a lookahead predictor)."""
+    B = x.shape[0]
+    _check("dv_layer_decode_presel", _lib.dv_layer_decode_presel(
+        C.byref(layer.desc), C.byref(layer.c), _ptr(x), B, _ptr(sel.u_h), _ptr(sel.n_u_h),
+        sel.max_u_h, _ptr(sel.u_n), _ptr(sel.n_u_n), sel.max_u_n, _ptr(k_cache), _ptr(v_cache),
+        kv_len, _ptr(h1), _ptr(y), ws.cptr, ws.nbytes, _stream(stream)))
 
 
 def dv_layer_decode_traced(layer: Layer, x: torch.Tensor, k_heads: int, k_neurons: int,

@@ -50,7 +50,11 @@ def parse_args(argv=None):
     p.add_argument("--copies", type=int, default=4)
     p.add_argument("--cpu-budget-s", type=float, default=15.0)
     p.add_argument("--no-extras", action="store_true",
-                   help="skip dense baseline, e2e, copy peak and CPU baseline legs")
+                   help="skip dense baseline, e2e, copy peak, CPU baseline and stack legs")
+    p.add_argument("--stack-layers", type=int, default=24,
+                   help="layers of the stack leg (0 skips it)")
+    p.add_argument("--stack-batches", default="1,2,4,8,16,32",
+                   help="batch sizes of the stack leg")
     return p.parse_args(argv)
 
 
@@ -328,6 +332,10 @@ def run_cuda(args):
     if not args.no_extras:
         line.update(extras(args, dv, traffic, cfg, desc, layers, caches, x, sel, ws, stream,
                            rank, us_per_decode, k_h, k_n, B))
+        if args.stack_layers > 0:
+            del layers, caches
+            torch.cuda.empty_cache()
+            line["stack"] = stack_bench(args, dv, traffic, cfg, x.device)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -404,6 +412,68 @@ def extras(args, dv, traffic, cfg, desc, layers, caches, x, sel, ws, stream, ran
     if rank == 0:
         out["cpu_baseline"] = cpu_baseline(cfg, layers[0], caches[0], x, k_h, k_n,
                                            args.cpu_budget_s)
+    return out
+
+
+def stack_bench(args, dv, traffic, cfg, device):
+    """Tokens/s of an L-layer stack of this layer shape, lookahead predictor on
+    a side stream (attention_dv_predict_gb300/stack.py), one CUDA graph per
+    token step; at batch 1 also the same calls on one stream (no overlap)."""
+    import torch
+
+    import dv_inputs
+    from attention_dv_predict_gb300 import stack
+
+    n = args.stack_layers
+    desc = dv.desc_from_config(cfg)
+    weights = stack.make_stack_weights(cfg, n, device=device, seed0=100)
+    layers = stack.layers_from_weights(desc, weights)
+    P = 2 if cfg.dtype == "f16" else 4
+    out = {"layers": n, "shape": cfg.name, "kv_len": cfg.kv_len,
+           "note": "layer l+1's selection predicted from layer l's input on a side stream; "
+                   "one CUDA graph per token step; GB/s on the stack's required bytes",
+           "batches": []}
+    for B in [int(b) for b in args.stack_batches.split(",") if b]:
+        caches = stack.stack_caches(cfg, n, B, device=device, seed0=100)
+        x0 = dv_inputs.make_x(cfg, B, seed=5, device=device)
+        st = stack.LayerStack(desc, layers, B, cfg.k_heads, cfg.k_neurons, device=device)
+        st.keep_selection = True
+        st.run(x0, caches, cfg.kv_len)
+        req = sum(traffic.sparse_step_bytes(cfg.d_model, cfg.n_heads, cfg.head_dim, cfg.d_ffn,
+                                            cfg.pred_rank, P, B, int(k["n_u_h"].item()),
+                                            int(k["n_u_n"].item()), cfg.kv_len).total
+                  for k in st.kept)
+        st.keep_selection = False
+        entry = {"batch": B, "required_bytes": req}
+        for mode in (("overlap", "serial") if B == 1 else ("overlap",)):
+            serial = mode == "serial"
+            st.run(x0, caches, cfg.kv_len, serial=serial)
+            cs = torch.cuda.Stream(device=device)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cs):
+                st.enqueue(x0, caches, cfg.kv_len, serial=serial)
+            reps = max(3, 40 // B)
+            for _ in range(2):
+                g.replay()
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(reps):
+                g.replay()
+            b.record()
+            b.synchronize()
+            ms = a.elapsed_time(b) / reps
+            key = "" if mode == "overlap" else "serial_"
+            entry[key + "ms_per_token_step"] = round(ms, 4)
+            entry[key + "tokens_per_s"] = round(B / (ms * 1e-3), 1)
+            entry[key + "us_per_layer"] = round(ms * 1e3 / n, 2)
+            if mode == "overlap":
+                entry["achieved_gbs"] = round(req / (ms * 1e-3) / 1e9, 1)
+            del g
+        out["batches"].append(entry)
+        del caches, st
+        torch.cuda.empty_cache()
     return out
 
 

@@ -17,13 +17,6 @@
  *    state between calls other than what lives in the caller's workspace.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
  *    stream) and returns without synchronising, except where stated.
- *    dv_layer_decode and dv_predict_topk launch their first kernel as a
- *    programmatic dependent of the previous kernel on the stream: it may
- *    read the predictor weights (pred_h, pred_a) before that kernel has
- *    finished, everything else only after.  So do not write those weights
- *    from a kernel that signals early completion to its dependents
- *    (griddepcontrol.launch_dependents) right before the call; kernels that
- *    do not, and copies, are waited for in full.
  *    Index counts stay on the device; no call reads device memory on the
  *    host, so a call can be captured in a CUDA graph.
  *  - Arguments are checked on the host before anything is launched; a bad
@@ -204,6 +197,22 @@ int dv_layer_decode(const dv_layer_desc *desc, const dv_layer_weights *w, const 
                     const float *x_pred, int batch, int k_heads, int k_neurons, void *k_cache,
                     void *v_cache, int kv_len, const dv_selection *sel, float *h1, float *y,
                     void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * dv_layer_decode_presel -- the layer decode on a selection computed earlier:
+ * dv_sparse_attn then dv_sparse_mlp in one call (five kernels, chained).
+ * ("DejaVu Guide ...", "2. Pipelined Overlap Execution": the lookahead
+ * predictor for layer l+1 runs while layer l computes, so by the time layer
+ * l+1 starts its head and neuron sets are ready.)
+ *   u_h / n_u_h (max_u_h), u_n / n_u_n (max_u_n): device unions, ascending,
+ *   as dv_predict_topk writes them; x, y [B, d] binary32 device, distinct;
+ *   h1 [B, d] optional output of the attention block (NULL: workspace).
+ */
+int dv_layer_decode_presel(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x,
+                           int batch, const int32_t *u_h, const int32_t *n_u_h, int max_u_h,
+                           const int32_t *u_n, const int32_t *n_u_n, int max_u_n, void *k_cache,
+                           void *v_cache, int kv_len, float *h1, float *y, void *ws,
+                           size_t ws_bytes, void *stream);
 
 /*
  * dv_layer_decode_traced -- dv_layer_decode that also records

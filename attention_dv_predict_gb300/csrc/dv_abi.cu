@@ -145,6 +145,28 @@ NeuronSel make_neuron_sel(const dv_layer_desc &D, int B, int kn, const dv_select
     return ns;
 }
 
+// QKV and FC1 use the tensor-core row kernel for binary16 weights from
+// kMmaMinBatch batch rows on.
+bool use_mma(const dv_layer_desc &D, int B)
+{
+    return D.dtype == DV_F16 && B >= kMmaMinBatch && D.d_model % 32 == 0;
+}
+
+// Fills the tensor-core fields of a; returns its dynamic shared memory.
+size_t set_mma(RowArgs &a, const dv_layer_desc &D, void *ws, const WsLayout &L)
+{
+    int S = 1, ks = 0;
+    rowdot_mma_plan(D.d_model, &S, &ks);
+    a.mma_seg = S;
+    a.mma_ks = ks;
+    const int rows_max = 3 * D.n_heads * D.head_dim > D.d_ffn ? 3 * D.n_heads * D.head_dim
+                                                               : D.d_ffn;
+    a.mma_groups = ceil_div(rows_max, 16);
+    a.mma_part = at<float>(ws, L.mma_part);
+    a.mma_cnt = at<int>(ws, L.mma_cnt);
+    return rowdot_mma_smem(ks);
+}
+
 // PRED1 (head scores, low-rank factor u) and PRED2 (neuron scores +
 // first-digit histogram).  pdl_first: launch PRED1 as a programmatic
 // dependent of the previous kernel on the stream.  No entry point does: a
@@ -276,8 +298,16 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     dv_status s = lc.mark();
     if (s)
         return s;
-    if (launch_rowdot(RK_QKV, D.dtype, nb, a, grid, smem, lc.st, !first) != cudaSuccess)
+    if (use_mma(D, B)) {
+        size_t sm = set_mma(a, D, ws, L);
+        if (ns && select_final_smem(D.d_ffn) > sm)
+            sm = select_final_smem(D.d_ffn);
+        if (launch_rowdot_mma(RK_QKV, a, dim3(lc.nsm, ceil_div(B, 8)), sm, lc.st, !first) !=
+            cudaSuccess)
+            return DV_ERR_CUDA;
+    } else if (launch_rowdot(RK_QKV, D.dtype, nb, a, grid, smem, lc.st, !first) != cudaSuccess) {
         return DV_ERR_CUDA;
+    }
 
     AttnArgs t;
     std::memset(&t, 0, sizeof(t));
@@ -372,9 +402,15 @@ dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float
     dv_status s = lc.mark();
     if (s)
         return s;
-    if (launch_rowdot(RK_FC1, D.dtype, nb, a, dim3(lc.nsm, ceil_div(B, nb)),
-                      rowdot_smem(RK_FC1, nb, d), lc.st, !first) != cudaSuccess)
+    if (use_mma(D, B)) {
+        const size_t sm = set_mma(a, D, ws, L);
+        if (launch_rowdot_mma(RK_FC1, a, dim3(lc.nsm, ceil_div(B, 8)), sm, lc.st, !first) !=
+            cudaSuccess)
+            return DV_ERR_CUDA;
+    } else if (launch_rowdot(RK_FC1, D.dtype, nb, a, dim3(lc.nsm, ceil_div(B, nb)),
+                             rowdot_smem(RK_FC1, nb, d), lc.st, !first) != cudaSuccess) {
         return DV_ERR_CUDA;
+    }
 
     ColArgs c;
     std::memset(&c, 0, sizeof(c));
@@ -530,6 +566,14 @@ bool ws_layout(const dv_layer_desc &D, int B, WsLayout *L)
     L->cand_idx = take((size_t)B * kTopkCand * 4);
     L->cand_cnt = take((size_t)B * 4);
     L->xn = take((size_t)B * d * 4);
+    {  // tensor-core row kernel (binary16, batch tiles of 8)
+        int S = 1, ks = 0;
+        rowdot_mma_plan(D.d_model, &S, &ks);
+        const size_t tiles = (size_t)ceil_div(B, 8);
+        const size_t groups = (size_t)ceil_div(3 * H * dh > N ? 3 * H * dh : N, 16);
+        L->mma_part = take(tiles * groups * S * 128 * 4);
+        L->mma_cnt = take(tiles * groups * 4);
+    }
     L->total = off;
     L->bpad = (int)bp;
     L->attn_splits_max = (int)splits;

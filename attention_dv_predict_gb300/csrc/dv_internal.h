@@ -114,6 +114,11 @@ struct RowArgs {
     // fused decode: PRED1 clears it, PRED2's side CTA sets it once its results
     // are published; the QKV kernel starts on it instead of the grid dependency
     int *side_flag;
+    // tensor-core variant (k_rowdot_mma): K segments, their length, group
+    // partials [tiles][groups][segments][16][8] and arrival counters
+    int mma_seg, mma_ks, mma_groups;
+    float *mma_part;
+    int *mma_cnt;
     int *status;
 };
 
@@ -176,6 +181,7 @@ struct WsLayout {
     size_t sel_idx_h, sel_idx_n, sel_u_h, sel_n_u_h, sel_u_n, sel_n_u_n;
     size_t nbits, cand_key, cand_idx, cand_cnt;  // neuron selection state
     size_t xn;  // normalised input of the attention block (fused decode)
+    size_t mma_part, mma_cnt;  // tensor-core row kernel: group partials and counters
     size_t total;
     int bpad;         // batch rounded up to the largest batch tile (8)
     int attn_splits_max;
@@ -202,5 +208,11 @@ RowGeo rowdot_geometry(int K, int dtype, int nb);
 int colacc_nb(int B);
 int colacc_block_cols(int dtype, int nb);
 size_t rowdot_smem(int kind, int nb, int K);
+// Tensor-core row kernel (binary16 weights, batch tiles of 8; QKV and FC1).
+cudaError_t launch_rowdot_mma(int kind, const RowArgs &a, dim3 grid, size_t smem,
+                              cudaStream_t st, bool pdl);
+void rowdot_mma_plan(int K, int *S, int *ks);
+size_t rowdot_mma_smem(int ks);
+constexpr int kMmaMinBatch = 3;  // batches from which QKV and FC1 use tensor cores
 
 }  // namespace dv

@@ -616,6 +616,243 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot(const RowArgs a)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Tensor-core variant for batch tiles of 8 rows (binary16 weights; QKV, FC1).
+//
+// out[b][row] = sum_k W[row][k] x[b][k] as mma.sync m16n8k16 (f32 accumulate):
+// A = 16 weight rows x 16 k, B = 16 k x 8 batch rows.  A lane loads 16
+// contiguous bytes (8 k) of row g and of row g + 8 (g = lane / 4, t = lane % 4,
+// k = 8t .. 8t + 7 of a 32-k block); the first 4 k feed one mma, the last 4
+// the next, so the fragments' k order is a fixed permutation of the block
+// that A and B share (the sum over k does not depend on it).  Activations
+// are split into binary16 hi = rn(x) and lo = rn(x - hi), each multiplied
+// separately, so the products keep binary32 accuracy.  K is cut into S
+// segments so one segment's hi/lo activations fit in shared memory; the
+// CTAs of segment s split the 16-row groups, and a group's S partial sums
+// are added in segment order by the last warp to finish it.
+
+constexpr int kMmaBK = 4;  // 32-k blocks per load batch (two batches in flight)
+
+DV_DEV void mma16816(float (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3,
+                     unsigned b0, unsigned b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// One output of row `row` (metadata m) for batch row b.
+template <typename T, int KIND>
+DV_DEV void finalize_one(const RowArgs &a, int row, const RowRef &m, int b, float v)
+{
+    if constexpr (KIND == RK_QKV) {
+        v += Elem<T>::load(static_cast<const T *>(a.bias), ((size_t)m.t * a.H + m.h) * a.dh + m.e);
+        if (m.t == 0) {
+            a.out0[((size_t)b * a.max_sel + m.j) * a.dh + m.e] = v * a.q_scale;
+        } else {
+            T *cache = static_cast<T *>(m.t == 1 ? a.kc : a.vc);
+            cache[(((size_t)b * a.H + m.h) * a.kv_cap + a.kv_len) * a.dh + m.e] =
+                Elem<T>::from_float(v);
+        }
+    } else {
+        v += Elem<T>::load(static_cast<const T *>(a.bias), (size_t)m.h);
+        a.out0[(size_t)b * a.max_sel + row] = fmaxf(v, 0.f);
+    }
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
+{
+    using T = __half;
+    extern __shared__ __align__(16) float smem[];
+    __shared__ float red[34];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int tile = blockIdx.y, b0 = tile * 8;
+    int ncta = gridDim.x;
+    if constexpr (KIND == RK_QKV) {
+        if (a.side_cta) {
+            ncta = gridDim.x - 1;
+            if (blockIdx.x == ncta) {  // the neuron selection (as in k_rowdot)
+                pdl_wait();
+                pdl_launch_dependents();
+                if (tile == 0) {
+                    __shared__ int nscr[48];
+                    neuron_select_cta(a.ns, final_smem(smem, a.ns.N, nscr));
+                }
+                return;
+            }
+        }
+        if (a.side_flag) {
+            __shared__ int s_ready;
+            if (threadIdx.x == 0) {
+                int ok = 0;
+                for (int it = 0; it < kSideSpin && !ok; ++it) {
+                    ok = ld_acquire_gpu(a.side_flag);
+                    if (!ok)
+                        __nanosleep(128);
+                }
+                s_ready = ok;
+            }
+            __syncthreads();
+            if (!s_ready)
+                pdl_wait();
+            pdl_launch_dependents();
+        } else {
+            pdl_wait();
+            pdl_launch_dependents();
+        }
+    }
+    const int K = a.K;
+    int rows;
+    if constexpr (KIND == RK_QKV)
+        rows = min(max(ld_cg(a.n_sel), 0), a.max_sel) * 3 * a.dh;
+    else
+        rows = min(max(ld_cg(a.n_sel), 0), a.max_sel);
+    const int ngroups = (rows + 15) >> 4;
+    const int S = a.mma_seg;
+    // segment of this CTA, its CTAs, and this CTA's share of the row groups
+    const int sgm = (int)((long long)blockIdx.x * S / ncta);
+    const int cf = (int)(((long long)sgm * ncta + S - 1) / S);
+    const int cl = (int)(((long long)(sgm + 1) * ncta + S - 1) / S);
+    const int r = blockIdx.x - cf, m = cl - cf;
+    const int g0 = (int)((long long)ngroups * r / m), g1 = (int)((long long)ngroups * (r + 1) / m);
+    const int wg0 = g0 + (int)((long long)(g1 - g0) * warp / kWarpsPerBlock);
+    const int wg1 = g0 + (int)((long long)(g1 - g0) * (warp + 1) / kWarpsPerBlock);
+    const int k0 = sgm * a.mma_ks;
+    const int kn = min(a.mma_ks, K - k0);  // multiple of 32
+    const int ldx = a.mma_ks + 32;         // staged row stride in halfs (64-byte pad)
+
+    if constexpr (KIND == RK_FC1) {  // h1 comes from the previous kernel
+        pdl_wait();
+        pdl_launch_dependents();
+    }
+    // this segment's activations of batch rows b0 .. b0 + 7: hi and lo halves
+    __half *xh = reinterpret_cast<__half *>(smem);
+    __half *xl = xh + 8 * ldx;
+    for (int bi = 0; bi < 8; ++bi) {
+        const int b = b0 + bi;
+        if (b >= a.B) {
+            for (int i = threadIdx.x; i < kn; i += blockDim.x) {
+                xh[bi * ldx + i] = __float2half_rn(0.f);
+                xl[bi * ldx + i] = __float2half_rn(0.f);
+            }
+            continue;
+        }
+        norm_row<T>(a.x + (size_t)b * a.x_ld, K, a.norm_g, a.norm_b, a.norm_kind, a.eps, red,
+                    [&](int c, const float(&v)[8]) {
+                        const int kk = c * 8 - k0;
+                        if (kk < 0 || kk >= kn)
+                            return;
+                        __align__(16) __half hi[8], lo[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            hi[e] = __float2half_rn(v[e]);
+                            lo[e] = __float2half_rn(v[e] - __half2float(hi[e]));
+                        }
+                        *reinterpret_cast<uint4 *>(xh + bi * ldx + kk) =
+                            *reinterpret_cast<const uint4 *>(hi);
+                        *reinterpret_cast<uint4 *>(xl + bi * ldx + kk) =
+                            *reinterpret_cast<const uint4 *>(lo);
+                    });
+    }
+    __syncthreads();
+
+    const int g = lane >> 2, t = lane & 3;
+    const int nblk = kn >> 5;
+    const __half *xhr = xh + g * ldx + 8 * t, *xlr = xl + g * ldx + 8 * t;
+    for (int grp = wg0; grp < wg1; ++grp) {
+        const int ra = grp * 16 + g, rb = ra + 8;
+        RowRef ma, mb;
+        ma.p = mb.p = nullptr;
+        ma.j = ma.t = ma.e = ma.h = mb.j = mb.t = mb.e = mb.h = 0;
+        if (ra < rows)
+            ma = row_ref<T, KIND>(a, ra, nullptr, 0, 0);
+        if (rb < rows)
+            mb = row_ref<T, KIND>(a, rb, nullptr, 0, 0);
+        if ((ra < rows && !ma.p) || (rb < rows && !mb.p))
+            set_status(a.status, DV_ERR_DEVICE_INDEX);
+        const T *pa = ma.p ? static_cast<const T *>(ma.p) + k0 + 8 * t : nullptr;
+        const T *pb = mb.p ? static_cast<const T *>(mb.p) + k0 + 8 * t : nullptr;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        uint4 wa[kMmaBK], wb[kMmaBK];
+#pragma unroll
+        for (int i = 0; i < kMmaBK; ++i) {
+            wa[i] = (i < nblk && pa) ? ld_stream(pa + i * 32) : make_uint4(0u, 0u, 0u, 0u);
+            wb[i] = (i < nblk && pb) ? ld_stream(pb + i * 32) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        for (int blk0 = 0; blk0 < nblk; blk0 += kMmaBK) {
+            uint4 na[kMmaBK], nb[kMmaBK];
+#pragma unroll
+            for (int i = 0; i < kMmaBK; ++i) {
+                const int blk = blk0 + kMmaBK + i;
+                na[i] = (blk < nblk && pa) ? ld_stream(pa + blk * 32) : make_uint4(0u, 0u, 0u, 0u);
+                nb[i] = (blk < nblk && pb) ? ld_stream(pb + blk * 32) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int i = 0; i < kMmaBK; ++i) {
+                const int blk = blk0 + i;
+                if (blk < nblk) {
+                    const uint4 h4 = *reinterpret_cast<const uint4 *>(xhr + blk * 32);
+                    const uint4 l4 = *reinterpret_cast<const uint4 *>(xlr + blk * 32);
+                    mma16816(acc, wa[i].x, wb[i].x, wa[i].y, wb[i].y, h4.x, h4.y);
+                    mma16816(acc, wa[i].x, wb[i].x, wa[i].y, wb[i].y, l4.x, l4.y);
+                    mma16816(acc, wa[i].z, wb[i].z, wa[i].w, wb[i].w, h4.z, h4.w);
+                    mma16816(acc, wa[i].z, wb[i].z, wa[i].w, wb[i].w, l4.z, l4.w);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kMmaBK; ++i) {
+                wa[i] = na[i];
+                wb[i] = nb[i];
+            }
+        }
+        // acc: (row ra, batch 2t), (ra, 2t+1), (rb, 2t), (rb, 2t+1)
+        if (S > 1) {
+            float *pp = a.mma_part + (((size_t)tile * a.mma_groups + grp) * S + sgm) * 128;
+            pp[g * 8 + 2 * t] = acc[0];
+            pp[g * 8 + 2 * t + 1] = acc[1];
+            pp[(g + 8) * 8 + 2 * t] = acc[2];
+            pp[(g + 8) * 8 + 2 * t + 1] = acc[3];
+            __threadfence();
+            int last = 0;
+            int *cnt = a.mma_cnt + (size_t)tile * a.mma_groups + grp;
+            if (lane == 0)
+                last = (atomicAdd(cnt, 1) == S - 1);
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (!last)
+                continue;
+            __threadfence();
+            float sum[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int q = 0; q < S; ++q) {
+                const float *qp = a.mma_part + (((size_t)tile * a.mma_groups + grp) * S + q) * 128;
+                sum[0] += __ldcg(qp + g * 8 + 2 * t);
+                sum[1] += __ldcg(qp + g * 8 + 2 * t + 1);
+                sum[2] += __ldcg(qp + (g + 8) * 8 + 2 * t);
+                sum[3] += __ldcg(qp + (g + 8) * 8 + 2 * t + 1);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                acc[i] = sum[i];
+            if (lane == 0)
+                *cnt = 0;
+        }
+        if (ma.p) {
+            if (b0 + 2 * t < a.B)
+                finalize_one<T, KIND>(a, ra, ma, b0 + 2 * t, acc[0]);
+            if (b0 + 2 * t + 1 < a.B)
+                finalize_one<T, KIND>(a, ra, ma, b0 + 2 * t + 1, acc[1]);
+        }
+        if (mb.p) {
+            if (b0 + 2 * t < a.B)
+                finalize_one<T, KIND>(a, rb, mb, b0 + 2 * t, acc[2]);
+            if (b0 + 2 * t + 1 < a.B)
+                finalize_one<T, KIND>(a, rb, mb, b0 + 2 * t + 1, acc[3]);
+        }
+    }
+}
+
 template <typename T, int NB, int KIND>
 cudaError_t launch_one(const RowArgs &a, dim3 grid, size_t smem, cudaStream_t st, bool pdl)
 {
@@ -729,5 +966,57 @@ cudaError_t launch_rowdot(int kind, int dtype, int nb, const RowArgs &a, dim3 gr
         return dispatch_kind<__half>(kind, nb, a, grid, smem, st, pdl);
     return dispatch_kind<float>(kind, nb, a, grid, smem, st, pdl);
 }
+
+cudaError_t launch_rowdot_mma(int kind, const RowArgs &a, dim3 grid, size_t smem,
+                              cudaStream_t st, bool pdl)
+{
+    if (kind != RK_QKV && kind != RK_FC1)
+        return cudaErrorInvalidValue;
+    void (*kern)(RowArgs) = kind == RK_QKV ? k_rowdot_mma<RK_QKV> : k_rowdot_mma<RK_FC1>;
+    static bool configured[2][kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    const int ki = kind == RK_QKV ? 0 : 1;
+    if (!configured[ki][dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap);
+        if (e != cudaSuccess)
+            return e;
+        configured[ki][dev] = true;
+    }
+    if (smem > kSmemCap)
+        return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+// K segments and their length for the tensor-core variant: each segment's
+// hi/lo activations of 8 batch rows (32 bytes per k, plus padding) must fit
+// the shared-memory budget.
+void rowdot_mma_plan(int K, int *S, int *ks)
+{
+    const size_t budget = 160 * 1024;
+    int s = 1;
+    while ((size_t)32 * ((size_t)(K + s - 1) / s + 32) > budget)
+        ++s;
+    int len = (K + s - 1) / s;
+    len = (len + 31) / 32 * 32;
+    *ks = len;
+    *S = (K + len - 1) / len;
+}
+
+size_t rowdot_mma_smem(int ks) { return (size_t)32 * (ks + 32); }
 
 }  // namespace dv

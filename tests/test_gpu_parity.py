@@ -256,6 +256,15 @@ def test_opt66b_full(dv, B):
         assert CFG["opt66b"].k_neurons < g["u_n"].size <= 8 * CFG["opt66b"].k_neurons
 
 
+@pytest.mark.parametrize("B", [3, 16])
+def test_opt67b_batches_tensor_core_path(dv, B):
+    # B >= 3 with binary16 weights runs QKV and fc1 on the tensor-core row
+    # kernel (one partial batch tile at B = 3, two tiles at B = 16)
+    case = make_case(CFG["opt6.7b"], B=B, gen_device="cuda", norm_affine=True)
+    g = run_gpu_layer(dv, case)
+    check_layer_parity(case, g)
+
+
 def test_opt175b_full(dv):
     case = make_case(CFG["opt175b"], gen_device="cuda", norm_affine=False)
     g = run_gpu_layer(dv, case)

@@ -33,7 +33,7 @@ def mods():
     return dv, stack
 
 
-@pytest.mark.parametrize("name,B,n_layers", [("tiny", 2, 4), ("opt6.7b", 1, 3)])
+@pytest.mark.parametrize("name,B,n_layers", [("tiny", 2, 4), ("opt6.7b", 1, 3), ("opt6.7b", 4, 2)])
 def test_stack_layers_match_oracle(mods, name, B, n_layers):
     dv, stack = mods
     cfg = dv_inputs.CONFIGS[name].with_(batch=B)

@@ -133,7 +133,9 @@ template <typename T, int NB, int KIND, int P>
 __global__ void __launch_bounds__(kThreads, 1) k_colacc(const ColArgs a)
 {
     constexpr int EPC = Elem<T>::EPC;
-    constexpr int R = 8 / P;            // rows per batch: 8 loads in flight per lane
+    // rows per batch: 8 loads in flight per lane (4 rows at NB >= 8, whose
+    // accumulators take the registers)
+    constexpr int R = NB >= 8 ? 4 : 8 / P;
     constexpr int CB = 32 * P * EPC;    // columns per block
     constexpr int CPT = (CB + kThreads - 1) / kThreads;  // block columns per thread
     extern __shared__ __align__(16) float red[];         // [kWarpsPerBlock][CB]
@@ -225,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_colacc(const ColArgs a)
             // warp w takes rows s0 + w + 16 t; R rows per batch, two batches in flight
             const int cnt = (s1 - s0 - warp + kWarpsPerBlock - 1) / kWarpsPerBlock;
             const int nbatch = cnt > 0 ? (cnt + R - 1) / R : 0;
-            auto load = [&](int q, uint4 (&v)[R][P], float (&c)[R][NB]) {
+            auto load = [&](int q, uint4 (&v)[R][P]) {
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     const int t = q * R + r;
@@ -237,39 +239,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_colacc(const ColArgs a)
                         v[r][p] = (off >= 0 && col < a.d) ? ld_stream(W + off + col)
                                                           : make_uint4(0u, 0u, 0u, 0u);
                     }
-#pragma unroll
-                    for (int b = 0; b < NB; ++b)
-                        c[r][b] = (off >= 0) ? scoef[li * NB + b] : 0.f;
                 }
             };
             uint4 vc[R][P];
-            float cc[R][NB];
-            load(0, vc, cc);
+            load(0, vc);
             for (int q = 0; q < nbatch; ++q) {
                 uint4 vn[R][P];
-                float cn[R][NB];
-                load(q + 1 < nbatch ? q + 1 : nbatch, vn, cn);
+                load(q + 1 < nbatch ? q + 1 : nbatch, vn);
 #pragma unroll
-                for (int r = 0; r < R; ++r)
+                for (int r = 0; r < R; ++r) {
+                    // the row's coefficients, read at use (a broadcast over the warp)
+                    const int t = q * R + r;
+                    const bool live = t < cnt;
+                    const float *cf = scoef + (warp + kWarpsPerBlock * (live ? t : 0)) * NB;
 #pragma unroll
                     for (int p = 0; p < P; ++p) {
                         float f[EPC];
                         Elem<T>::unpack(vc[r][p], f);
 #pragma unroll
-                        for (int b = 0; b < NB; ++b)
+                        for (int b = 0; b < NB; ++b) {
+                            const float c = live ? cf[b] : 0.f;
 #pragma unroll
                             for (int e = 0; e < EPC; ++e)
-                                acc[b][p * EPC + e] = fmaf(cc[r][b], f[e], acc[b][p * EPC + e]);
+                                acc[b][p * EPC + e] = fmaf(c, f[e], acc[b][p * EPC + e]);
+                        }
                     }
+                }
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
+                for (int r = 0; r < R; ++r)
 #pragma unroll
                     for (int p = 0; p < P; ++p)
                         vc[r][p] = vn[r][p];
-#pragma unroll
-                    for (int b = 0; b < NB; ++b)
-                        cc[r][b] = cn[r][b];
-                }
             }
         }
 

@@ -9,13 +9,14 @@
 //          selected fc2 columns, kept transposed so each is one contiguous row).
 //
 // Work: the output columns are cut into blocks of CB columns (CB = 32 lanes
-// x P chunks of 16 bytes: 2 KB of a binary16 row).  The (block, row) pieces
-// are dealt to the CTAs of a persistent grid in contiguous, balanced ranges,
-// block-major.  Inside a CTA the warps take the rows of a block round-robin,
-// two batches of rows in flight per warp, each lane accumulating P strided
-// 16-byte chunks (every load instruction reads 512 contiguous bytes, and a
-// warp reads a whole 2 KB piece of a row at once); the 16 warps then reduce
-// in shared memory.  A block covered entirely by one CTA is finished there;
+// x P chunks of 16 bytes: 1 KB of a binary16 row at P = 2, 512 bytes at
+// P = 1; narrow blocks keep the number of CTAs sharing a block, and so the
+// final cross-CTA sum, small).  The (block, row) pieces are dealt to the
+// CTAs of a persistent grid in contiguous, balanced ranges, block-major.
+// Inside a CTA the warps take the rows of a block round-robin, two batches of
+// rows in flight per warp, each lane accumulating P strided 16-byte chunks
+// (every load instruction reads 512 contiguous bytes, and a warp reads a
+// whole piece of a row at once); the 16 warps then reduce in shared memory.  A block covered entirely by one CTA is finished there;
 // a block shared by several CTAs is finished by the last of them to arrive
 // (atomic count of rows), which sums their partials in CTA order -- results
 // do not depend on scheduling.
@@ -24,7 +25,7 @@
 namespace dv {
 namespace {
 
-constexpr int kStageRows = 256;  // rows whose offsets and coefficients are staged at once
+constexpr int kStageRows = 1024;  // rows whose offsets and coefficients are staged at once
 constexpr int kMaxCover = 512;   // CTAs that may share one column block
 constexpr int kCoverBatch = 8;   // partials loaded together by the combining CTA
 constexpr int kRecBatch = 8;     // attention chunk records loaded together
@@ -55,6 +56,31 @@ DV_DEV float coef_at(const ColArgs &a, int b, int i)
         const int j = i / a.dh, e = i - j * a.dh;
         const int C = a.attn_C, rec = kAttnRec + a.dh;
         const float *r = a.attn_rec + ((size_t)b * a.max_sel + j) * C * rec;
+        if (C <= kRecBatch) {  // all records in one batch of loads
+            float m[kRecBatch], l[kRecBatch], o[kRecBatch];
+#pragma unroll
+            for (int u = 0; u < kRecBatch; ++u) {
+                const float *rc = r + (size_t)u * rec;
+                const bool in = u < C;
+                m[u] = in ? __ldcg(rc) : -INFINITY;
+                l[u] = in ? __ldcg(rc + 1) : 0.f;
+                o[u] = in ? __ldcg(rc + kAttnRec + e) : 0.f;
+            }
+            float MM = m[0];
+#pragma unroll
+            for (int u = 1; u < kRecBatch; ++u)
+                MM = fmaxf(MM, m[u]);
+            float LL = 0.f, OO = 0.f;
+#pragma unroll
+            for (int u = 0; u < kRecBatch; ++u) {
+                if (u >= C)
+                    break;
+                const float w = expf(m[u] - MM);
+                LL = fmaf(l[u], w, LL);
+                OO = fmaf(o[u], w, OO);
+            }
+            return OO / LL;
+        }
         float MM = -INFINITY;
         for (int c0 = 0; c0 < C; c0 += kRecBatch) {
             float m[kRecBatch];
@@ -217,11 +243,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_colacc(const ColArgs a)
                 pdl_launch_dependents();
                 waited = true;
             }
-            for (int i = s0 + tid; i < s1; i += blockDim.x) {
+            // FU rows per thread at once, so that their loads overlap
+            constexpr int FU = NB <= 2 ? 2 : 1;
+            for (int i = s0 + tid; i < s1; i += FU * blockDim.x) {
+                float cv[FU][NB];
 #pragma unroll
-                for (int b = 0; b < NB; ++b)
-                    scoef[(i - s0) * NB + b] =
-                        (b0 + b < a.B) ? coef_at<KIND>(a, b0 + b, i) : 0.f;
+                for (int f = 0; f < FU; ++f)
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) {
+                        const int ii = i + f * (int)blockDim.x;
+                        cv[f][b] = (b0 + b < a.B && ii < s1) ? coef_at<KIND>(a, b0 + b, ii) : 0.f;
+                    }
+#pragma unroll
+                for (int f = 0; f < FU; ++f)
+                    if (i + f * (int)blockDim.x < s1)
+#pragma unroll
+                        for (int b = 0; b < NB; ++b)
+                            scoef[(i + f * blockDim.x - s0) * NB + b] = cv[f][b];
             }
             __syncthreads();
             // warp w takes rows s0 + w + 16 t; R rows per batch, two batches in flight

@@ -150,7 +150,7 @@ struct ColArgs {
 // 16-byte chunks per lane of the column kernel (columns per block = 32 * P *
 // elements per chunk); fewer for larger batch tiles to bound registers.
 template <int NB>
-constexpr int colacc_chunks() { return NB == 1 ? 4 : (NB == 2 ? 2 : 1); }
+constexpr int colacc_chunks() { return NB <= 2 ? 2 : 1; }
 
 // Split-KV decode attention over the selected heads.
 struct AttnArgs {

@@ -52,7 +52,8 @@ dv_status check_desc(const dv_layer_desc *D)
     if ((dh & (dh - 1)) || hb < 16 || hb > 512)
         return DV_ERR_UNSUPPORTED;
     // activations of one row must fit the row-dot kernel's shared memory
-    if ((size_t)D->d_model * 4 > kSmemCap || (size_t)D->pred_rank * 4 > kSmemCap)
+    if (rowdot_smem(RK_PRED1, 1, D->d_model) > kSmemCap ||
+        rowdot_smem(RK_PRED2, 1, D->pred_rank) > kSmemCap)
         return DV_ERR_UNSUPPORTED;
     // one warp selects the heads; the neuron selection's bitmaps fit one CTA
     if (D->n_heads > 256 || D->d_ffn > (1 << 19))
@@ -173,9 +174,12 @@ size_t set_mma(RowArgs &a, const dv_layer_desc &D, void *ws, const WsLayout &L)
 // cross-stream event wait before the call is not covered by PRED1's grid
 // wait (a lookahead predictor on a second stream then overwrote a selection
 // still in use), and the gain measured was within noise.
+// plan != nullptr: fill the persistent layer kernel's arguments instead of
+// launching (here and in run_attn / run_mlp).
 dv_status run_scores(const dv_layer_desc &D, const dv_layer_weights &w, const float *xp, int B,
                      float *sh_user, float *sn_user, void *ws, const WsLayout &L, Launch &lc,
-                     const PredSide *side = nullptr, bool pdl_first = false)
+                     const PredSide *side = nullptr, bool pdl_first = false,
+                     LayerArgs *plan = nullptr)
 {
     const int d = D.d_model, H = D.n_heads, N = D.d_ffn, r = D.pred_rank;
     int *ctl = at<int>(ws, L.ctl);
@@ -204,8 +208,10 @@ dv_status run_scores(const dv_layer_desc &D, const dv_layer_weights &w, const fl
     dv_status s = lc.mark();
     if (s)
         return s;
-    if (launch_rowdot(RK_PRED1, D.dtype, nb, a, grid, rowdot_smem(RK_PRED1, nb, d), lc.st,
-                      pdl_first) != cudaSuccess)
+    if (plan)
+        plan->pred1 = a;
+    else if (launch_rowdot(RK_PRED1, D.dtype, nb, a, grid, rowdot_smem(RK_PRED1, nb, d), lc.st,
+                           pdl_first) != cudaSuccess)
         return DV_ERR_CUDA;
 
     RowArgs b2;
@@ -232,8 +238,10 @@ dv_status run_scores(const dv_layer_desc &D, const dv_layer_weights &w, const fl
     grid = dim3(lc.nsm, ceil_div(B, nb));
     if ((s = lc.mark()))
         return s;
-    if (launch_rowdot(RK_PRED2, D.dtype, nb, b2, grid, rowdot_smem(RK_PRED2, nb, r), lc.st,
-                      true) != cudaSuccess)
+    if (plan)
+        plan->pred2 = b2;
+    else if (launch_rowdot(RK_PRED2, D.dtype, nb, b2, grid, rowdot_smem(RK_PRED2, nb, r), lc.st,
+                           true) != cudaSuccess)
         return DV_ERR_CUDA;
     return DV_OK;
 }
@@ -245,7 +253,7 @@ dv_status run_scores(const dv_layer_desc &D, const dv_layer_weights &w, const fl
 dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const float *x, int B,
                    const int32_t *u_h, const int32_t *n_u_h, int max_u_h, void *kc, void *vc,
                    int kv_len, float *h1, void *ws, const WsLayout &L, Launch &lc, bool first,
-                   const NeuronSel *ns)
+                   const NeuronSel *ns, LayerArgs *plan = nullptr)
 {
     const int d = D.d_model, H = D.n_heads, dh = D.head_dim;
     int *ctl = at<int>(ws, L.ctl);
@@ -298,7 +306,9 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     dv_status s = lc.mark();
     if (s)
         return s;
-    if (use_mma(D, B)) {
+    if (plan) {
+        plan->qkv = a;
+    } else if (use_mma(D, B)) {
         size_t sm = set_mma(a, D, ws, L);
         if (ns && select_final_smem(D.d_ffn) > sm)
             sm = select_final_smem(D.d_ffn);
@@ -323,8 +333,9 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     t.kc = kc;
     t.vc = vc;
     const int L1 = kv_len + 1;
-    // chunks per (batch row, head): enough CTAs to cover the SMs once
-    int chunks = lc.nsm / (B * max_u_h);
+    // chunks per (batch row, head): enough CTAs to cover the SMs once (in
+    // the persistent kernel attention runs on all CTAs but the last)
+    int chunks = (plan ? lc.nsm - 1 : lc.nsm) / (B * max_u_h);
     if (chunks < 1)
         chunks = 1;
     if (chunks > L1)
@@ -339,7 +350,9 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     const int lpk = (int)((size_t)dh * esize(D.dtype) / 16);
     if ((s = lc.mark()))
         return s;
-    if (launch_attn(D.dtype, lpk, t, dim3(lc.nsm), lc.st, true) != cudaSuccess)
+    if (plan)
+        plan->attn = t;
+    else if (launch_attn(D.dtype, lpk, t, dim3(lc.nsm), lc.st, true) != cudaSuccess)
         return DV_ERR_CUDA;
 
     ColArgs c;
@@ -363,15 +376,17 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     nb = colacc_nb(B);
     if ((s = lc.mark()))
         return s;
-    if (launch_colacc(CK_OPROJ, D.dtype, nb, c, dim3(lc.nsm, ceil_div(B, nb)), lc.st, true) !=
-        cudaSuccess)
+    if (plan)
+        plan->oproj = c;
+    else if (launch_colacc(CK_OPROJ, D.dtype, nb, c, dim3(lc.nsm, ceil_div(B, nb)), lc.st,
+                           true) != cudaSuccess)
         return DV_ERR_CUDA;
     return DV_OK;
 }
 
 dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float *h1, int B,
                   const int32_t *u_n, const int32_t *n_u_n, int max_u_n, float *y, void *ws,
-                  const WsLayout &L, Launch &lc, bool first)
+                  const WsLayout &L, Launch &lc, bool first, LayerArgs *plan = nullptr)
 {
     const int d = D.d_model, N = D.d_ffn;
     int *ctl = at<int>(ws, L.ctl);
@@ -402,7 +417,9 @@ dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float
     dv_status s = lc.mark();
     if (s)
         return s;
-    if (use_mma(D, B)) {
+    if (plan) {
+        plan->fc1 = a;
+    } else if (use_mma(D, B)) {
         const size_t sm = set_mma(a, D, ws, L);
         if (launch_rowdot_mma(RK_FC1, a, dim3(lc.nsm, ceil_div(B, 8)), sm, lc.st, !first) !=
             cudaSuccess)
@@ -433,8 +450,10 @@ dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float
     nb = colacc_nb(B);
     if ((s = lc.mark()))
         return s;
-    if (launch_colacc(CK_FC2, D.dtype, nb, c, dim3(lc.nsm, ceil_div(B, nb)), lc.st, true) !=
-        cudaSuccess)
+    if (plan)
+        plan->fc2 = c;
+    else if (launch_colacc(CK_FC2, D.dtype, nb, c, dim3(lc.nsm, ceil_div(B, nb)), lc.st, true) !=
+             cudaSuccess)
         return DV_ERR_CUDA;
     return DV_OK;
 }
@@ -453,11 +472,65 @@ bool sel_ok(const dv_selection *sel)
     return sel && sel->idx_h && sel->idx_n && sel->u_h && sel->n_u_h && sel->u_n && sel->n_u_n;
 }
 
+// The persistent layer kernel serves binary16 layers with 128-wide heads at
+// batches of 1 and 2, where every step takes the whole batch as one tile on
+// CUDA cores.  Returns that tile (0: not eligible) and the kernel's dynamic
+// shared memory (the largest of its phases').
+int persistent_plan(const dv_layer_desc &D, int B, int nsm, size_t *smem)
+{
+    if (D.dtype != DV_F16 || D.head_dim != 128 || B > 2 || use_mma(D, B) || nsm < 2)
+        return 0;
+    const int nb = B;
+    if (rowdot_nb(B, D.d_model, RK_PRED1) != nb || rowdot_nb(B, D.pred_rank, RK_PRED2) != nb ||
+        rowdot_nb(B, D.d_model, RK_QKV) != nb || rowdot_nb(B, D.d_model, RK_FC1) != nb ||
+        colacc_nb(B) != nb)
+        return 0;
+    size_t sm = rowdot_smem(RK_PRED1, nb, D.d_model);
+    const size_t parts[] = {rowdot_smem(RK_PRED2, nb, D.pred_rank),
+                            rowdot_smem(RK_QKV, nb, D.d_model), select_final_smem(D.d_ffn),
+                            rowdot_smem(RK_FC1, nb, D.d_model),
+                            colacc_smem_bytes(colacc_block_cols(D.dtype, nb), nb),
+                            attn_smem_bytes(D.head_dim)};
+    for (size_t p : parts)
+        if (p > sm)
+            sm = p;
+    if (sm > kSmemCap)
+        return 0;
+    // one CTA per SM must fit; the answer is kept per device, tile and size
+    struct Fit {
+        int dev, nb;
+        size_t smem;
+        int ctas;
+    };
+    static std::mutex mu;
+    static Fit known[16];
+    static int n_known = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 0;
+    int ctas = -1;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < n_known; ++i)
+            if (known[i].dev == dev && known[i].nb == nb && known[i].smem == sm)
+                ctas = known[i].ctas;
+        if (ctas < 0) {
+            ctas = layer_ctas_per_sm(nb, sm);
+            if (n_known < 16)
+                known[n_known++] = Fit{dev, nb, sm, ctas};
+        }
+    }
+    if (ctas < 1)
+        return 0;
+    *smem = sm;
+    return nb;
+}
+
 dv_status layer_decode_impl(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x,
                             const float *x_pred, int batch, int k_heads, int k_neurons, void *kc,
                             void *vc, int kv_len, const dv_selection *sel, float *h1, float *y,
                             void *ws, size_t ws_bytes, void *const *events, int n_events,
-                            void *stream, bool pdl_first)
+                            void *stream, bool pdl_first, bool persistent = false)
 {
     dv_status s = check_desc(desc);
     if (s)
@@ -499,6 +572,26 @@ dv_status layer_decode_impl(const dv_layer_desc *desc, const dv_layer_weights *w
     side.norm_kind = D.norm;
     side.eps = D.ln_eps;
     side.xn = at<float>(ws, L.xn);
+    if (persistent) {  // one persistent kernel
+        size_t psmem = 0;
+        const int pnb = events ? 0 : persistent_plan(D, batch, lc.nsm, &psmem);
+        if (!pnb)
+            return DV_ERR_UNSUPPORTED;
+        LayerArgs plan;
+        std::memset(&plan, 0, sizeof(plan));
+        if ((s = run_scores(D, *w, x_pred ? x_pred : x, batch, nullptr, nullptr, ws, L, lc, &side,
+                            false, &plan)) ||
+            (s = run_attn(D, *w, x, batch, sel->u_h, sel->n_u_h, max_u_h, kc, vc, kv_len, h1p, ws,
+                          L, lc, false, &ns, &plan)) ||
+            (s = run_mlp(D, *w, h1p, batch, sel->u_n, sel->n_u_n, max_u_n, y, ws, L, lc, false,
+                         &plan)))
+            return s;
+        plan.bar = at<int>(ws, L.ctl) + kLayerBarWord;
+        plan.status = at<int>(ws, L.ctl);
+        if (launch_layer(pnb, plan, lc.nsm, psmem, lc.st) != cudaSuccess)
+            return DV_ERR_CUDA;
+        return cuda_status(cudaGetLastError());
+    }
     if ((s = run_scores(D, *w, x_pred ? x_pred : x, batch, nullptr, nullptr, ws, L, lc, &side,
                         pdl_first)))
         return s;
@@ -641,6 +734,16 @@ int dv_layer_decode_launches(const dv_layer_desc *desc, int batch)
     return kLayerLaunches;
 }
 
+int dv_layer_decode_persistent_ok(const dv_layer_desc *desc, int batch)
+{
+    if (check_desc(desc) != DV_OK || batch < 1 || batch > DV_MAX_BATCH)
+        return 0;
+    Launch lc;
+    size_t sm = 0;
+    return make_launch(nullptr, nullptr, 0, &lc) == DV_OK &&
+           persistent_plan(*desc, batch, lc.nsm, &sm) != 0;
+}
+
 int dv_predict_topk(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x_pred,
                     int batch, int k_heads, int k_neurons, const dv_selection *sel,
                     float *scores_h, float *scores_n, void *ws, size_t ws_bytes, void *stream)
@@ -765,6 +868,16 @@ int dv_layer_decode(const dv_layer_desc *desc, const dv_layer_weights *w, const 
 {
     return layer_decode_impl(desc, w, x, x_pred, batch, k_heads, k_neurons, k_cache, v_cache,
                              kv_len, sel, h1, y, ws, ws_bytes, nullptr, 0, stream, false);
+}
+
+int dv_layer_decode_persistent(const dv_layer_desc *desc, const dv_layer_weights *w,
+                               const float *x, const float *x_pred, int batch, int k_heads,
+                               int k_neurons, void *k_cache, void *v_cache, int kv_len,
+                               const dv_selection *sel, float *h1, float *y, void *ws,
+                               size_t ws_bytes, void *stream)
+{
+    return layer_decode_impl(desc, w, x, x_pred, batch, k_heads, k_neurons, k_cache, v_cache,
+                             kv_len, sel, h1, y, ws, ws_bytes, nullptr, 0, stream, false, true);
 }
 
 int dv_layer_decode_traced(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x,

@@ -199,4 +199,82 @@ DV_DEV void st_release_gpu(int *p, int v)
 DV_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 DV_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
+// ---------------------------------------------------------------------------
+// How the body of a kernel family waits for its inputs.  Every call site is
+// reached by all threads of the CTA.
+//
+// PdlDep: the body is a kernel of its own, launched as a programmatic
+// dependent of the kernel before it.  wait() is the grid dependency, after
+// which the body lets its own dependents launch; trigger() lets them launch
+// without waiting.
+struct PdlDep {
+    DV_DEV void wait() const
+    {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
+    DV_DEV void trigger() const { pdl_launch_dependents(); }
+};
+
+// Polls of a phase counter (each ~64 ns of sleep plus an L2 round trip) and
+// the time after which a wait gives up.
+constexpr int kPhaseSpin = 1 << 20;
+constexpr unsigned long long kPhaseSpinNs = 50ull * 1000 * 1000;
+
+DV_DEV unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Poll *c (acquire) until it reaches target; false if the bound ran out.
+DV_DEV bool poll_count(const int *c, int target)
+{
+    const unsigned long long t0 = global_ns();
+    for (int it = 0; it < kPhaseSpin; ++it) {
+        if (ld_acquire_gpu(c) >= target)
+            return true;
+        if ((it & 63) == 63 && global_ns() - t0 > kPhaseSpinNs)
+            return false;
+        __nanosleep(64);
+    }
+    return ld_acquire_gpu(c) >= target;
+}
+
+// PhaseDep: the body is one phase of the persistent layer kernel.  wait()
+// returns once up to two phase counters (CTAs that finished the producing
+// phases) reach their targets.  Thread 0 polls with acquire loads, then the
+// CTA barrier passes the ordering on; a wait that runs out records
+// DV_ERR_TIMEOUT and returns, so every CTA still runs to its end.
+struct PhaseDep {
+    const int *c0, *c1;  // NULL: unused
+    int t0, t1;
+    int *status;
+    DV_DEV void wait() const
+    {
+        if (threadIdx.x == 0) {
+            bool ok = true;
+            if (c0)
+                ok = poll_count(c0, t0) && ok;
+            if (c1)
+                ok = poll_count(c1, t1) && ok;
+            if (!ok)
+                set_status(status, DV_ERR_TIMEOUT);
+        }
+        __syncthreads();
+    }
+    DV_DEV void trigger() const {}
+};
+
+// A CTA finished a phase: after the barrier, one release add counts it (the
+// release orders every write the CTA made before the barrier ahead of the
+// count; a reader's acquire poll plus barrier orders them before its reads).
+DV_DEV void phase_arrive(int *c)
+{
+    __syncthreads();
+    if (threadIdx.x == 0)
+        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(c) : "memory");
+}
+
 }  // namespace dv

@@ -150,7 +150,18 @@ struct ColArgs {
 // 16-byte chunks per lane of the column kernel (columns per block = 32 * P *
 // elements per chunk); fewer for larger batch tiles to bound registers.
 template <int NB>
-constexpr int colacc_chunks() { return NB <= 2 ? 2 : 1; }
+__host__ __device__ constexpr int colacc_chunks() { return NB <= 2 ? 2 : 1; }
+
+// Dynamic shared memory of the column kernel: block partials of the 16 warps
+// (CB columns each), then kColStageRows row offsets and coefficients (nb per
+// row) and kColMaxCover partial slots.
+constexpr int kColStageRows = 1024;
+constexpr int kColMaxCover = 512;
+__host__ __device__ constexpr size_t colacc_smem_bytes(int cb, int nb)
+{
+    return (size_t)kWarpsPerBlock * cb * 4 + (size_t)kColStageRows * 8 +
+           (size_t)kColStageRows * nb * 4 + (size_t)kColMaxCover * 4;
+}
 
 // Split-KV decode attention over the selected heads.
 struct AttnArgs {
@@ -165,6 +176,36 @@ struct AttnArgs {
     const int *side_flag; // fused decode: set once the head union is published
     int *status;
 };
+
+// Persistent layer kernel (dv_layer.cu): the seven steps of the fused decode
+// as phases of one cooperative grid, one CTA per SM, ordered by counters of
+// the CTAs that finished each phase (workspace control words, zero at rest).
+enum LayerBar {
+    kBarPred1 = 0,  // CTAs done with PRED1 (all)
+    kBarPred2,      // ... PRED2 (all, the side CTA included)
+    kBarQkv,        // ... QKV rows (all but the last CTA)
+    kBarSel,        // the last CTA's neuron selection
+    kBarAttn,       // ... attention (all but the last)
+    kBarOproj,      // ... out-projection (all but the last)
+    kBarFc1,        // ... fc1 (all)
+    kBarExit,       // CTAs at the end; the last resets every counter
+    kBarCount
+};
+constexpr int kLayerBarWord = 8;  // first control word of the counters
+
+struct LayerArgs {
+    RowArgs pred1, pred2, qkv, fc1;
+    AttnArgs attn;
+    ColArgs oproj, fc2;
+    int *bar;      // kBarCount counters
+    int *status;
+};
+
+// Dynamic shared memory of the attention kernel: the 16 warps' partial
+// outputs of dh floats.
+__host__ __device__ constexpr size_t attn_smem_bytes(int dh) { return (size_t)kWarpsPerBlock * dh * 4; }
+
+constexpr int kSelStage = 1024;  // gather indices a row-dot CTA stages in shared memory
 
 // ---------------------------------------------------------------------------
 // Workspace layout (byte offsets from the workspace base, 256-byte aligned).
@@ -201,6 +242,11 @@ cudaError_t launch_attn(int dtype, int lanes_per_key, const AttnArgs &a, dim3 gr
 cudaError_t launch_select(const SelectArgs &a, int grid, cudaStream_t st);
 size_t select_final_smem(int N);
 cudaError_t launch_copy(void *dst, const void *src, size_t n16, int grid, cudaStream_t st);
+// Persistent layer kernel (binary16 weights, head_dim 128, one batch tile of
+// nb in {1, 2} rows): cooperative launch of `grid` CTAs.
+cudaError_t launch_layer(int nb, const LayerArgs &a, int grid, size_t smem, cudaStream_t st);
+// CTAs of the persistent layer kernel one SM holds at this shared memory (0 on error).
+int layer_ctas_per_sm(int nb, size_t smem);
 
 // Largest-batch tile each kernel family handles per CTA.
 int rowdot_nb(int B, int K, int kind);

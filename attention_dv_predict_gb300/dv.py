@@ -62,11 +62,14 @@ _SIGS = {
     "dv_workspace_init": ([_P, _SZ, _P], _I),
     "dv_check": ([_P, _SZ, _P], _I),
     "dv_layer_decode_launches": ([_D, _I], _I),
+    "dv_layer_decode_persistent_ok": ([_D, _I], _I),
     "dv_predict_topk": ([_D, _W, _P, _I, _I, _I, _S, _P, _P, _P, _SZ, _P], _I),
     "dv_predict_topk_noalloc": ([_D, _W, _P, _I, _I, _I, _S, _P, _P, _P], _I),
     "dv_sparse_attn": ([_D, _W, _P, _I, _P, _P, _I, _P, _P, _I, _P, _P, _SZ, _P], _I),
     "dv_sparse_mlp": ([_D, _W, _P, _I, _P, _P, _I, _P, _P, _SZ, _P], _I),
     "dv_layer_decode": ([_D, _W, _P, _P, _I, _I, _I, _P, _P, _I, _S, _P, _P, _P, _SZ, _P], _I),
+    "dv_layer_decode_persistent": ([_D, _W, _P, _P, _I, _I, _I, _P, _P, _I, _S, _P, _P, _P, _SZ,
+                                    _P], _I),
     "dv_layer_decode_presel": ([_D, _W, _P, _I, _P, _P, _I, _P, _P, _I, _P, _P, _I, _P, _P, _P,
                                 _SZ, _P], _I),
     "dv_layer_decode_traced": ([_D, _W, _P, _P, _I, _I, _I, _P, _P, _I, _S, _P, _P, _P, _SZ,
@@ -200,6 +203,10 @@ def dv_layer_decode_launches(desc: LayerDesc, batch: int) -> int:
     return int(_lib.dv_layer_decode_launches(C.byref(desc), int(batch)))
 
 
+def dv_layer_decode_persistent_ok(desc: LayerDesc, batch: int) -> bool:
+    return bool(_lib.dv_layer_decode_persistent_ok(C.byref(desc), int(batch)))
+
+
 def dv_predict_topk(layer: Layer, x_pred: torch.Tensor, k_heads: int, k_neurons: int,
                     sel: SelectionBuffers, ws: Workspace, scores_h: Optional[torch.Tensor] = None,
                     scores_n: Optional[torch.Tensor] = None, stream=None):
@@ -244,6 +251,19 @@ def dv_layer_decode(layer: Layer, x: torch.Tensor, k_heads: int, k_neurons: int,
                     stream=None):
     B = x.shape[0]
     _check("dv_layer_decode", _lib.dv_layer_decode(
+        C.byref(layer.desc), C.byref(layer.c), _ptr(x), _ptr(x_pred), B, k_heads, k_neurons,
+        _ptr(k_cache), _ptr(v_cache), kv_len, C.byref(sel.c), _ptr(h1), _ptr(y), ws.cptr,
+        ws.nbytes, _stream(stream)))
+
+
+def dv_layer_decode_persistent(layer: Layer, x: torch.Tensor, k_heads: int, k_neurons: int,
+                               k_cache: torch.Tensor, v_cache: torch.Tensor, kv_len: int,
+                               sel: SelectionBuffers, y: torch.Tensor, ws: Workspace,
+                               x_pred: Optional[torch.Tensor] = None,
+                               h1: Optional[torch.Tensor] = None, stream=None):
+    """dv_layer_decode as one persistent kernel (see dv_layer_decode_persistent_ok)."""
+    B = x.shape[0]
+    _check("dv_layer_decode_persistent", _lib.dv_layer_decode_persistent(
         C.byref(layer.desc), C.byref(layer.c), _ptr(x), _ptr(x_pred), B, k_heads, k_neurons,
         _ptr(k_cache), _ptr(v_cache), kv_len, C.byref(sel.c), _ptr(h1), _ptr(y), ws.cptr,
         ws.nbytes, _stream(stream)))

@@ -132,6 +132,10 @@ int dv_check(void *ws, size_t ws_bytes, void *stream);
 /* Kernel launches one dv_layer_decode enqueues (for launch accounting). */
 int dv_layer_decode_launches(const dv_layer_desc *desc, int batch);
 
+/* 1 if dv_layer_decode_persistent serves this shape and batch on the current
+ * device, else 0. */
+int dv_layer_decode_persistent_ok(const dv_layer_desc *desc, int batch);
+
 /*
  * dv_predict_topk -- the lookahead predictors and top-k selection.
  * ("DejaVu Guide ...", "1. Mathematical Formulation of Lookahead Predictors":
@@ -192,11 +196,30 @@ int dv_sparse_mlp(const dv_layer_desc *desc, const dv_layer_weights *w, const fl
  * k_heads, k_neurons).)
  *   h1: optional device output [B, d] of the attention block's result
  *       (NULL keeps it in the workspace).
+ * Seven kernels (the predictors, QKV, attention, out-projection, fc1, fc2),
+ * chained by programmatic dependent launch.
  */
 int dv_layer_decode(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x,
                     const float *x_pred, int batch, int k_heads, int k_neurons, void *k_cache,
                     void *v_cache, int kv_len, const dv_selection *sel, float *h1, float *y,
                     void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * dv_layer_decode_persistent -- dv_layer_decode as one persistent
+ * cooperative kernel: one CTA per SM runs the seven steps as phases ordered
+ * by counters in the workspace instead of kernel boundaries (every wait
+ * bounded: DV_ERR_TIMEOUT in the status word if one ran out).  Serves
+ * binary16 layers with head_dim 128 at batch 1 or 2 where one CTA per SM
+ * fits (dv_layer_decode_persistent_ok); DV_ERR_UNSUPPORTED otherwise,
+ * launching nothing.  Arguments as dv_layer_decode.  The selections and the
+ * KV append are identical to dv_layer_decode's; out-projection partial sums
+ * are grouped over one CTA fewer, so y agrees to rounding, not bitwise.
+ */
+int dv_layer_decode_persistent(const dv_layer_desc *desc, const dv_layer_weights *w,
+                               const float *x, const float *x_pred, int batch, int k_heads,
+                               int k_neurons, void *k_cache, void *v_cache, int kv_len,
+                               const dv_selection *sel, float *h1, float *y, void *ws,
+                               size_t ws_bytes, void *stream);
 
 /*
  * dv_layer_decode_presel -- the layer decode on a selection computed earlier:

@@ -100,8 +100,9 @@ def make_case(cfg, B=None, k_h=None, k_n=None, kv_len=None, seed=0, gen_device="
                 kc.cpu().numpy(), vc.cpu().numpy())
 
 
-def run_gpu_layer(dv, case: Case, stream=None):
-    """dv_layer_decode on the case; returns host copies of everything."""
+def run_gpu_layer(dv, case: Case, stream=None, entry="dv_layer_decode"):
+    """`entry` (dv_layer_decode or dv_layer_decode_persistent) on the case;
+    returns host copies of everything."""
     desc = dv.desc_from_config(case.cfg, case.kv_cap)
     layer = dv.Layer(desc, case.w_dev)
     sel = dv.SelectionBuffers(desc, case.B, case.k_h, case.k_n)
@@ -112,7 +113,7 @@ def run_gpu_layer(dv, case: Case, stream=None):
     vc = torch.from_numpy(case.vc).cuda()
     y = torch.empty_like(x)
     h1 = torch.empty_like(x)
-    dv.dv_layer_decode(layer, x, case.k_h, case.k_n, kc, vc, case.kv_len, sel, y, ws, x_pred=xp,
+    getattr(dv, entry)(layer, x, case.k_h, case.k_n, kc, vc, case.kv_len, sel, y, ws, x_pred=xp,
                        h1=h1, stream=stream)
     torch.cuda.synchronize()
     assert dv.dv_check(ws) == dv.DV_OK

@@ -19,8 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdv.so")
-SOURCES = ["dv_abi.cu", "dv_rowdot.cu", "dv_colacc.cu", "dv_attn.cu", "dv_select.cu",
-           "dv_layer.cu"]
+SOURCES = ["dv_abi.cu", "dv_rowdot.cu", "dv_colacc.cu", "dv_colacc_mma.cu", "dv_attn.cu",
+           "dv_select.cu", "dv_layer.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -83,6 +83,11 @@ dv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DV_OK : DV_ERR_
 struct Launch {
     cudaStream_t st;
     int nsm;
+    // chain the call's kernels by programmatic dependent launch; off for the
+    // tensor-core configuration (binary16 from kMmaMinBatch batch rows),
+    // where the chained step measured ~113 us slower per decode than plain
+    // stream order at batches 4 and 8 (and 13 us faster at batch 1)
+    bool pdl;
     void *const *events;  // optional trace events
     int n_events;
     int next_event;
@@ -111,6 +116,7 @@ dv_status make_launch(void *stream, void *const *events, int n_events, Launch *L
         return DV_ERR_UNSUPPORTED;
     L->st = static_cast<cudaStream_t>(stream);
     L->nsm = nsm;
+    L->pdl = true;
     L->events = events;
     L->n_events = n_events;
     L->next_event = 0;
@@ -146,8 +152,8 @@ NeuronSel make_neuron_sel(const dv_layer_desc &D, int B, int kn, const dv_select
     return ns;
 }
 
-// QKV and FC1 use the tensor-core row kernel for binary16 weights from
-// kMmaMinBatch batch rows on.
+// Binary16 layers use the tensor-core row kernel (QKV, FC1) and column kernel
+// (out-projection, fc2) from kMmaMinBatch batch rows on.
 bool use_mma(const dv_layer_desc &D, int B)
 {
     return D.dtype == DV_F16 && B >= kMmaMinBatch && D.d_model % 32 == 0;
@@ -211,7 +217,7 @@ dv_status run_scores(const dv_layer_desc &D, const dv_layer_weights &w, const fl
     if (plan)
         plan->pred1 = a;
     else if (launch_rowdot(RK_PRED1, D.dtype, nb, a, grid, rowdot_smem(RK_PRED1, nb, d), lc.st,
-                           pdl_first) != cudaSuccess)
+                           lc.pdl && pdl_first) != cudaSuccess)
         return DV_ERR_CUDA;
 
     RowArgs b2;
@@ -241,7 +247,7 @@ dv_status run_scores(const dv_layer_desc &D, const dv_layer_weights &w, const fl
     if (plan)
         plan->pred2 = b2;
     else if (launch_rowdot(RK_PRED2, D.dtype, nb, b2, grid, rowdot_smem(RK_PRED2, nb, r), lc.st,
-                           true) != cudaSuccess)
+                           lc.pdl) != cudaSuccess)
         return DV_ERR_CUDA;
     return DV_OK;
 }
@@ -312,10 +318,12 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
         size_t sm = set_mma(a, D, ws, L);
         if (ns && select_final_smem(D.d_ffn) > sm)
             sm = select_final_smem(D.d_ffn);
-        if (launch_rowdot_mma(RK_QKV, a, dim3(lc.nsm, ceil_div(B, 8)), sm, lc.st, !first) !=
+        if (launch_rowdot_mma(RK_QKV, a, dim3(lc.nsm, ceil_div(B, 8)), sm, lc.st,
+                              lc.pdl && !first) !=
             cudaSuccess)
             return DV_ERR_CUDA;
-    } else if (launch_rowdot(RK_QKV, D.dtype, nb, a, grid, smem, lc.st, !first) != cudaSuccess) {
+    } else if (launch_rowdot(RK_QKV, D.dtype, nb, a, grid, smem, lc.st, lc.pdl && !first) !=
+               cudaSuccess) {
         return DV_ERR_CUDA;
     }
 
@@ -352,7 +360,7 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
         return s;
     if (plan)
         plan->attn = t;
-    else if (launch_attn(D.dtype, lpk, t, dim3(lc.nsm), lc.st, true) != cudaSuccess)
+    else if (launch_attn(D.dtype, lpk, t, dim3(lc.nsm), lc.st, lc.pdl) != cudaSuccess)
         return DV_ERR_CUDA;
 
     ColArgs c;
@@ -376,11 +384,16 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     nb = colacc_nb(B);
     if ((s = lc.mark()))
         return s;
-    if (plan)
+    if (plan) {
         plan->oproj = c;
-    else if (launch_colacc(CK_OPROJ, D.dtype, nb, c, dim3(lc.nsm, ceil_div(B, nb)), lc.st,
-                           true) != cudaSuccess)
+    } else if (use_mma(D, B)) {
+        if (launch_colacc_mma(CK_OPROJ, c, dim3(lc.nsm, ceil_div(B, 8)), lc.st, lc.pdl) !=
+            cudaSuccess)
+            return DV_ERR_CUDA;
+    } else if (launch_colacc(CK_OPROJ, D.dtype, nb, c, dim3(lc.nsm, ceil_div(B, nb)), lc.st,
+                             lc.pdl) != cudaSuccess) {
         return DV_ERR_CUDA;
+    }
     return DV_OK;
 }
 
@@ -421,11 +434,12 @@ dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float
         plan->fc1 = a;
     } else if (use_mma(D, B)) {
         const size_t sm = set_mma(a, D, ws, L);
-        if (launch_rowdot_mma(RK_FC1, a, dim3(lc.nsm, ceil_div(B, 8)), sm, lc.st, !first) !=
+        if (launch_rowdot_mma(RK_FC1, a, dim3(lc.nsm, ceil_div(B, 8)), sm, lc.st,
+                              lc.pdl && !first) !=
             cudaSuccess)
             return DV_ERR_CUDA;
     } else if (launch_rowdot(RK_FC1, D.dtype, nb, a, dim3(lc.nsm, ceil_div(B, nb)),
-                             rowdot_smem(RK_FC1, nb, d), lc.st, !first) != cudaSuccess) {
+                             rowdot_smem(RK_FC1, nb, d), lc.st, lc.pdl && !first) != cudaSuccess) {
         return DV_ERR_CUDA;
     }
 
@@ -450,11 +464,16 @@ dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float
     nb = colacc_nb(B);
     if ((s = lc.mark()))
         return s;
-    if (plan)
+    if (plan) {
         plan->fc2 = c;
-    else if (launch_colacc(CK_FC2, D.dtype, nb, c, dim3(lc.nsm, ceil_div(B, nb)), lc.st, true) !=
-             cudaSuccess)
+    } else if (use_mma(D, B)) {
+        if (launch_colacc_mma(CK_FC2, c, dim3(lc.nsm, ceil_div(B, 8)), lc.st, lc.pdl) !=
+            cudaSuccess)
+            return DV_ERR_CUDA;
+    } else if (launch_colacc(CK_FC2, D.dtype, nb, c, dim3(lc.nsm, ceil_div(B, nb)), lc.st,
+                             lc.pdl) != cudaSuccess) {
         return DV_ERR_CUDA;
+    }
     return DV_OK;
 }
 
@@ -552,6 +571,7 @@ dv_status layer_decode_impl(const dv_layer_desc *desc, const dv_layer_weights *w
     Launch lc;
     if ((s = make_launch(stream, events, n_events, &lc)))
         return s;
+    lc.pdl = !use_mma(D, batch);
     float *h1p = h1 ? h1 : at<float>(ws, L.h1);
     const int max_u_h = batch * k_heads < D.n_heads ? batch * k_heads : D.n_heads;
     const int max_u_n = batch * k_neurons < D.d_ffn ? batch * k_neurons : D.d_ffn;
@@ -763,6 +783,7 @@ int dv_predict_topk(const dv_layer_desc *desc, const dv_layer_weights *w, const 
     Launch lc;
     if ((s = make_launch(stream, nullptr, 0, &lc)))
         return s;
+    lc.pdl = !use_mma(D, batch);
     if ((s = run_scores(D, *w, x_pred, batch, scores_h, scores_n, ws, L, lc)))
         return s;
     SelectArgs sa;
@@ -799,6 +820,7 @@ int dv_sparse_attn(const dv_layer_desc *desc, const dv_layer_weights *w, const f
     Launch lc;
     if ((s = make_launch(stream, nullptr, 0, &lc)))
         return s;
+    lc.pdl = !use_mma(D, batch);
     if ((s = run_attn(D, *w, x, batch, u_h, n_u_h, max_u_h, k_cache, v_cache, kv_len, h1, ws, L,
                       lc, true, nullptr)))
         return s;
@@ -824,6 +846,7 @@ int dv_sparse_mlp(const dv_layer_desc *desc, const dv_layer_weights *w, const fl
     Launch lc;
     if ((s = make_launch(stream, nullptr, 0, &lc)))
         return s;
+    lc.pdl = !use_mma(D, batch);
     if ((s = run_mlp(D, *w, h1, batch, u_n, n_u_n, max_u_n, y, ws, L, lc, true)))
         return s;
     return cuda_status(cudaGetLastError());
@@ -852,6 +875,7 @@ int dv_layer_decode_presel(const dv_layer_desc *desc, const dv_layer_weights *w,
     Launch lc;
     if ((s = make_launch(stream, nullptr, 0, &lc)))
         return s;
+    lc.pdl = !use_mma(D, batch);
     float *h1p = h1 ? h1 : at<float>(ws, L.h1);
     if ((s = run_attn(D, *w, x, batch, u_h, n_u_h, max_u_h, k_cache, v_cache, kv_len, h1p, ws, L,
                       lc, true, nullptr)))
@@ -1051,6 +1075,7 @@ int dv_predict_topk_noalloc(const dv_layer_desc *desc, const dv_layer_weights *w
     Launch lc;
     if ((s = make_launch(stream, nullptr, 0, &lc)))
         return s;
+    lc.pdl = !use_mma(D, batch);
     if (cudaMemsetAsync(ws, 0, zero_bytes, lc.st) != cudaSuccess)
         return DV_ERR_CUDA;
     if ((s = run_scores(D, *w, x_pred, batch, scores_h, scores_n, ws, L, lc)))

@@ -259,6 +259,9 @@ cudaError_t launch_rowdot_mma(int kind, const RowArgs &a, dim3 grid, size_t smem
                               cudaStream_t st, bool pdl);
 void rowdot_mma_plan(int K, int *S, int *ks);
 size_t rowdot_mma_smem(int ks);
-constexpr int kMmaMinBatch = 3;  // batches from which QKV and FC1 use tensor cores
+constexpr int kMmaMinBatch = 3;  // batches from which binary16 layers use tensor cores
+// Tensor-core column kernel (binary16, batch tiles of 8; out-projection, fc2).
+cudaError_t launch_colacc_mma(int kind, const ColArgs &a, dim3 grid, cudaStream_t st, bool pdl);
+size_t colacc_mma_smem();
 
 }  // namespace dv

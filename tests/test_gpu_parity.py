@@ -265,6 +265,41 @@ def test_opt67b_batches_tensor_core_path(dv, B):
     check_layer_parity(case, g)
 
 
+# d = 4128 leaves a 32-column last block for the tensor-core column kernel
+# (512-column blocks); batches 3, 5 and 11 give partial and multiple tiles of 8
+RAGGED_MMA = dv_inputs.LayerConfig("ragged_mma", 4128, 6, 128, 3000, 64, 70, 1, "f16",
+                                   dv_inputs.Fraction(1, 10), k_heads_fixed=2)
+
+
+@pytest.mark.parametrize("B", [3, 5, 11])
+def test_tensor_core_paths_ragged(dv, B):
+    case = make_case(RAGGED_MMA, B=B, seed=20 + B)
+    g = run_gpu_layer(dv, case)
+    check_layer_parity(case, g)
+
+
+def test_tensor_core_column_kernel_several_stages(dv):
+    """fc2 over 18000 caller-chosen neurons at batch 8 and d = 12288: each CTA
+    holds > 2048 rows of its column block, so it stages them in two passes."""
+    cfg = dv_inputs.LayerConfig("wide_mlp", 12288, 2, 128, 20480, 64, 4, 8, "f16",
+                                dv_inputs.Fraction(1, 10), k_heads_fixed=1)
+    case = make_case(cfg, B=8, seed=31, gen_device="cuda")
+    desc = dv.desc_from_config(case.cfg, case.kv_cap)
+    layer = dv.Layer(desc, case.w_dev)
+    ws = dv.Workspace(desc, case.B)
+    rng = np.random.default_rng(3)
+    u_n = np.sort(rng.choice(cfg.d_ffn, 18000, replace=False)).astype(np.int32)
+    h1 = torch.from_numpy(case.x).cuda()
+    y = torch.empty_like(h1)
+    nun = torch.tensor([u_n.size], dtype=torch.int32, device="cuda")
+    dv.dv_sparse_mlp(layer, h1, torch.from_numpy(u_n).cuda(), nun, y, ws)
+    torch.cuda.synchronize()
+    assert dv.dv_check(ws) == dv.DV_OK
+    D = oracle.desc_from_config(case.cfg, case.kv_cap)
+    yo, _ = oracle.sparse_mlp(D, case.w_host, case.x.astype(np.float64), u_n)
+    assert_close(y.cpu().numpy() - case.x, yo - case.x, "y - h1")
+
+
 def test_opt175b_full(dv):
     case = make_case(CFG["opt175b"], gen_device="cuda", norm_affine=False)
     g = run_gpu_layer(dv, case)

@@ -387,7 +387,8 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     if (plan) {
         plan->oproj = c;
     } else if (use_mma(D, B)) {
-        if (launch_colacc_mma(CK_OPROJ, c, dim3(lc.nsm, ceil_div(B, 8)), lc.st, lc.pdl) !=
+        const int nt = colacc_mma_tiles(B);
+        if (launch_colacc_mma(CK_OPROJ, nt, c, dim3(lc.nsm, ceil_div(B, 8 * nt)), lc.st, lc.pdl) !=
             cudaSuccess)
             return DV_ERR_CUDA;
     } else if (launch_colacc(CK_OPROJ, D.dtype, nb, c, dim3(lc.nsm, ceil_div(B, nb)), lc.st,
@@ -467,7 +468,8 @@ dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float
     if (plan) {
         plan->fc2 = c;
     } else if (use_mma(D, B)) {
-        if (launch_colacc_mma(CK_FC2, c, dim3(lc.nsm, ceil_div(B, 8)), lc.st, lc.pdl) !=
+        const int nt = colacc_mma_tiles(B);
+        if (launch_colacc_mma(CK_FC2, nt, c, dim3(lc.nsm, ceil_div(B, 8 * nt)), lc.st, lc.pdl) !=
             cudaSuccess)
             return DV_ERR_CUDA;
     } else if (launch_colacc(CK_FC2, D.dtype, nb, c, dim3(lc.nsm, ceil_div(B, nb)), lc.st,

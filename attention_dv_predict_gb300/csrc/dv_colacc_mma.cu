@@ -1,5 +1,6 @@
 // dv_colacc_mma.cu -- tensor-core variant of the column-gather GEMV for batch
-// tiles of 8 rows (binary16 weights; out-projection and fc2), sm_103a.
+// tiles of 8 rows, one or two tiles per weight pass (binary16 weights;
+// out-projection and fc2), sm_103a.
 //
 //   out[b][c] = res[b][c] + bias[c] + sum_i coef[b][i] * W[row(i)][c]
 // (the kernels of dv_colacc.cuh, same gather, coefficients and residual).
@@ -13,6 +14,9 @@
 //                 carries both and the products keep ~22 bits;
 //   B (16 x 8)  = 16 gathered weight rows x 8 columns;
 //   D (16 x 8)  = hi and lo partial sums, added at the end.
+// A CTA takes NT tiles of 8 batch rows (NT = 2 above 8 rows): the B
+// fragments of each weight group feed the MMAs of every tile, so the
+// weights are read once per 8 NT batch rows.
 // Each warp owns 32 columns of a 512-column block.  The CTA copies groups of
 // 16 gathered rows x 1 KB into a shared-memory ring with cp.async (warp w
 // copies row w of the group, 512 contiguous bytes per instruction; no
@@ -33,16 +37,16 @@ namespace {
 
 constexpr int kCmCB = 32 * kWarpsPerBlock;  // columns per block (512)
 constexpr int kCmStages = 6;                // 16-row groups in flight per CTA
-constexpr int kCmSR = 2048;                 // rows staged at once (multiple of 16)
+constexpr int kCmSRT = 2048;                // rows x tiles staged at once (NT x rows <= 2048)
 constexpr int kCmLd = kCmCB + 8;            // halves per staged row (16-byte pad: ldmatrix
                                             // rows of a warp fall in distinct banks)
 constexpr size_t kCmRing = (size_t)kCmStages * 16 * kCmLd * 2;
-constexpr size_t kCmFrag = (size_t)(kCmSR / 16) * 32 * 16;
-constexpr size_t kCmOff = (size_t)kCmSR * 8;
+constexpr size_t kCmFrag = (size_t)(kCmSRT / 16) * 32 * 16;
+constexpr size_t kCmOff = (size_t)kCmSRT * 8;
 constexpr size_t kCmSmem = kCmRing + kCmFrag + kCmOff + (size_t)kMaxCover * 4;
 constexpr int kCmFill = 8;   // coefficients in flight per thread while staging
 constexpr int kCmCover = 4;  // CTA partials loaded together by the combining CTA
-static_assert(8 * kCmCB == 8 * kThreads, "the combine gives each thread 8 outputs");
+static_assert(kCmCB == kThreads, "the combine gives each thread 8 outputs of each tile");
 
 // CTA c takes pieces [total c / nc, total (c + 1) / nc).
 DV_DEV long long cm_piece0(int c, int nc, long long total) { return total * c / nc; }
@@ -89,13 +93,14 @@ DV_DEV void mma_f16(float (&d)[4], const uint4 &a, unsigned b0, unsigned b1)
         : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
 }
 
-template <int KIND, class Dep>
+template <int KIND, int NT, class Dep>
 DV_DEV void colacc_mma_body(const ColArgs &a, int cta, int nct, const Dep &dep)
 {
-    constexpr int NB = 8, CB = kCmCB;
+    constexpr int NB = 8 * NT, CB = kCmCB;
+    constexpr int SR = kCmSRT / NT;  // rows staged at once
     extern __shared__ __align__(16) unsigned char cm_smem[];
     __half *ring = reinterpret_cast<__half *>(cm_smem);
-    uint4 *frag = reinterpret_cast<uint4 *>(cm_smem + kCmRing);        // [group][lane]
+    uint4 *frag = reinterpret_cast<uint4 *>(cm_smem + kCmRing);  // [group][tile][lane]
     long long *soff = reinterpret_cast<long long *>(cm_smem + kCmRing + kCmFrag);
     int *s_cover = reinterpret_cast<int *>(cm_smem + kCmRing + kCmFrag + kCmOff);
     __shared__ int s_last, s_ncover;
@@ -128,15 +133,17 @@ DV_DEV void colacc_mma_body(const ColArgs &a, int cta, int nct, const Dep &dep)
         const int i1 = (int)min((long long)rows, i0 + (p1 - pp));
         pp += i1 - i0;
         const int col0 = cb * CB + 32 * warp;  // this warp's first column
-        float acc[4][4];
+        float acc[NT][4][4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+        for (int n = 0; n < NT; ++n)
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                acc[j][e] = 0.f;
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    acc[n][j][e] = 0.f;
 
-        for (int s0 = i0; s0 < i1; s0 += kCmSR) {
-            const int s1 = min(i1, s0 + kCmSR);
+        for (int s0 = i0; s0 < i1; s0 += SR) {
+            const int s1 = min(i1, s0 + SR);
             const int ngr = (s1 - s0 + 15) >> 4;
             __syncthreads();  // the previous stage's offsets and fragments are consumed
             for (int i = tid; i < ngr * 16; i += blockDim.x) {
@@ -176,15 +183,15 @@ DV_DEV void colacc_mma_body(const ColArgs &a, int cta, int nct, const Dep &dep)
                 waited = true;
             }
             // coefficients as A fragments: for row k of group q and batch row
-            // b, lane 4b + (k & 7) / 2 holds hi in halves (k >= 8 ? 4 : 0) +
-            // (k & 1) and lo two halves further
+            // 8n + b (tile n), lane 4b + (k & 7) / 2 of fragment (q, n) holds
+            // hi in halves (k >= 8 ? 4 : 0) + (k & 1) and lo two halves further
             const int nitems = ngr * 16 * NB;
             for (int base = tid; base < nitems; base += kCmFill * blockDim.x) {
                 float cv[kCmFill];
 #pragma unroll
                 for (int u = 0; u < kCmFill; ++u) {
                     const int it = base + u * blockDim.x;
-                    const int i = it >> 3, b = it & 7;
+                    const int i = it / NB, b = it - i * NB;
                     cv[u] = (it < nitems && s0 + i < s1 && b0 + b < a.B && soff[i] >= 0)
                                 ? coef_at<KIND>(a, b0 + b, s0 + i)
                                 : 0.f;
@@ -194,11 +201,13 @@ DV_DEV void colacc_mma_body(const ColArgs &a, int cta, int nct, const Dep &dep)
                     const int it = base + u * blockDim.x;
                     if (it >= nitems)
                         break;
-                    const int i = it >> 3, b = it & 7;
+                    const int i = it / NB, bb = it - i * NB;
+                    const int n = bb >> 3, b = bb & 7;
                     const int q = i >> 4, k = i & 15;
                     const __half hi = __float2half_rn(cv[u]);
                     const __half lo = __float2half_rn(cv[u] - __half2float(hi));
-                    __half *fh = reinterpret_cast<__half *>(frag + q * 32 + 4 * b + ((k & 7) >> 1));
+                    __half *fh = reinterpret_cast<__half *>(frag + (q * NT + n) * 32 + 4 * b +
+                                                            ((k & 7) >> 1));
                     const int ho = ((k >> 3) ? 4 : 0) + (k & 1);
                     fh[ho] = hi;
                     fh[ho + 2] = lo;
@@ -215,44 +224,56 @@ DV_DEV void colacc_mma_body(const ColArgs &a, int cta, int nct, const Dep &dep)
                 cp_async_wait<kCmStages - 2>();
                 __syncthreads();
                 issue(q + kCmStages - 1);
-                const uint4 af = frag[q * 32 + lane];
+                uint4 af[NT];
+#pragma unroll
+                for (int n = 0; n < NT; ++n)
+                    af[n] = frag[(q * NT + n) * 32 + lane];
                 const __half *slot = ring + (q % kCmStages) * 16 * kCmLd + mrow * kCmLd + mcol;
 #pragma unroll
                 for (int jp = 0; jp < 2; ++jp) {
                     unsigned bf[4];
                     ldsm_x4_trans(bf, slot + 16 * jp);
-                    mma_f16(acc[2 * jp], af, bf[0], bf[1]);
-                    mma_f16(acc[2 * jp + 1], af, bf[2], bf[3]);
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        mma_f16(acc[n][2 * jp], af[n], bf[0], bf[1]);
+                        mma_f16(acc[n][2 * jp + 1], af[n], bf[2], bf[3]);
+                    }
                 }
             }
             cp_async_wait<0>();
         }
 
-        // this piece's sums: batch row g, columns col0 + 8j + 2t (+1)
+        // this piece's sums: batch row 8n + g, columns col0 + 8j + 2t (+1)
         const bool whole = (i0 == 0 && i1 == rows);
         const int slot = (cb == first_cb) ? 0 : 1;
         if (whole) {
-            if (b0 + g < a.B) {
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const int b = b0 + 8 * n + g;
+                if (b >= a.B)
+                    continue;
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int col = col0 + 8 * j + 2 * t + e;
                         if (col < a.d)
-                            a.out[(size_t)(b0 + g) * a.d + col] =
-                                (__ldcg(a.res + (size_t)(b0 + g) * a.d + col) +
-                                 __half2float(bias[col])) +
-                                (acc[j][e] + acc[j][e + 2]);
+                            a.out[(size_t)b * a.d + col] =
+                                (__ldcg(a.res + (size_t)b * a.d + col) + __half2float(bias[col])) +
+                                (acc[n][j][e] + acc[n][j][e + 2]);
                     }
             }
             continue;
         }
         float *pp_out = a.part + (((size_t)tile * nc + cta) * 2 + slot) * NB * CB;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+        for (int n = 0; n < NT; ++n)
 #pragma unroll
-            for (int e = 0; e < 2; ++e)
-                pp_out[g * CB + 32 * warp + 8 * j + 2 * t + e] = acc[j][e] + acc[j][e + 2];
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                    pp_out[(8 * n + g) * CB + 32 * warp + 8 * j + 2 * t + e] =
+                        acc[n][j][e] + acc[n][j][e + 2];
         __threadfence();
         __syncthreads();
         if (tid == 0) {
@@ -275,9 +296,9 @@ DV_DEV void colacc_mma_body(const ColArgs &a, int cta, int nct, const Dep &dep)
                 s_ncover = min(cz - ca + 1, kMaxCover);
         }
         __syncthreads();
-        {
+        for (int n = 0; n < NT; ++n) {
             const int ncover = s_ncover;
-            const int e0 = tid * 8;  // outputs e0 .. e0 + 7: batch row e0 / CB
+            const int e0 = n * 8 * CB + tid * 8;  // outputs e0 .. e0 + 7: batch row e0 / CB
             float sum[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e)
@@ -323,22 +344,27 @@ DV_DEV void colacc_mma_body(const ColArgs &a, int cta, int nct, const Dep &dep)
         dep.wait();
 }
 
-template <int KIND>
+template <int KIND, int NT>
 __global__ void __launch_bounds__(kThreads, 1) k_colacc_mma(const ColArgs a)
 {
-    colacc_mma_body<KIND>(a, blockIdx.x, gridDim.x, PdlDep{});
+    colacc_mma_body<KIND, NT>(a, blockIdx.x, gridDim.x, PdlDep{});
 }
 
 }  // namespace
 
 size_t colacc_mma_smem() { return kCmSmem; }
 
-cudaError_t launch_colacc_mma(int kind, const ColArgs &a, dim3 grid, cudaStream_t st, bool pdl)
+int colacc_mma_tiles(int B) { return B > 8 ? 2 : 1; }
+
+cudaError_t launch_colacc_mma(int kind, int nt, const ColArgs &a, dim3 grid, cudaStream_t st,
+                              bool pdl)
 {
-    if (kind != CK_OPROJ && kind != CK_FC2)
+    if ((kind != CK_OPROJ && kind != CK_FC2) || (nt != 1 && nt != 2))
         return cudaErrorInvalidValue;
-    void (*kern)(ColArgs) = kind == CK_OPROJ ? k_colacc_mma<CK_OPROJ> : k_colacc_mma<CK_FC2>;
-    static bool configured[2][kMaxDevices] = {};
+    void (*kern)(ColArgs) =
+        kind == CK_OPROJ ? (nt == 1 ? k_colacc_mma<CK_OPROJ, 1> : k_colacc_mma<CK_OPROJ, 2>)
+                         : (nt == 1 ? k_colacc_mma<CK_FC2, 1> : k_colacc_mma<CK_FC2, 2>);
+    static bool configured[2][2][kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
@@ -346,11 +372,11 @@ cudaError_t launch_colacc_mma(int kind, const ColArgs &a, dim3 grid, cudaStream_
     if (dev < 0 || dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
     const int ki = kind == CK_OPROJ ? 0 : 1;
-    if (!configured[ki][dev]) {
+    if (!configured[ki][nt - 1][dev]) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCmSmem);
         if (e != cudaSuccess)
             return e;
-        configured[ki][dev] = true;
+        configured[ki][nt - 1][dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;

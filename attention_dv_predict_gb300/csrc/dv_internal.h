@@ -260,8 +260,11 @@ cudaError_t launch_rowdot_mma(int kind, const RowArgs &a, dim3 grid, size_t smem
 void rowdot_mma_plan(int K, int *S, int *ks);
 size_t rowdot_mma_smem(int ks);
 constexpr int kMmaMinBatch = 3;  // batches from which binary16 layers use tensor cores
-// Tensor-core column kernel (binary16, batch tiles of 8; out-projection, fc2).
-cudaError_t launch_colacc_mma(int kind, const ColArgs &a, dim3 grid, cudaStream_t st, bool pdl);
+// Tensor-core column kernel (binary16, nt batch tiles of 8 per CTA;
+// out-projection, fc2): grid.y = ceil(B / (8 nt)).
+int colacc_mma_tiles(int B);
+cudaError_t launch_colacc_mma(int kind, int nt, const ColArgs &a, dim3 grid, cudaStream_t st,
+                              bool pdl);
 size_t colacc_mma_smem();
 
 }  // namespace dv

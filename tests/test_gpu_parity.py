@@ -266,12 +266,13 @@ def test_opt67b_batches_tensor_core_path(dv, B):
 
 
 # d = 4128 leaves a 32-column last block for the tensor-core column kernel
-# (512-column blocks); batches 3, 5 and 11 give partial and multiple tiles of 8
+# (512-column blocks); batches 3, 5, 11 and 25 give partial tiles of 8 and
+# one or two CTA tiles of 16 rows (two batch tiles per weight pass)
 RAGGED_MMA = dv_inputs.LayerConfig("ragged_mma", 4128, 6, 128, 3000, 64, 70, 1, "f16",
                                    dv_inputs.Fraction(1, 10), k_heads_fixed=2)
 
 
-@pytest.mark.parametrize("B", [3, 5, 11])
+@pytest.mark.parametrize("B", [3, 5, 11, 25])
 def test_tensor_core_paths_ragged(dv, B):
     case = make_case(RAGGED_MMA, B=B, seed=20 + B)
     g = run_gpu_layer(dv, case)

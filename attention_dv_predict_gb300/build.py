@@ -40,8 +40,18 @@ def _flags(extra=()):
                    "-I", CSRC, *extra]
 
 
+def _code_only(text: str) -> str:
+    """The source with C/C++ comments removed and whitespace collapsed."""
+    import re
+
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return " ".join(text.split())
+
+
 def source_hash() -> str:
-    """sha256 over the library's sources (identifies the kernels a profile covers)."""
+    """sha256 over the library's code (identifies the kernels a profile covers;
+    comments and layout do not count)."""
     import hashlib
 
     h = hashlib.sha256()
@@ -49,8 +59,8 @@ def source_hash() -> str:
         path = os.path.normpath(os.path.join(CSRC, name))
         if os.path.isfile(path):
             h.update(name.encode())
-            with open(path, "rb") as f:
-                h.update(f.read())
+            with open(path, encoding="utf-8") as f:
+                h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

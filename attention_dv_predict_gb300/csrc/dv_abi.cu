@@ -127,9 +127,11 @@ template <typename P>
 P *at(void *ws, size_t off) { return reinterpret_cast<P *>(static_cast<char *>(ws) + off); }
 
 // ---------------------------------------------------------------------------
-// The blocks of the decode step.  Every launch after the first of a call is
-// a programmatic dependent launch (the kernels wait for their inputs with
-// griddepcontrol.wait); the first one is ordered normally after prior work.
+// The blocks of the decode step.  Where Launch::pdl is set (every call but
+// binary16 ones from kMmaMinBatch batch rows) each launch after the first of
+// a call is a programmatic dependent launch (the kernels wait for their
+// inputs with griddepcontrol.wait); the first one, and every launch when
+// pdl is off, is ordered normally after prior work.
 
 NeuronSel make_neuron_sel(const dv_layer_desc &D, int B, int kn, const dv_selection &sel,
                           void *ws, const WsLayout &L)

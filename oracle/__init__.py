@@ -40,36 +40,62 @@ class Weights(C.Structure):
 
 
 _lib = None
+_lib_omp = None
 
 
-def lib():
-    global _lib
-    if _lib is None:
-        path = _build.build()
-        L = C.CDLL(path)
-        L.dvo_half_to_double.argtypes = [C.c_uint16]
-        L.dvo_half_to_double.restype = C.c_double
-        L.dvo_double_to_half.argtypes = [C.c_double]
-        L.dvo_double_to_half.restype = C.c_uint16
-        L.dvo_norm_row.argtypes = [C.POINTER(Desc), _F64P, _P, _P, _F64P]
-        L.dvo_norm_row.restype = None
-        L.dvo_topk.argtypes = [_F32P, C.c_int, C.c_int, _I32P]
-        L.dvo_union.argtypes = [_I32P, C.c_int, C.c_int, C.c_int, _I32P, _I32P]
-        L.dvo_predict.argtypes = [C.POINTER(Desc), C.POINTER(Weights), _F32P, C.c_int, C.c_int,
-                                  C.c_int, _F32P, _F32P, _I32P, _I32P, _I32P, _I32P, _I32P, _I32P]
-        L.dvo_sparse_attn.argtypes = [C.POINTER(Desc), C.POINTER(Weights), _F32P, C.c_int, _I32P,
-                                      C.c_int, _P, _P, C.c_int, _F64P, _F64P]
-        L.dvo_sparse_mlp.argtypes = [C.POINTER(Desc), C.POINTER(Weights), _F64P, C.c_int, _I32P,
-                                     C.c_int, _F64P, _F64P]
-        L.dvo_layer.argtypes = [C.POINTER(Desc), C.POINTER(Weights), _F32P, C.c_int, _I32P, C.c_int,
-                                _I32P, C.c_int, _P, _P, C.c_int, _F64P, _F64P]
-        L.dvo_dense_layer.argtypes = [C.POINTER(Desc), C.POINTER(Weights), _F32P, C.c_int, _P, _P,
-                                      C.c_int, _F64P, _F64P, _F64P]
-        for f in ("dvo_topk", "dvo_union", "dvo_predict", "dvo_sparse_attn", "dvo_sparse_mlp",
-                  "dvo_layer", "dvo_dense_layer"):
-            getattr(L, f).restype = C.c_int
-        _lib = L
-    return _lib
+def _load(path: str):
+    L = C.CDLL(path)
+    L.dvo_half_to_double.argtypes = [C.c_uint16]
+    L.dvo_half_to_double.restype = C.c_double
+    L.dvo_double_to_half.argtypes = [C.c_double]
+    L.dvo_double_to_half.restype = C.c_uint16
+    L.dvo_norm_row.argtypes = [C.POINTER(Desc), _F64P, _P, _P, _F64P]
+    L.dvo_norm_row.restype = None
+    L.dvo_topk.argtypes = [_F32P, C.c_int, C.c_int, _I32P]
+    L.dvo_union.argtypes = [_I32P, C.c_int, C.c_int, C.c_int, _I32P, _I32P]
+    L.dvo_predict.argtypes = [C.POINTER(Desc), C.POINTER(Weights), _F32P, C.c_int, C.c_int,
+                              C.c_int, _F32P, _F32P, _I32P, _I32P, _I32P, _I32P, _I32P, _I32P]
+    L.dvo_sparse_attn.argtypes = [C.POINTER(Desc), C.POINTER(Weights), _F32P, C.c_int, _I32P,
+                                  C.c_int, _P, _P, C.c_int, _F64P, _F64P]
+    L.dvo_sparse_mlp.argtypes = [C.POINTER(Desc), C.POINTER(Weights), _F64P, C.c_int, _I32P,
+                                 C.c_int, _F64P, _F64P]
+    L.dvo_layer.argtypes = [C.POINTER(Desc), C.POINTER(Weights), _F32P, C.c_int, _I32P, C.c_int,
+                            _I32P, C.c_int, _P, _P, C.c_int, _F64P, _F64P]
+    L.dvo_dense_layer.argtypes = [C.POINTER(Desc), C.POINTER(Weights), _F32P, C.c_int, _P, _P,
+                                  C.c_int, _F64P, _F64P, _F64P]
+    L.dvo_layer_decode.argtypes = [C.POINTER(Desc), C.POINTER(Weights), _F32P, _F32P, C.c_int,
+                                   C.c_int, C.c_int, _P, _P, C.c_int, _F32P, _F32P, _I32P,
+                                   _I32P, _I32P, _I32P, _I32P, _I32P, _F64P, _F64P]
+    L.dvo_set_threads.argtypes = [C.c_int]
+    L.dvo_set_threads.restype = C.c_int
+    for f in ("dvo_topk", "dvo_union", "dvo_predict", "dvo_sparse_attn", "dvo_sparse_mlp",
+              "dvo_layer", "dvo_dense_layer", "dvo_layer_decode"):
+        getattr(L, f).restype = C.c_int
+    return L
+
+
+def lib(threads: int = 0):
+    """The oracle library.  threads == 0: the plain single-threaded build;
+    threads > 0 (or -1 for every host core): the OpenMP build, set to that
+    many threads (same results bit for bit)."""
+    global _lib, _lib_omp
+    if threads == 0:
+        if _lib is None:
+            _lib = _load(_build.build())
+        return _lib
+    if _lib_omp is None:
+        _build.build()
+        path = _build.build_omp()
+        if path is None:
+            raise RuntimeError("the OpenMP build of the oracle is unavailable on this host")
+        _lib_omp = _load(path)
+    _lib_omp.dvo_set_threads(int(threads))
+    return _lib_omp
+
+
+def threads_used(threads: int) -> int:
+    """Threads the library chosen by ``threads`` runs its loops on."""
+    return 1 if threads == 0 else lib(threads).dvo_set_threads(int(threads))
 
 
 def _ptr(a: np.ndarray, ctype=None):
@@ -149,7 +175,8 @@ def union(idx: np.ndarray, n: int) -> np.ndarray:
     return out[: int(cnt[0])].copy()
 
 
-def predict(D: Desc, w: Dict[str, np.ndarray], x_pred: np.ndarray, k_h: int, k_n: int):
+def predict(D: Desc, w: Dict[str, np.ndarray], x_pred: np.ndarray, k_h: int, k_n: int,
+            threads: int = 0):
     """Scores (binary32), per-row top-k and unions.  Returns a dict."""
     W = _W(D, w)
     x = np.ascontiguousarray(x_pred, dtype=np.float32)
@@ -163,7 +190,7 @@ def predict(D: Desc, w: Dict[str, np.ndarray], x_pred: np.ndarray, k_h: int, k_n
     u_n = np.empty(N, np.int32)
     nuh = np.zeros(1, np.int32)
     nun = np.zeros(1, np.int32)
-    _rc(lib().dvo_predict(C.byref(D), C.byref(W.s), _ptr(x, _F32P), B, k_h, k_n,
+    _rc(lib(threads).dvo_predict(C.byref(D), C.byref(W.s), _ptr(x, _F32P), B, k_h, k_n,
                           _ptr(s_h, _F32P), _ptr(s_n, _F32P), _ptr(idx_h, _I32P),
                           _ptr(idx_n, _I32P), _ptr(u_h, _I32P), _ptr(nuh, _I32P),
                           _ptr(u_n, _I32P), _ptr(nun, _I32P)), "dvo_predict")
@@ -209,7 +236,7 @@ def sparse_mlp(D: Desc, w, h1, u_n):
     return y, pre[:, : u.size]
 
 
-def layer(D: Desc, w, x, u_h, u_n, k_cache, v_cache, kv_len, inplace=False):
+def layer(D: Desc, w, x, u_h, u_n, k_cache, v_cache, kv_len, inplace=False, threads: int = 0):
     """Sparse layer on the given unions: (h1, y, k_cache, v_cache)."""
     W = _W(D, w)
     x = np.ascontiguousarray(x, dtype=np.float32)
@@ -219,7 +246,7 @@ def layer(D: Desc, w, x, u_h, u_n, k_cache, v_cache, kv_len, inplace=False):
     kc, vc = _caches(D, k_cache, v_cache, inplace)
     h1 = np.empty((B, D.d_model), np.float64)
     y = np.empty((B, D.d_model), np.float64)
-    _rc(lib().dvo_layer(C.byref(D), C.byref(W.s), _ptr(x, _F32P), B, _ptr(uh, _I32P), uh.size,
+    _rc(lib(threads).dvo_layer(C.byref(D), C.byref(W.s), _ptr(x, _F32P), B, _ptr(uh, _I32P), uh.size,
                         _ptr(un, _I32P), un.size, _ptr(kc), _ptr(vc), kv_len, _ptr(h1, _F64P),
                         _ptr(y, _F64P)), "dvo_layer")
     return h1, y, kc, vc
@@ -240,12 +267,38 @@ def dense_layer(D: Desc, w, x, k_cache, v_cache, kv_len, inplace=False):
     return h1, y, pre, kc, vc
 
 
-def layer_decode(D: Desc, w, x, k_h, k_n, k_cache, v_cache, kv_len, x_pred=None, inplace=False):
-    """Predict from x_pred (default x), then the sparse layer on the unions."""
-    p = predict(D, w, x if x_pred is None else x_pred, k_h, k_n)
-    h1, y, kc, vc = layer(D, w, x, p["u_h"], p["u_n"], k_cache, v_cache, kv_len, inplace)
-    p.update({"h1": h1, "y": y, "k_cache": kc, "v_cache": vc})
-    return p
+def layer_decode(D: Desc, w, x, k_h, k_n, k_cache, v_cache, kv_len, x_pred=None, inplace=False,
+                 threads: int = 0):
+    """The whole decode step (``dvo_layer_decode``): predict from x_pred
+    (x when None), then the sparse layer on x over the predicted unions.
+    Returns the dict of ``predict`` plus h1, y and the appended caches."""
+    W = _W(D, w)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    B = x.shape[0]
+    xp = None if x_pred is None else np.ascontiguousarray(x_pred, dtype=np.float32)
+    if xp is not None and xp.shape != x.shape:
+        raise ValueError("x_pred must have the shape of x")
+    H, N = D.n_heads, D.d_ffn
+    kc, vc = _caches(D, k_cache, v_cache, inplace)
+    s_h = np.empty((B, H), np.float32)
+    s_n = np.empty((B, N), np.float32)
+    idx_h = np.empty((B, k_h), np.int32)
+    idx_n = np.empty((B, k_n), np.int32)
+    u_h = np.empty(H, np.int32)
+    u_n = np.empty(N, np.int32)
+    nuh = np.zeros(1, np.int32)
+    nun = np.zeros(1, np.int32)
+    h1 = np.empty((B, D.d_model), np.float64)
+    y = np.empty((B, D.d_model), np.float64)
+    _rc(lib(threads).dvo_layer_decode(C.byref(D), C.byref(W.s), _ptr(x, _F32P),
+                               None if xp is None else _ptr(xp, _F32P), B, k_h, k_n, _ptr(kc),
+                               _ptr(vc), kv_len, _ptr(s_h, _F32P), _ptr(s_n, _F32P),
+                               _ptr(idx_h, _I32P), _ptr(idx_n, _I32P), _ptr(u_h, _I32P),
+                               _ptr(nuh, _I32P), _ptr(u_n, _I32P), _ptr(nun, _I32P),
+                               _ptr(h1, _F64P), _ptr(y, _F64P)), "dvo_layer_decode")
+    return {"s_h": s_h, "s_n": s_n, "idx_h": idx_h, "idx_n": idx_n,
+            "u_h": u_h[: int(nuh[0])].copy(), "u_n": u_n[: int(nun[0])].copy(),
+            "h1": h1, "y": y, "k_cache": kc, "v_cache": vc}
 
 
 def numpy_weights(w_torch: Dict) -> Dict[str, np.ndarray]:
@@ -255,4 +308,4 @@ def numpy_weights(w_torch: Dict) -> Dict[str, np.ndarray]:
 
 __all__ = ["Desc", "make_desc", "desc_from_config", "half_to_double", "double_to_half",
            "norm_row", "topk", "union", "predict", "sparse_attn", "sparse_mlp", "layer",
-           "dense_layer", "layer_decode", "numpy_weights", "lib"]
+           "dense_layer", "layer_decode", "numpy_weights", "lib", "threads_used"]

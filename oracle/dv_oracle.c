@@ -9,7 +9,14 @@
  * Arithmetic: every product and sum is in IEEE binary64, in plain loops whose
  * order is the order of the definitions below.  Weights are read in the
  * caller's storage type (binary32, or binary16 decoded exactly), so the oracle
- * sees the same weight values as the GPU path.  Single-threaded.
+ * sees the same weight values as the GPU path.
+ *
+ * Threads: built plainly, the library is single-threaded and the OpenMP
+ * pragmas below are ignored.  Built with -fopenmp (a second library, used only
+ * to time the CPU baseline on every host core), the loops over independent
+ * output elements -- scores, projected rows, output columns -- are shared out
+ * among threads.  Each element is still one thread's plain loop in the same
+ * order, so both builds give the same bits.
  *
  * Sources (the DejaVu pages):
  *  [P1-MF]  "DejaVu Guide: Contextual Sparsity for LLM Inference",
@@ -51,6 +58,9 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 /* ------------------------------------------------------------------------ */
 /* binary16 <-> binary64 from the IEEE 754 binary16 layout:                  */
@@ -251,18 +261,21 @@ int dvo_predict(const dvo_desc *D, const dvo_weights *W, const float *x_pred, in
         return 2;
     for (int b = 0; b < B; ++b) {
         const float *xb = x_pred + (size_t)b * d;
+#pragma omp parallel for schedule(static)
         for (int h = 0; h < H; ++h) {
             double acc = 0.0;
             for (int c = 0; c < d; ++c)
                 acc += (double)xb[c] * ld(W->pred_h, t, (size_t)h * d + c);
             s_h[(size_t)b * H + h] = (float)acc;
         }
+#pragma omp parallel for schedule(static)
         for (int q = 0; q < r; ++q) {
             double acc = 0.0;
             for (int c = 0; c < d; ++c)
                 acc += (double)xb[c] * ld(W->pred_a, t, (size_t)q * d + c);
             u[q] = acc;
         }
+#pragma omp parallel for schedule(static)
         for (int j = 0; j < N; ++j) {
             double acc = 0.0;
             for (int q = 0; q < r; ++q)
@@ -319,6 +332,7 @@ int dvo_sparse_attn(const dvo_desc *D, const dvo_weights *W, const float *x, int
         for (int j = 0; j < n_u_h; ++j) {
             int h = u_h[j];
             size_t cache_row0 = ((size_t)b * H + h) * (size_t)cap; /* position 0 */
+#pragma omp parallel for collapse(2) schedule(static)
             for (int tt = 0; tt < 3; ++tt) {
                 for (int e = 0; e < dh; ++e) {
                     size_t row = ((size_t)tt * H + h) * dh + e;
@@ -356,6 +370,7 @@ int dvo_sparse_attn(const dvo_desc *D, const dvo_weights *W, const float *x, int
         }
         if (attn_o)
             memcpy(attn_o + (size_t)b * n_u_h * dh, o, (size_t)n_u_h * dh * sizeof(double));
+#pragma omp parallel for schedule(static)
         for (int c = 0; c < d; ++c) {
             double acc = 0.0;
             for (int j = 0; j < n_u_h; ++j)
@@ -393,6 +408,7 @@ int dvo_sparse_mlp(const dvo_desc *D, const dvo_weights *W, const double *h1, in
     for (int b = 0; b < B; ++b) {
         const double *hb = h1 + (size_t)b * d;
         dvo_norm_row(D, hb, W->ln2_g, W->ln2_b, hn);
+#pragma omp parallel for schedule(static)
         for (int i = 0; i < n_u_n; ++i) {
             size_t j = (size_t)u_n[i];
             double acc = 0.0;
@@ -403,6 +419,7 @@ int dvo_sparse_mlp(const dvo_desc *D, const dvo_weights *W, const double *h1, in
                 pre[(size_t)b * n_u_n + i] = p;
             a[i] = p > 0.0 ? p : 0.0;
         }
+#pragma omp parallel for schedule(static)
         for (int c = 0; c < d; ++c) {
             double acc = 0.0;
             for (int i = 0; i < n_u_n; ++i)
@@ -532,4 +549,20 @@ int dvo_layer_decode(const dvo_desc *D, const dvo_weights *W, const float *x,
     if (rc)
         return rc;
     return dvo_layer(D, W, x, B, u_h, *n_u_h, u_n, *n_u_n, k_cache, v_cache, kv_len, h1, y);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Threads used by the OpenMP build (n <= 0: every available core); returns  */
+/* the number its loops will use.  The plain build always returns 1.         */
+int dvo_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n <= 0)
+        n = omp_get_num_procs();
+    omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
 }

@@ -15,7 +15,9 @@ fails at least one test:
   dense layer bit for bit; a perfect ReLU mask equals the dense MLP bit for
   bit; unselected rows, heads and KV contribute nothing;
 * a dense brute force built from numpy/scipy library routines on the tiny
-  shape, and the page's PyTorch listing restated in torch on the CPU.
+  shape, and the sparse MLP against the dense MLP under a 0/1 neuron mask
+  with the selection from numpy scores and a stable argsort;
+* the whole decode step against its parts (predict on x_pred, layer on x).
 """
 
 import math
@@ -402,32 +404,78 @@ def test_dense_layer_numpy_brute_force(dtype, B):
     np.testing.assert_allclose(yo, y, rtol=1e-11, atol=1e-11)
 
 
-def test_page_listing_restated_in_torch():
-    """The guide's PyTorch listing (predictor -> topk -> gather fc1 rows ->
-    activation -> gather fc2 columns -> down-projection -> residual), with the
-    OPT substitutions (ReLU, LayerNorm, biases, low-rank neuron scorer)."""
-    import torch.nn.functional as F
+def _ref_topk_rows(scores, k):
+    """Per-row k largest binary32 scores, ties to the lower index, ascending:
+    a stable argsort on (-score, index), independent of the oracle's sort."""
+    out = []
+    for row in np.asarray(scores, np.float32):
+        keys = np.where(row == 0.0, np.float32(0.0), row)  # -0 and +0 are equal
+        order = np.lexsort((np.arange(row.size), -keys.astype(np.float64)))
+        out.append(np.sort(order[:k]))
+    return np.array(out, np.int32)
 
-    cfg, D, w, _, _, x = _tiny_random(B=1)
-    rng = np.random.default_rng(10)
-    h1 = rng.standard_normal((1, cfg.d_model))
-    t = {k: torch.from_numpy(v.astype(np.float64)) for k, v in w.items()}
-    xp = torch.from_numpy(x.astype(np.float64))
-    head_scores = F.linear(xp, t["pred_h"])
-    neuron_scores = F.linear(F.linear(xp, t["pred_a"]), t["pred_b"])
-    active_heads = torch.topk(head_scores, cfg.k_heads, dim=-1).indices.squeeze(0)
-    active = torch.topk(neuron_scores, cfg.k_neurons, dim=-1).indices.squeeze(0)
+
+def test_sparse_mlp_equals_masked_dense_mlp():
+    """The sparse MLP is the dense MLP with every unselected neuron's
+    activation forced to zero (the guide's "Core Innovation 2:
+    Hardware-Efficient Dynamic Sparse Matrix Execution": only the selected
+    neurons' fc1 rows and fc2 columns take part).  The selection comes from
+    the low-rank scores computed here with numpy in binary64 and rounded to
+    binary32, top-k by a stable argsort; the MLP is dense numpy with a 0/1
+    mask over the union of the rows' sets."""
+    cfg, D, w, _, _, x = _tiny_random(B=2)
+    f = {k: v.astype(np.float64) for k, v in w.items()}
+    xp = x.astype(np.float64)
+    s_n = ((xp @ f["pred_a"].T) @ f["pred_b"].T).astype(np.float32)
+    s_h = (xp @ f["pred_h"].T).astype(np.float32)
+    idx_n = _ref_topk_rows(s_n, cfg.k_neurons)
+    idx_h = _ref_topk_rows(s_h, cfg.k_heads)
     p = oracle.predict(D, w, x, cfg.k_heads, cfg.k_neurons)
-    assert np.array_equal(np.sort(active_heads.numpy()), p["idx_h"][0])
-    assert np.array_equal(np.sort(active.numpy()), p["idx_n"][0])
-    hin = torch.from_numpy(h1)
-    normed = F.layer_norm(hin, (cfg.d_model,), t["ln2_g"], t["ln2_b"], eps=cfg.ln_eps)
-    w1_sparse = t["w1"][active, :]
-    inter = F.relu(F.linear(normed, w1_sparse, t["b1"][active]))
-    w2_sparse = t["w2T"].T[:, active]
-    out = hin + F.linear(inter, w2_sparse, t["b2"])
-    y, _ = oracle.sparse_mlp(D, w, h1, p["idx_n"][0])
-    np.testing.assert_allclose(y, out.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.array_equal(p["idx_n"], idx_n) and np.array_equal(p["idx_h"], idx_h)
+    u_n = np.union1d(idx_n[0], idx_n[1]).astype(np.int32)
+    assert np.array_equal(p["u_n"], u_n)
+
+    rng = np.random.default_rng(10)
+    h1 = rng.standard_normal((2, cfg.d_model))
+    hn = _np_layernorm(h1, f["ln2_g"], f["ln2_b"], cfg.ln_eps)
+    mask = np.zeros(cfg.d_ffn)
+    mask[u_n] = 1.0
+    act = np.maximum(hn @ f["w1"].T + f["b1"], 0.0) * mask
+    y_ref = h1 + f["b2"] + act @ f["w2T"]
+    y, _ = oracle.sparse_mlp(D, w, h1, u_n)
+    np.testing.assert_allclose(y, y_ref, rtol=1e-12, atol=1e-12)
+    # the mask matters: the dense MLP differs
+    y_dense = h1 + f["b2"] + np.maximum(hn @ f["w1"].T + f["b1"], 0.0) @ f["w2T"]
+    assert np.max(np.abs(y_dense - y)) > 1e-6
+
+
+def test_layer_decode_composes_predict_and_layer():
+    """The decode step predicts the sets from x_pred and runs the layer on x
+    over them (the guide's "Core Innovation 1: Asynchronous Lookahead
+    Predictors": a layer's sets come from an earlier input).  x_pred != x
+    with different sets, so a swap of the two inputs anywhere in the
+    composition changes the result; x_pred = None means x."""
+    cfg, D, w, kc, vc, x = _tiny_random(dtype="f16", B=3)
+    xp = dv_inputs.make_x(cfg.with_(dtype="f16"), 3, 7, "cpu").numpy()
+    p = oracle.predict(D, w, xp, cfg.k_heads, cfg.k_neurons)
+    px = oracle.predict(D, w, x, cfg.k_heads, cfg.k_neurons)
+    assert not np.array_equal(p["u_n"], px["u_n"])
+    kc0, vc0 = kc.copy(), vc.copy()
+    r = oracle.layer_decode(D, w, x, cfg.k_heads, cfg.k_neurons, kc, vc, cfg.kv_len, x_pred=xp)
+    assert np.array_equal(kc, kc0) and np.array_equal(vc, vc0)  # inputs untouched
+    for key in ("s_h", "s_n", "idx_h", "idx_n", "u_h", "u_n"):
+        assert np.array_equal(r[key], p[key]), key
+    h1, y, kc1, vc1 = oracle.layer(D, w, x, p["u_h"], p["u_n"], kc, vc, cfg.kv_len)
+    assert np.array_equal(r["h1"], h1) and np.array_equal(r["y"], y)
+    assert np.array_equal(r["k_cache"], kc1) and np.array_equal(r["v_cache"], vc1)
+    h1s, _, _, _ = oracle.layer(D, w, xp, p["u_h"], p["u_n"], kc, vc, cfg.kv_len)
+    assert not np.array_equal(h1s, h1)  # the layer input is x, not x_pred
+    r0 = oracle.layer_decode(D, w, x, cfg.k_heads, cfg.k_neurons, kc, vc, cfg.kv_len)
+    r1 = oracle.layer_decode(D, w, x, cfg.k_heads, cfg.k_neurons, kc, vc, cfg.kv_len, x_pred=x)
+    for key in ("u_h", "u_n", "h1", "y", "k_cache", "v_cache"):
+        assert np.array_equal(r0[key], r1[key]), key
+    for key in ("u_h", "u_n"):
+        assert np.array_equal(r0[key], px[key]), key
 
 
 def test_oracle_rejects_bad_arguments():

@@ -486,23 +486,46 @@ def _oracle_inputs(cfg, layer, cache, x):
     return D, w, kc.cpu().numpy(), vc.cpu().numpy(), x.cpu().numpy()
 
 
-def cpu_baseline(cfg, layer, cache, x, k_h, k_n, budget_s):
-    """The CPU oracle (single-threaded C, binary64) on the same workload."""
-    import oracle
-
-    D, w, kc, vc, xh = _oracle_inputs(cfg, layer, cache, x)
+def _time_oracle(fn, budget_s, min_runs=3, max_runs=50):
     times = []
     t_end = time.perf_counter() + budget_s
     while True:
         t = time.perf_counter()
-        oracle.layer_decode(D, w, xh, k_h, k_n, kc, vc, cfg.kv_len, inplace=True)
+        fn()
         times.append(time.perf_counter() - t)
-        if time.perf_counter() >= t_end or len(times) >= 50:
+        if len(times) >= max_runs or (time.perf_counter() >= t_end and len(times) >= min_runs):
             break
-    us = statistics.median(times) * 1e6
-    return {"value": round(us, 1), "unit": "µs per layer-decode", "cores": 1, "kind": "oracle",
-            "sample": f"{len(times)} full layer decodes of the same {cfg.name} workload "
-                      f"(median), single-threaded C oracle on the host"}
+    return statistics.median(times) * 1e6, len(times)
+
+
+def cpu_baseline(cfg, layer, cache, x, k_h, k_n, budget_s):
+    """The CPU oracle (C, binary64) on the same workload: on every host core
+    (the OpenMP build, same bits) and on one thread."""
+    import oracle
+
+    D, w, kc, vc, xh = _oracle_inputs(cfg, layer, cache, x)
+    host = os.cpu_count() or 1
+
+    def run(threads):
+        return _time_oracle(lambda: oracle.layer_decode(D, w, xh, k_h, k_n, kc, vc, cfg.kv_len,
+                                                        inplace=True, threads=threads),
+                            budget_s / 2)
+
+    us1, n1 = run(0)
+    single = {"value": round(us1, 1), "cores": 1, "runs": n1}
+    try:
+        cores = oracle.threads_used(-1)
+        usn, nn = run(-1)
+    except RuntimeError:  # no OpenMP build on this host: the single-thread figure only
+        return {"value": round(us1, 1), "unit": "µs per layer-decode", "cores": 1,
+                "host_cores": host, "kind": "oracle", "single_thread": single,
+                "sample": f"{n1} full layer decodes of the same {cfg.name} workload (median), "
+                          "single-threaded C oracle (no OpenMP on this host)"}
+    return {"value": round(usn, 1), "unit": "µs per layer-decode", "cores": cores,
+            "host_cores": host, "kind": "oracle", "single_thread": single,
+            "sample": f"{nn} full layer decodes of the same {cfg.name} workload (median) on "
+                      f"{cores} threads (OpenMP build of the C oracle, same bits); "
+                      f"single_thread: {n1} decodes on one thread"}
 
 
 # ---------------------------------------------------------------------------
@@ -532,9 +555,15 @@ def run_reference(args):
     kch, vch, xh = kc.cpu().numpy(), vc.cpu().numpy(), x.cpu().numpy()
     D = oracle.desc_from_config(cfg)
 
+    try:
+        threads = -1
+        cores = oracle.threads_used(threads)
+    except RuntimeError:  # no OpenMP build on this host
+        threads, cores = 0, 1
+
     def one():
         oracle.layer_decode(D, wn, xh, cfg.k_heads, cfg.k_neurons, kch, vch, cfg.kv_len,
-                            inplace=True)
+                            inplace=True, threads=threads)
 
     budget = 150.0
     t = time.perf_counter()
@@ -555,10 +584,11 @@ def run_reference(args):
         "steps_run": steps_run, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_config(cfg, B),
-        "cpu_baseline": {"value": round(us, 1), "unit": "µs per layer-decode", "cores": 1,
-                         "kind": "oracle",
+        "cpu_baseline": {"value": round(us, 1), "unit": "µs per layer-decode", "cores": cores,
+                         "host_cores": os.cpu_count() or 1, "kind": "oracle",
                          "sample": f"{steps_run} of the {args.steps} requested steps (bounded to "
-                                   f"~{int(budget)} s), each one full layer decode"},
+                                   f"~{int(budget)} s), each one full layer decode on {cores} "
+                                   f"thread(s)"},
         "e2e": {"value": round(us, 1), "unit": "µs per layer-decode", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "note": "the reference arm is the CPU oracle (no upstream code exists to install)",

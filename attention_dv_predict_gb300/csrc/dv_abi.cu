@@ -1,10 +1,14 @@
 // dv_abi.cu -- C entry points of libdv: argument checks, workspace layout and
 // the launch sequence of the sparse layer decode.  See include/dv.h.
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "dv_internal.h"
 
@@ -549,11 +553,159 @@ int persistent_plan(const dv_layer_desc &D, int B, int nsm, size_t *smem)
     return nb;
 }
 
+// The streaming kernel (dv_stream.cu) serves binary16 layers with 128-wide
+// heads at batches of 1 and 2 whose shapes fit its tiling: rows of at most
+// 4 x 512 chunks (d <= 16384), predictor rank <= 1024, a column-group split
+// of the SMs, and one CTA per SM with the shared memory below.  Fills `a`
+// (all but the call's pointers) and returns true when it serves.
+bool stream_plan(const dv_layer_desc &D, int B, int k_h, int k_n, int kv_len, int G,
+                 StreamArgs *a, int *ni, size_t *smem)
+{
+    if (D.dtype != DV_F16 || D.head_dim != 128 || B < 1 || B > 2 || G < 2 ||
+        G > kStreamMaxCtas)
+        return false;
+    const int d = D.d_model, cpr = d / 8;
+    const int nseg = ceil_div(cpr, kStreamUnitBytes / 16);
+    if (d % 8 || nseg > 4 || D.pred_rank % 8 || D.pred_rank > 1024 || D.n_heads > 256)
+        return false;
+    int ncg = 0;
+    for (int c : {8, 4, 2, 1})
+        if (G % c == 0 && 8 * ceil_div(cpr, c) <= 2048 && G / c <= kStreamMaxGroupCtas) {
+            ncg = c;
+            break;
+        }
+    if (!ncg)
+        return false;
+    const int cg = 8 * ceil_div(cpr, ncg), gm = G / ncg;
+    const int max_u_h = std::min(D.n_heads, B * k_h), max_u_n = std::min(D.d_ffn, B * k_n);
+    int C = (G - 1) / (B * max_u_h);
+    C = std::max(1, std::min(C, std::min(kMaxAttnChunks, kv_len + 1)));
+    const size_t uni = stream_union_bytes(B, D.d_ffn, max_u_h, max_u_n, cg, gm);
+    const size_t fixed = stream_smem_bytes((int)uni, 0);
+    if (fixed + 4 * (size_t)kStreamStageBytes > kStreamSmemMax)
+        return false;
+    const int nst = (int)std::min<size_t>(kStreamMaxStages,
+                                          (kStreamSmemMax - fixed) / kStreamStageBytes);
+    const size_t sm = stream_smem_bytes((int)uni, nst);
+    // one CTA per SM must fit; the answer is kept per device and size
+    struct Fit {
+        int dev, nb, ni;
+        size_t smem;
+        int ctas;
+    };
+    static std::mutex mu;
+    static Fit known[32];
+    static int n_known = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return false;
+    int ctas = -1;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < n_known; ++i)
+            if (known[i].dev == dev && known[i].nb == B && known[i].ni == nseg &&
+                known[i].smem == sm)
+                ctas = known[i].ctas;
+        if (ctas < 0) {
+            ctas = stream_ctas_per_sm(B, nseg, sm);
+            if (n_known < 32)
+                known[n_known++] = Fit{dev, B, nseg, sm, ctas};
+        }
+    }
+    if (ctas < 1)
+        return false;
+    std::memset(a, 0, sizeof(*a));
+    a->B = B;
+    a->d = d;
+    a->H = D.n_heads;
+    a->dh = D.head_dim;
+    a->N = D.d_ffn;
+    a->r = D.pred_rank;
+    a->k_h = k_h;
+    a->k_n = k_n;
+    a->max_u_h = max_u_h;
+    a->max_u_n = max_u_n;
+    a->kv_len = kv_len;
+    a->kv_cap = D.kv_cap;
+    a->norm_kind = D.norm;
+    a->eps = D.ln_eps;
+    a->q_scale = (float)(1.0 / std::sqrt((double)D.head_dim));
+    a->G = G;
+    a->nseg = nseg;
+    a->ncg = ncg;
+    a->gm = gm;
+    a->cg = cg;
+    a->attn_C = C;
+    a->nstages = nst;
+    a->uni_bytes = (int)uni;
+    *ni = nseg;
+    *smem = sm;
+    return true;
+}
+
+dv_status stream_launch(const dv_layer_desc &D, const dv_layer_weights &w, const float *x,
+                        const float *xp, int B, int k_h, int k_n, void *kc, void *vc, int kv_len,
+                        const dv_selection &sel, float *h1, float *y, void *ws, const WsLayout &L,
+                        const Launch &lc, bool *served)
+{
+    StreamArgs a;
+    int ni = 0;
+    size_t smem = 0;
+    *served = false;
+    if (!stream_plan(D, B, k_h, k_n, kv_len, lc.nsm, &a, &ni, &smem))
+        return DV_OK;
+    *served = true;
+    a.x = x;
+    a.x_pred = xp;
+    a.ln1_g = w.ln1_g;
+    a.ln1_b = w.ln1_b;
+    a.w_qkv = w.w_qkv;
+    a.b_qkv = w.b_qkv;
+    a.w_oT = w.w_oT;
+    a.b_o = w.b_o;
+    a.ln2_g = w.ln2_g;
+    a.ln2_b = w.ln2_b;
+    a.w1 = w.w1;
+    a.b1 = w.b1;
+    a.w2T = w.w2T;
+    a.b2 = w.b2;
+    a.pred_h = w.pred_h;
+    a.pred_a = w.pred_a;
+    a.pred_b = w.pred_b;
+    a.kc = kc;
+    a.vc = vc;
+    a.idx_h = sel.idx_h;
+    a.idx_n = sel.idx_n;
+    a.u_h = sel.u_h;
+    a.n_u_h = sel.n_u_h;
+    a.u_n = sel.u_n;
+    a.n_u_n = sel.n_u_n;
+    a.h1 = h1;
+    a.y = y;
+    a.part1 = at<float>(ws, L.st_part1);
+    a.s_h = at<float>(ws, L.s_h);
+    a.s_n = at<float>(ws, L.s_n);
+    a.partQ = at<float>(ws, L.st_partQ);
+    a.attn_rec = at<float>(ws, L.attn_part);
+    a.partO = at<float>(ws, L.st_partO);
+    a.stats = at<float>(ws, L.st_stats);
+    a.partF = at<float>(ws, L.st_partF);
+    a.partY = at<float>(ws, L.st_partY);
+    a.hist = at<int>(ws, L.hist);
+    a.rowbits = at<unsigned>(ws, L.nbits);
+    a.cand_key = at<unsigned>(ws, L.cand_key);
+    a.cand_idx = at<int>(ws, L.cand_idx);
+    a.cand_cnt = at<int>(ws, L.cand_cnt);
+    a.ctl = at<int>(ws, L.ctl);
+    return cuda_status(launch_stream(B, ni, a, smem, lc.st));
+}
+
 dv_status layer_decode_impl(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x,
                             const float *x_pred, int batch, int k_heads, int k_neurons, void *kc,
                             void *vc, int kv_len, const dv_selection *sel, float *h1, float *y,
                             void *ws, size_t ws_bytes, void *const *events, int n_events,
-                            void *stream, bool pdl_first, bool persistent = false)
+                            void *stream, bool pdl_first, bool persistent = false,
+                            bool chained = false)
 {
     dv_status s = check_desc(desc);
     if (s)
@@ -596,6 +748,17 @@ dv_status layer_decode_impl(const dv_layer_desc *desc, const dv_layer_weights *w
     side.norm_kind = D.norm;
     side.eps = D.ln_eps;
     side.xn = at<float>(ws, L.xn);
+    if (!events && !chained) {  // the streaming kernel where it serves
+        bool served = false;
+        s = stream_launch(D, *w, x, x_pred ? x_pred : x, batch, k_heads, k_neurons, kc, vc, kv_len,
+                          *sel, h1p, y, ws, L, lc, &served);
+        if (s)
+            return s;
+        if (served)
+            return cuda_status(cudaGetLastError());
+        if (persistent)
+            return DV_ERR_UNSUPPORTED;
+    }
     if (persistent) {  // one persistent kernel
         size_t psmem = 0;
         const int pnb = events ? 0 : persistent_plan(D, batch, lc.nsm, &psmem);
@@ -691,6 +854,17 @@ bool ws_layout(const dv_layer_desc &D, int B, WsLayout *L)
         L->mma_part = take(tiles * groups * S * 128 * 4);
         L->mma_cnt = take(tiles * groups * 4);
     }
+    {  // streaming kernel (binary16, batches 1-2; sized for either when B <= 2)
+        const size_t nseg = (size_t)ceil_div(D.d_model / 8, kStreamUnitBytes / 16);
+        const size_t bs = (size_t)(B <= 2 ? B : 0);
+        L->st_part1 = take(bs * (H + r) * nseg * 4);
+        L->st_partQ = take(bs * 3 * H * dh * nseg * 4);
+        L->st_partF = take(bs * N * nseg * 4);
+        // G x cg <= gm x (d + 8 ncg), gm <= kStreamMaxGroupCtas, ncg <= 8
+        L->st_partO = take(bs * kStreamMaxGroupCtas * (d + 64) * 4);
+        L->st_partY = take(bs * kStreamMaxGroupCtas * (d + 64) * 4);
+        L->st_stats = take(bs * kStreamMaxCtas * 4 * 4);
+    }
     L->total = off;
     L->bpad = (int)bp;
     L->attn_splits_max = (int)splits;
@@ -763,9 +937,30 @@ int dv_layer_decode_persistent_ok(const dv_layer_desc *desc, int batch)
     if (check_desc(desc) != DV_OK || batch < 1 || batch > DV_MAX_BATCH)
         return 0;
     Launch lc;
+    StreamArgs a;
+    int ni = 0;
     size_t sm = 0;
     return make_launch(nullptr, nullptr, 0, &lc) == DV_OK &&
-           persistent_plan(*desc, batch, lc.nsm, &sm) != 0;
+           stream_plan(*desc, batch, desc->n_heads, desc->d_ffn, desc->kv_cap - 1, lc.nsm, &a,
+                       &ni, &sm);
+}
+
+int dv_layer_decode_plan(const dv_layer_desc *desc, int batch, int k_heads, int k_neurons,
+                         int kv_len)
+{
+    if (check_desc(desc) != DV_OK || batch < 1 || batch > DV_MAX_BATCH || k_heads < 1 ||
+        k_heads > desc->n_heads || k_neurons < 1 || k_neurons > desc->d_ffn || kv_len < 0 ||
+        kv_len >= desc->kv_cap)
+        return 0;
+    Launch lc;
+    StreamArgs a;
+    int ni = 0;
+    size_t sm = 0;
+    if (make_launch(nullptr, nullptr, 0, &lc) != DV_OK)
+        return 0;
+    return stream_plan(*desc, batch, k_heads, k_neurons, kv_len, lc.nsm, &a, &ni, &sm)
+               ? 1
+               : kLayerLaunches;
 }
 
 int dv_predict_topk(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x_pred,
@@ -898,6 +1093,16 @@ int dv_layer_decode(const dv_layer_desc *desc, const dv_layer_weights *w, const 
                              kv_len, sel, h1, y, ws, ws_bytes, nullptr, 0, stream, false);
 }
 
+int dv_layer_decode_chained(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x,
+                            const float *x_pred, int batch, int k_heads, int k_neurons,
+                            void *k_cache, void *v_cache, int kv_len, const dv_selection *sel,
+                            float *h1, float *y, void *ws, size_t ws_bytes, void *stream)
+{
+    return layer_decode_impl(desc, w, x, x_pred, batch, k_heads, k_neurons, k_cache, v_cache,
+                             kv_len, sel, h1, y, ws, ws_bytes, nullptr, 0, stream, false, false,
+                             true);
+}
+
 int dv_layer_decode_persistent(const dv_layer_desc *desc, const dv_layer_weights *w,
                                const float *x, const float *x_pred, int batch, int k_heads,
                                int k_neurons, void *k_cache, void *v_cache, int kv_len,
@@ -965,6 +1170,18 @@ int dv_layer_decode_host(const dv_layer_desc *desc, const dv_layer_weights *w, c
     return cuda_status(cudaStreamSynchronize(st));
 }
 
+int dv_test_hold_wait(void *ws, size_t ws_bytes, int wait_id, int budget_us, void *stream)
+{
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < 256)
+        return DV_ERR_WORKSPACE;
+    if (wait_id < 0 || wait_id > 9 || budget_us < 1)
+        return DV_ERR_INVALID_ARG;
+    static_assert(kSwHold == kSwBudget + 1, "budget and hold are adjacent control words");
+    const int words[2] = {wait_id ? budget_us : 0, wait_id};
+    return cuda_status(cudaMemcpyAsync(static_cast<int *>(ws) + kSwBudget, words, sizeof(words),
+                                       cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream)));
+}
+
 int dv_hbm_copy(void *dst, const void *src, size_t bytes, void *stream)
 {
     if (!ptr_ok(dst) || !ptr_ok(src) || bytes == 0 || (bytes & 15u))
@@ -995,7 +1212,11 @@ constexpr size_t kNoallocScratch = DV_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratch];
 
 std::mutex g_noalloc_mu;
-void *g_noalloc_base[kMaxDevices];
+struct NoallocBase {
+    unsigned long long ctx_id;  // unique ID of the context the address belongs to (0: none)
+    void *ptr;
+};
+NoallocBase g_noalloc_base[kMaxDevices];
 
 // Layout inside the scratch.  The fields the kernels require to start at
 // zero (status word, first-digit histograms, candidate counters, row
@@ -1029,8 +1250,42 @@ size_t noalloc_layout(const dv_layer_desc &D, int B, WsLayout *L, size_t *zero_b
     return off;
 }
 
-// Device address of the scratch on the current device.  The first call per
-// device looks it up (this may load the library's device code).
+// Unique ID of the calling thread's current CUDA context (0 if there is none
+// or the driver cannot tell).  Context IDs are never reused within a process,
+// so a context re-created after cudaDeviceReset gets a new one.  The two
+// driver calls are resolved through the runtime, so the library does not link
+// the driver library itself.
+unsigned long long current_context_id()
+{
+    static std::once_flag once;
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+        get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of the scratch on the current device.  It is looked up with
+// the device current the first time the device is used, and again whenever
+// the device's context has changed since (after cudaDeviceReset the module is
+// loaded anew and the array may move); where the context cannot be
+// identified it is looked up on every call.
 dv_status noalloc_base(void **out)
 {
     int dev = 0;
@@ -1039,15 +1294,20 @@ dv_status noalloc_base(void **out)
     if (dev < 0 || dev >= kMaxDevices)
         return DV_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> guard(g_noalloc_mu);
-    if (!g_noalloc_base[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
-            return DV_ERR_CUDA;
-        if (reinterpret_cast<uintptr_t>(p) & 255u)
-            return DV_ERR_WORKSPACE;
-        g_noalloc_base[dev] = p;
+    NoallocBase &nb = g_noalloc_base[dev];
+    const unsigned long long id = current_context_id();
+    if (id != 0 && nb.ctx_id == id && nb.ptr) {
+        *out = nb.ptr;
+        return DV_OK;
     }
-    *out = g_noalloc_base[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
+        return DV_ERR_CUDA;
+    if (reinterpret_cast<uintptr_t>(p) & 255u)
+        return DV_ERR_WORKSPACE;
+    nb.ctx_id = current_context_id();  // the lookup may have created the context
+    nb.ptr = p;
+    *out = p;
     return DV_OK;
 }
 

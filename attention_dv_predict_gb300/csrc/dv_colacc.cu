@@ -18,19 +18,12 @@ cudaError_t launch_one(const ColArgs &a, dim3 grid, cudaStream_t st, bool pdl)
     constexpr int CB = 32 * P * Elem<T>::EPC;
     const size_t smem = colacc_smem_bytes(CB, NB);
     auto kern = k_colacc<T, NB, KIND, P>;
-    static bool configured[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static DeviceOnce once;
+    cudaError_t e = once.run([&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    });
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= kMaxDevices)
-        return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess)
-            return e;
-        configured[dev] = true;
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);

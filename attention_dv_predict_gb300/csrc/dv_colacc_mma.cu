@@ -364,20 +364,13 @@ cudaError_t launch_colacc_mma(int kind, int nt, const ColArgs &a, dim3 grid, cud
     void (*kern)(ColArgs) =
         kind == CK_OPROJ ? (nt == 1 ? k_colacc_mma<CK_OPROJ, 1> : k_colacc_mma<CK_OPROJ, 2>)
                          : (nt == 1 ? k_colacc_mma<CK_FC2, 1> : k_colacc_mma<CK_FC2, 2>);
-    static bool configured[2][2][kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static DeviceOnce once[2][2];
+    cudaError_t e = once[kind == CK_OPROJ ? 0 : 1][nt - 1].run([&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kCmSmem);
+    });
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= kMaxDevices)
-        return cudaErrorInvalidDevice;
-    const int ki = kind == CK_OPROJ ? 0 : 1;
-    if (!configured[ki][nt - 1][dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCmSmem);
-        if (e != cudaSuccess)
-            return e;
-        configured[ki][nt - 1][dev] = true;
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);

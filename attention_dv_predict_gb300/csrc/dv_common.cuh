@@ -121,17 +121,33 @@ DV_DEV int warp_incl_scan(int v, int lane)
     return v;
 }
 
-// Exclusive prefix sum over the block (blockDim.x a multiple of 32, <= 1024).
+// Thread groups that the block-wide helpers below work over.  CtaGroup is
+// the whole CTA (__syncthreads).  ConsumerGroup is the first kConsumers
+// threads of a CTA whose remaining warp runs on its own (the weight producer
+// of the streaming layer kernel): it synchronises on named barrier 1, so the
+// other warp never has to join.
+struct CtaGroup {
+    DV_DEV static int size() { return blockDim.x; }
+    DV_DEV static void sync() { __syncthreads(); }
+};
+constexpr int kConsumers = 512;
+struct ConsumerGroup {
+    DV_DEV static int size() { return kConsumers; }
+    DV_DEV static void sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+};
+
+// Exclusive prefix sum over the group (a multiple of 32 threads, <= 1024).
 // `scratch` holds >= 33 ints of shared memory.  Returns this thread's
-// exclusive prefix; *total receives the block total.  Contains barriers.
+// exclusive prefix; *total receives the group total.  Contains barriers.
+template <class Grp = CtaGroup>
 DV_DEV int block_excl_scan(int v, int *scratch, int *total)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nw = blockDim.x >> 5;
+    const int nw = Grp::size() >> 5;
     int inc = warp_incl_scan(v, lane);
     if (lane == 31)
         scratch[warp] = inc;
-    __syncthreads();
+    Grp::sync();
     if (warp == 0) {
         int t = lane < nw ? scratch[lane] : 0;
         int ti = warp_incl_scan(t, lane);
@@ -140,31 +156,32 @@ DV_DEV int block_excl_scan(int v, int *scratch, int *total)
         if (lane == 31)
             scratch[32] = ti;
     }
-    __syncthreads();
+    Grp::sync();
     int r = scratch[warp] + inc - v;
     *total = scratch[32];
-    __syncthreads();
+    Grp::sync();
     return r;
 }
 
-// Sum over the block (float); result valid in every thread.  Barriers inside.
+// Sum over the group (float); result valid in every thread.  Barriers inside.
+template <class Grp = CtaGroup>
 DV_DEV float block_sum(float v, float *scratch)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nw = blockDim.x >> 5;
+    const int nw = Grp::size() >> 5;
     v = warp_sum(v);
     if (lane == 0)
         scratch[warp] = v;
-    __syncthreads();
+    Grp::sync();
     if (warp == 0) {
         float t = lane < nw ? scratch[lane] : 0.f;
         t = warp_sum(t);
         if (lane == 0)
             scratch[32] = t;
     }
-    __syncthreads();
+    Grp::sync();
     float r = scratch[32];
-    __syncthreads();
+    Grp::sync();
     return r;
 }
 

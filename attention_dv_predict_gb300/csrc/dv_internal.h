@@ -6,6 +6,9 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "dv.h"
 
 namespace dv {
@@ -19,6 +22,38 @@ constexpr int kMaxAttnChunks = 64;               // attention chunks per (batch 
 constexpr int kAttnRec = 4;                      // floats before o[] in a split record
 constexpr size_t kSmemCap = 200 * 1024;          // dynamic shared memory budget
 constexpr int kMaxDevices = 64;
+
+// One-time set-up of a kernel per device (its shared-memory opt-in, made
+// once so that later launches can be captured in a CUDA graph): run(f) calls
+// f() with the current device until it has succeeded once.  First calls from
+// several host threads are serialised by a mutex; later calls cost one
+// atomic load.
+class DeviceOnce {
+public:
+    template <class F>
+    cudaError_t run(F &&f)
+    {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess)
+            return e;
+        if (dev < 0 || dev >= kMaxDevices)
+            return cudaErrorInvalidDevice;
+        if (done_[dev].load(std::memory_order_acquire))
+            return cudaSuccess;
+        std::lock_guard<std::mutex> lock(mu_);
+        if (done_[dev].load(std::memory_order_relaxed))
+            return cudaSuccess;
+        e = f();
+        if (e == cudaSuccess)
+            done_[dev].store(true, std::memory_order_release);
+        return e;
+    }
+
+private:
+    std::atomic<bool> done_[kMaxDevices] = {};
+    std::mutex mu_;
+};
 
 enum RowKind { RK_PRED1 = 0, RK_PRED2 = 1, RK_QKV = 2, RK_FC1 = 3 };
 enum ColKind { CK_OPROJ = 0, CK_FC2 = 1 };
@@ -223,6 +258,9 @@ struct WsLayout {
     size_t nbits, cand_key, cand_idx, cand_cnt;  // neuron selection state
     size_t xn;  // normalised input of the attention block (fused decode)
     size_t mma_part, mma_cnt;  // tensor-core row kernel: group partials and counters
+    // streaming kernel: segment sums of the predictor, QKV and fc1 rows,
+    // column partials of the out-projection and fc2, norm statistics
+    size_t st_part1, st_partQ, st_partF, st_partO, st_partY, st_stats;
     size_t total;
     int bpad;         // batch rounded up to the largest batch tile (8)
     int attn_splits_max;
@@ -266,5 +304,92 @@ int colacc_mma_tiles(int B);
 cudaError_t launch_colacc_mma(int kind, int nt, const ColArgs &a, dim3 grid, cudaStream_t st,
                               bool pdl);
 size_t colacc_mma_smem();
+
+
+// ---------------------------------------------------------------------------
+// Streaming layer kernel (dv_stream.cu): the whole decode step as one
+// persistent cooperative grid whose producer warp streams every selected
+// weight byte into a shared-memory ring (bulk copies) while the consumer warps
+// compute; phases hand over through counters in the workspace control words.
+constexpr int kStreamStageBytes = 16384;  // one ring stage
+constexpr int kStreamMaxStages = 16;
+constexpr int kStreamThreads = 544;       // 16 consumer warps + the producer warp
+constexpr int kStreamUnitBytes = 8192;    // a row segment: 512 chunks of 16 bytes
+
+// Control words of the streaming kernel (int offsets into the workspace's
+// control block; all zero at rest).
+enum StreamWord {
+    kSwPred1 = 16,  // CTAs done with the predictor's first stage
+    kSwPred2,       // ... its neuron scores (histogram complete)
+    kSwPass,        // ... their share of the neuron selection pass
+    kSwQkv,         // ... QKV (all but the last CTA)
+    kSwAttn,        // ... attention (all CTAs)
+    kSwNorm2,       // ... the out-projection sums of their columns and the norm statistics
+    kSwFc1,         // ... fc1
+    kSwExit,        // CTAs at the end; the last resets the words
+    kSwHeads,       // flag: head selection published
+    kSwNeurons,     // flag: neuron selection published
+    kSwBudget,      // test hook: wait budget in microseconds (0: the default)
+    kSwHold,        // test hook: id of a wait that is made never to complete (0: none)
+    kSwOproj = 32,  // [8] per column group: CTAs done with their out-projection partials
+    kSwFc2 = 40,    // [8] per column group: ... fc2 partials
+    kSwEnd = 48
+};
+
+struct StreamArgs {
+    int B, d, H, dh, N, r;
+    int k_h, k_n, max_u_h, max_u_n;
+    int kv_len, kv_cap;
+    int norm_kind;
+    float eps, q_scale;
+    const float *x, *x_pred;
+    // binary16 weights (dv_layer_weights order)
+    const void *ln1_g, *ln1_b, *w_qkv, *b_qkv, *w_oT, *b_o, *ln2_g, *ln2_b, *w1, *b1, *w2T, *b2,
+        *pred_h, *pred_a, *pred_b;
+    void *kc, *vc;
+    int32_t *idx_h, *idx_n, *u_h, *n_u_h, *u_n, *n_u_n;
+    float *h1, *y;
+    // geometry
+    int G;       // CTAs (one per SM)
+    int nseg;    // 512-chunk segments of a d-long row
+    int ncg;     // column groups of the out-projection and fc2
+    int gm;      // CTAs per column group (G / ncg)
+    int cg;      // columns of the widest group (groups split the row's 16-byte
+                 // chunks into ncg nearly equal runs); stride of the partials
+    int attn_C;  // attention chunks per (batch row, head)
+    int nstages; // ring stages
+    int uni_bytes;  // shared-memory union region (phase scratch)
+    // workspace
+    float *part1;     // [B][(H + r) nseg] predictor row-segment sums
+    float *s_h, *s_n; // [B][H], [B][N] scores
+    float *partQ;     // [B][3 max_u_h dh nseg] QKV row-segment sums
+    float *attn_rec;  // [B][max_u_h][attn_C][kAttnRec + dh]
+    float *partO;     // [G][B][cg] out-projection column partials (a group's own width)
+    float *stats;     // [G][B][4] norm statistics of each CTA's columns
+    float *partF;     // [B][max_u_n nseg] fc1 row-segment sums
+    float *partY;     // [G][B][cg] fc2 column partials
+    int *hist;        // [B][kTopkBins]
+    unsigned *rowbits, *cand_key;
+    int *cand_idx, *cand_cnt;
+    int *ctl;         // control block ([0] status)
+};
+
+// The streaming kernel's column partials assume at most this many CTAs per
+// column group (workspace sizing).
+constexpr int kStreamMaxGroupCtas = 32;
+constexpr int kStreamMaxCtas = 512;
+
+// Launch of the streaming kernel for a batch of nb (1 or 2) and ni 512-chunk
+// segments per row (1..4); cooperative, `grid` CTAs of kStreamThreads.
+cudaError_t launch_stream(int nb, int ni, const StreamArgs &a, size_t smem, cudaStream_t st);
+// CTAs of the streaming kernel one SM holds at this shared memory (0 on error).
+int stream_ctas_per_sm(int nb, int ni, size_t smem);
+// Shared memory of the streaming kernel: fixed part + union + ring, and the
+// fixed part alone.
+size_t stream_smem_bytes(int uni_bytes, int nstages);
+size_t stream_fixed_smem();
+// Bytes of the union region (the largest phase scratch) for these sizes.
+size_t stream_union_bytes(int B, int N, int max_u_h, int max_u_n, int cg, int gm);
+constexpr size_t kStreamSmemMax = 226 * 1024;  // dynamic part (the opt-in limit is 227 KB)
 
 }  // namespace dv

@@ -90,20 +90,13 @@ template <int NB>
 cudaError_t launch_nb(const LayerArgs &a, int grid, size_t smem, cudaStream_t st)
 {
     auto kern = k_layer<__half, NB, 16>;
-    static bool configured[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static DeviceOnce once;
+    cudaError_t e = once.run([&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kSmemCap);
+    });
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= kMaxDevices)
-        return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSmemCap);
-        if (e != cudaSuccess)
-            return e;
-        configured[dev] = true;
-    }
     if (smem > kSmemCap)
         return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};

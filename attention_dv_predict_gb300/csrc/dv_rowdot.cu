@@ -256,20 +256,13 @@ cudaError_t launch_one(const RowArgs &a, dim3 grid, size_t smem, cudaStream_t st
     auto kern = k_rowdot<T, NB, KIND, U>;
     // Opt in to the shared-memory budget once per device (not per launch, so
     // later launches may be captured into a CUDA graph).
-    static bool configured[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static DeviceOnce once;
+    cudaError_t e = once.run([&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kSmemCap);
+    });
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= kMaxDevices)
-        return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSmemCap);
-        if (e != cudaSuccess)
-            return e;
-        configured[dev] = true;
-    }
     if (smem > kSmemCap || a.geo.U != U)
         return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
@@ -371,20 +364,13 @@ cudaError_t launch_rowdot_mma(int kind, const RowArgs &a, dim3 grid, size_t smem
     if (kind != RK_QKV && kind != RK_FC1)
         return cudaErrorInvalidValue;
     void (*kern)(RowArgs) = kind == RK_QKV ? k_rowdot_mma<RK_QKV> : k_rowdot_mma<RK_FC1>;
-    static bool configured[2][kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static DeviceOnce once[2];
+    cudaError_t e = once[kind == RK_QKV ? 0 : 1].run([&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kSmemCap);
+    });
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= kMaxDevices)
-        return cudaErrorInvalidDevice;
-    const int ki = kind == RK_QKV ? 0 : 1;
-    if (!configured[ki][dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap);
-        if (e != cudaSuccess)
-            return e;
-        configured[ki][dev] = true;
-    }
     if (smem > kSmemCap)
         return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};

@@ -40,20 +40,13 @@ size_t select_final_smem(int N) { return neuron_final_smem_bytes(N); }
 
 cudaError_t launch_select(const SelectArgs &a, int grid, cudaStream_t st)
 {
-    static bool configured[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static DeviceOnce once;
+    cudaError_t e = once.run([] {
+        return cudaFuncSetAttribute(k_select_final, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kSmemCap);
+    });
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= kMaxDevices)
-        return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        e = cudaFuncSetAttribute(k_select_final, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSmemCap);
-        if (e != cudaSuccess)
-            return e;
-        configured[dev] = true;
-    }
     const size_t smem = neuron_final_smem_bytes(a.ns.N);
     if (smem > kSmemCap)
         return cudaErrorInvalidValue;

@@ -117,9 +117,10 @@ DV_DEV int head_select(const float *s_h, int B, int H, int k, unsigned *sbits, i
 // Neuron selection (state: NeuronSel in the workspace).
 
 // Block-wide: bin of the krem-th largest key of a histogram of nb bins.
+template <class Grp = CtaGroup>
 DV_DEV void block_find_bin(const int *hist, int nb, int krem, int *scr)
 {
-    const int nt = blockDim.x, tid = threadIdx.x;
+    const int nt = Grp::size(), tid = threadIdx.x;
     const int per = (nb + nt - 1) / nt;
     const int top = nb - 1 - tid * per;
     int c = 0;
@@ -129,7 +130,7 @@ DV_DEV void block_find_bin(const int *hist, int nb, int krem, int *scr)
             c += hist[bin];
     }
     int tot;
-    const int before = block_excl_scan(c, scr + 4, &tot);
+    const int before = block_excl_scan<Grp>(c, scr + 4, &tot);
     if (before < krem && krem <= before + c) {
         int acc = before;
         for (int q = 0; q < per; ++q) {
@@ -145,15 +146,16 @@ DV_DEV void block_find_bin(const int *hist, int nb, int krem, int *scr)
             acc += h;
         }
     }
-    __syncthreads();
+    Grp::sync();
 }
 
 // The pass of one CTA over bitmap words [w0, w1) of every row (all threads
 // of the CTA).  Words are whole: each belongs to exactly one CTA.  hbuf:
 // shared [kTopkBins]; scr: shared [48]; sb1: shared [B].
+template <class Grp = CtaGroup>
 DV_DEV void neuron_pass(const NeuronSel &ns, int w0, int w1, int *sb1, int *hbuf, int *scr)
 {
-    const int tid = threadIdx.x, nt = blockDim.x;
+    const int tid = threadIdx.x, nt = Grp::size();
     const int lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
     const int W = (ns.N + 31) >> 5;
     for (int b = 0; b < ns.B; ++b) {
@@ -161,12 +163,12 @@ DV_DEV void neuron_pass(const NeuronSel &ns, int w0, int w1, int *sb1, int *hbuf
         const int *gh = ns.hist + (size_t)b * kTopkBins;
         for (int i = tid; i < kTopkBins; i += nt)
             hbuf[i] = ld_cg(gh + i);
-        __syncthreads();
-        block_find_bin(hbuf, kTopkBins, ns.k, scr);
+        Grp::sync();
+        block_find_bin<Grp>(hbuf, kTopkBins, ns.k, scr);
         if (tid == 0)
             sb1[b] = scr[0];
     }
-    __syncthreads();
+    Grp::sync();
     for (int b = 0; b < ns.B; ++b) {
         const unsigned b1 = (unsigned)sb1[b];
         const float *s = ns.s_n + (size_t)b * ns.N;
@@ -213,16 +215,17 @@ __host__ __device__ inline size_t neuron_final_smem_bytes(int N)
 }
 
 // Ascending indices of the set bits of bits[0..W), block-wide.
+template <class Grp = CtaGroup>
 DV_DEV int block_compact_bits(const unsigned *bits, int W, int32_t *out, int *scr)
 {
-    const int nt = blockDim.x, tid = threadIdx.x;
+    const int nt = Grp::size(), tid = threadIdx.x;
     const int per = (W + nt - 1) / nt;
     const int w0 = min(W, tid * per), w1 = min(W, w0 + per);
     int cnt = 0;
     for (int w = w0; w < w1; ++w)
         cnt += __popc(bits[w]);
     int tot;
-    int pos = block_excl_scan(cnt, scr + 4, &tot);
+    int pos = block_excl_scan<Grp>(cnt, scr + 4, &tot);
     for (int w = w0; w < w1; ++w) {
         unsigned b = bits[w];
         while (b) {
@@ -236,9 +239,10 @@ DV_DEV int block_compact_bits(const unsigned *bits, int W, int32_t *out, int *sc
 
 // Candidates beyond the capacity (many keys share the k-th key's top 11
 // bits): finish exactly with passes over the global scores.  Slow, rare.
+template <class Grp = CtaGroup>
 DV_DEV void neuron_overflow(const float *s, int N, unsigned prefix, int krem, const FinalSmem &sm)
 {
-    const int tid = threadIdx.x, nt = blockDim.x;
+    const int tid = threadIdx.x, nt = Grp::size();
     unsigned pmask = 0xffe00000u;
     const int shifts[2] = {10, 0};
     const int widths[2] = {11, 10};
@@ -246,18 +250,18 @@ DV_DEV void neuron_overflow(const float *s, int N, unsigned prefix, int krem, co
         const int shift = shifts[pass], nbins = 1 << widths[pass];
         for (int i = tid; i < nbins; i += nt)
             sm.hist[i] = 0;
-        __syncthreads();
+        Grp::sync();
         for (int i = tid; i < N; i += nt) {
             const unsigned key = score_key(ld_cg(s + i));
             if ((key & pmask) == prefix)
                 atomicAdd(&sm.hist[(key >> shift) & (unsigned)(nbins - 1)], 1);
         }
-        __syncthreads();
-        block_find_bin(sm.hist, nbins, krem, sm.scr);
+        Grp::sync();
+        block_find_bin<Grp>(sm.hist, nbins, krem, sm.scr);
         prefix |= (unsigned)sm.scr[0] << shift;
         pmask |= (unsigned)(nbins - 1) << shift;
         krem = sm.scr[1];
-        __syncthreads();
+        Grp::sync();
     }
     const unsigned T = prefix;
     int seen = 0;
@@ -266,25 +270,26 @@ DV_DEV void neuron_overflow(const float *s, int N, unsigned prefix, int krem, co
         const unsigned key = i < N ? score_key(ld_cg(s + i)) : 0u;
         const int eq = (i < N && key == T) ? 1 : 0;
         int tot;
-        const int rank = block_excl_scan(eq, sm.scr + 4, &tot);
+        const int rank = block_excl_scan<Grp>(eq, sm.scr + 4, &tot);
         if (i < N && (key > T || (eq && seen + rank < krem)))
             atomicOr(&sm.rowbits[i >> 5], 1u << (i & 31));
         seen += tot;
     }
-    __syncthreads();
+    Grp::sync();
 }
 
 // Finish row b: sm.rowbits holds the keys above bin b1, sm.ckey / sm.cidx the
 // ncand keys inside it (all of them when ncand <= kTopkCand; else the row is
 // finished from the global scores).  Selects the krem largest candidates
 // (ties to the lower index), adds the row to sm.ubits and writes idx_n[b].
+template <class Grp = CtaGroup>
 DV_DEV void neuron_row_finish(const NeuronSel &ns, int b, unsigned b1, int krem, int ncand,
                               const FinalSmem &sm)
 {
-    const int tid = threadIdx.x, nt = blockDim.x;
+    const int tid = threadIdx.x, nt = Grp::size();
     const int W = (ns.N + 31) >> 5;
     if (ncand > kTopkCand) {
-        neuron_overflow(ns.s_n + (size_t)b * ns.N, ns.N, b1 << 21, krem, sm);
+        neuron_overflow<Grp>(ns.s_n + (size_t)b * ns.N, ns.N, b1 << 21, krem, sm);
     } else {
         unsigned prefix = b1 << 21, pmask = 0xffe00000u;
         int kr = krem;
@@ -294,18 +299,18 @@ DV_DEV void neuron_row_finish(const NeuronSel &ns, int b, unsigned b1, int krem,
             const int shift = shifts[pass], nbins = 1 << widths[pass];
             for (int i = tid; i < nbins; i += nt)
                 sm.hist[i] = 0;
-            __syncthreads();
+            Grp::sync();
             for (int i = tid; i < ncand; i += nt) {
                 const unsigned key = sm.ckey[i];
                 if ((key & pmask) == prefix)
                     atomicAdd(&sm.hist[(key >> shift) & (unsigned)(nbins - 1)], 1);
             }
-            __syncthreads();
-            block_find_bin(sm.hist, nbins, kr, sm.scr);
+            Grp::sync();
+            block_find_bin<Grp>(sm.hist, nbins, kr, sm.scr);
             prefix |= (unsigned)sm.scr[0] << shift;
             pmask |= (unsigned)(nbins - 1) << shift;
             kr = sm.scr[1];
-            __syncthreads();
+            Grp::sync();
         }
         const unsigned T = prefix;
         const int need_eq = kr;
@@ -329,45 +334,48 @@ DV_DEV void neuron_row_finish(const NeuronSel &ns, int b, unsigned b1, int krem,
                 atomicOr(&sm.rowbits[idx >> 5], 1u << (idx & 31));
             }
         }
-        __syncthreads();
+        Grp::sync();
     }
     for (int i = tid; i < W; i += nt)
         sm.ubits[i] |= sm.rowbits[i];
-    block_compact_bits(sm.rowbits, W, ns.idx_n + (size_t)b * ns.k, sm.scr);
+    block_compact_bits<Grp>(sm.rowbits, W, ns.idx_n + (size_t)b * ns.k, sm.scr);
 }
 
 // Union of the rows (sm.ubits) to u_n / n_u_n.
+template <class Grp = CtaGroup>
 DV_DEV void neuron_union_out(const NeuronSel &ns, const FinalSmem &sm)
 {
     const int W = (ns.N + 31) >> 5;
-    __syncthreads();
-    const int tot = block_compact_bits(sm.ubits, W, ns.u_n, sm.scr);
+    Grp::sync();
+    const int tot = block_compact_bits<Grp>(sm.ubits, W, ns.u_n, sm.scr);
     if (threadIdx.x == 0)
         *ns.n_u_n = tot;
 }
 
 // Bin b1 of the k-th largest key of row b and the rank krem left inside it,
 // from the row's global first-digit histogram (staged in sm.hist).
+template <class Grp = CtaGroup>
 DV_DEV void neuron_row_bin(const NeuronSel &ns, int b, const FinalSmem &sm, unsigned *b1,
                            int *krem)
 {
-    const int tid = threadIdx.x, nt = blockDim.x;
+    const int tid = threadIdx.x, nt = Grp::size();
     const int *ghist = ns.hist + (size_t)b * kTopkBins;
     for (int i = tid; i < kTopkBins; i += nt)
         sm.hist[i] = __ldcg(ghist + i);
-    __syncthreads();
-    block_find_bin(sm.hist, kTopkBins, ns.k, sm.scr);
+    Grp::sync();
+    block_find_bin<Grp>(sm.hist, kTopkBins, ns.k, sm.scr);
     *b1 = (unsigned)sm.scr[0];
     *krem = sm.scr[1];
-    __syncthreads();  // every thread holds b1, krem before scr is reused
+    Grp::sync();  // every thread holds b1, krem before scr is reused
 }
 
 // Finish the selection of every row from the bitmaps and candidate lists of
 // the distributed pass (neuron_pass) and write idx_n, u_n, n_u_n; leave the
 // histogram and candidate counts zero.  One whole CTA; smem as FinalSmem.
+template <class Grp = CtaGroup>
 DV_DEV void neuron_final(const NeuronSel &ns, const FinalSmem &sm)
 {
-    const int tid = threadIdx.x, nt = blockDim.x;
+    const int tid = threadIdx.x, nt = Grp::size();
     const int W = (ns.N + 31) >> 5;
     for (int i = tid; i < W; i += nt)
         sm.ubits[i] = 0u;
@@ -377,23 +385,23 @@ DV_DEV void neuron_final(const NeuronSel &ns, const FinalSmem &sm)
             sm.rowbits[i] = __ldcg(gbits + i);
         unsigned b1;
         int krem;
-        neuron_row_bin(ns, b, sm, &b1, &krem);
+        neuron_row_bin<Grp>(ns, b, sm, &b1, &krem);
         const int ncand = __ldcg(ns.cand_cnt + b);
         if (ncand <= kTopkCand)
             for (int i = tid; i < ncand; i += nt) {
                 sm.ckey[i] = __ldcg(ns.cand_key + (size_t)b * kTopkCand + i);
                 sm.cidx[i] = __ldcg(ns.cand_idx + (size_t)b * kTopkCand + i);
             }
-        neuron_row_finish(ns, b, b1, krem, ncand, sm);
+        neuron_row_finish<Grp>(ns, b, b1, krem, ncand, sm);
         // leave this row's shared state zero for the next call
         int *ghist = ns.hist + (size_t)b * kTopkBins;
         for (int i = tid; i < kTopkBins; i += nt)
             ghist[i] = 0;
         if (tid == 0)
             ns.cand_cnt[b] = 0;
-        __syncthreads();
+        Grp::sync();
     }
-    neuron_union_out(ns, sm);
+    neuron_union_out<Grp>(ns, sm);
 }
 
 // The whole neuron selection in one CTA: for every row, the bin of the k-th

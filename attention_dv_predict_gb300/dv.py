@@ -63,6 +63,7 @@ _SIGS = {
     "dv_check": ([_P, _SZ, _P], _I),
     "dv_layer_decode_launches": ([_D, _I], _I),
     "dv_layer_decode_persistent_ok": ([_D, _I], _I),
+    "dv_layer_decode_plan": ([_D, _I, _I, _I, _I], _I),
     "dv_predict_topk": ([_D, _W, _P, _I, _I, _I, _S, _P, _P, _P, _SZ, _P], _I),
     "dv_predict_topk_noalloc": ([_D, _W, _P, _I, _I, _I, _S, _P, _P, _P], _I),
     "dv_sparse_attn": ([_D, _W, _P, _I, _P, _P, _I, _P, _P, _I, _P, _P, _SZ, _P], _I),
@@ -70,12 +71,15 @@ _SIGS = {
     "dv_layer_decode": ([_D, _W, _P, _P, _I, _I, _I, _P, _P, _I, _S, _P, _P, _P, _SZ, _P], _I),
     "dv_layer_decode_persistent": ([_D, _W, _P, _P, _I, _I, _I, _P, _P, _I, _S, _P, _P, _P, _SZ,
                                     _P], _I),
+    "dv_layer_decode_chained": ([_D, _W, _P, _P, _I, _I, _I, _P, _P, _I, _S, _P, _P, _P, _SZ,
+                                 _P], _I),
     "dv_layer_decode_presel": ([_D, _W, _P, _I, _P, _P, _I, _P, _P, _I, _P, _P, _I, _P, _P, _P,
                                 _SZ, _P], _I),
     "dv_layer_decode_traced": ([_D, _W, _P, _P, _I, _I, _I, _P, _P, _I, _S, _P, _P, _P, _SZ,
                                 C.POINTER(_P), _I, _P], _I),
     "dv_layer_decode_host": ([_D, _W, _P, _P, _I, _I, _I, _P, _P, _I, _S, _P, _P, _SZ, _P], _I),
     "dv_hbm_copy": ([_P, _P, _SZ, _P], _I),
+    "dv_test_hold_wait": ([_P, _SZ, _I, _I, _P], _I),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -207,6 +211,13 @@ def dv_layer_decode_persistent_ok(desc: LayerDesc, batch: int) -> bool:
     return bool(_lib.dv_layer_decode_persistent_ok(C.byref(desc), int(batch)))
 
 
+def dv_layer_decode_plan(desc: LayerDesc, batch: int, k_heads: int, k_neurons: int,
+                         kv_len: int) -> int:
+    """Kernel launches of one dv_layer_decode call (1: the streaming kernel)."""
+    return int(_lib.dv_layer_decode_plan(C.byref(desc), int(batch), int(k_heads), int(k_neurons),
+                                         int(kv_len)))
+
+
 def dv_predict_topk(layer: Layer, x_pred: torch.Tensor, k_heads: int, k_neurons: int,
                     sel: SelectionBuffers, ws: Workspace, scores_h: Optional[torch.Tensor] = None,
                     scores_n: Optional[torch.Tensor] = None, stream=None):
@@ -256,12 +267,25 @@ def dv_layer_decode(layer: Layer, x: torch.Tensor, k_heads: int, k_neurons: int,
         ws.nbytes, _stream(stream)))
 
 
+def dv_layer_decode_chained(layer: Layer, x: torch.Tensor, k_heads: int, k_neurons: int,
+                            k_cache: torch.Tensor, v_cache: torch.Tensor, kv_len: int,
+                            sel: SelectionBuffers, y: torch.Tensor, ws: Workspace,
+                            x_pred: Optional[torch.Tensor] = None,
+                            h1: Optional[torch.Tensor] = None, stream=None):
+    """dv_layer_decode as the seven chained kernels (every shape and batch)."""
+    B = x.shape[0]
+    _check("dv_layer_decode_chained", _lib.dv_layer_decode_chained(
+        C.byref(layer.desc), C.byref(layer.c), _ptr(x), _ptr(x_pred), B, k_heads, k_neurons,
+        _ptr(k_cache), _ptr(v_cache), kv_len, C.byref(sel.c), _ptr(h1), _ptr(y), ws.cptr,
+        ws.nbytes, _stream(stream)))
+
+
 def dv_layer_decode_persistent(layer: Layer, x: torch.Tensor, k_heads: int, k_neurons: int,
                                k_cache: torch.Tensor, v_cache: torch.Tensor, kv_len: int,
                                sel: SelectionBuffers, y: torch.Tensor, ws: Workspace,
                                x_pred: Optional[torch.Tensor] = None,
                                h1: Optional[torch.Tensor] = None, stream=None):
-    """dv_layer_decode as one persistent kernel (see dv_layer_decode_persistent_ok)."""
+    """dv_layer_decode through the streaming kernel only (see dv_layer_decode_persistent_ok)."""
     B = x.shape[0]
     _check("dv_layer_decode_persistent", _lib.dv_layer_decode_persistent(
         C.byref(layer.desc), C.byref(layer.c), _ptr(x), _ptr(x_pred), B, k_heads, k_neurons,
@@ -314,6 +338,12 @@ def dv_layer_decode_host(layer: Layer, x_host: torch.Tensor, k_heads: int, k_neu
         k_neurons, _ptr(k_cache), _ptr(v_cache), kv_len,
         C.byref(sel.c) if sel is not None else None, _ptr(y_host), ws.cptr, ws.nbytes,
         _stream(stream)))
+
+
+def dv_test_hold_wait(ws: Workspace, wait_id: int, budget_us: int, stream=None):
+    """Test support: make the next streaming decode's wait `wait_id` run out."""
+    _check("dv_test_hold_wait", _lib.dv_test_hold_wait(ws.cptr, ws.nbytes, int(wait_id),
+                                                        int(budget_us), _stream(stream)))
 
 
 def dv_hbm_copy(dst: torch.Tensor, src: torch.Tensor, nbytes: Optional[int] = None, stream=None):

@@ -129,11 +129,19 @@ int dv_workspace_init(void *ws, size_t ws_bytes, void *stream);
  * it.  Returns DV_OK if nothing was recorded. */
 int dv_check(void *ws, size_t ws_bytes, void *stream);
 
-/* Kernel launches one dv_layer_decode enqueues (for launch accounting). */
+/* Kernel launches of the chained decode (dv_layer_decode_chained, and the
+ * events dv_layer_decode_traced records around them). */
 int dv_layer_decode_launches(const dv_layer_desc *desc, int batch);
 
-/* 1 if dv_layer_decode_persistent serves this shape and batch on the current
- * device, else 0. */
+/* Kernel launches one dv_layer_decode call with these arguments enqueues on
+ * the current device: 1 where the streaming kernel serves it, else the
+ * chained decode's count.  0 for invalid arguments. */
+int dv_layer_decode_plan(const dv_layer_desc *desc, int batch, int k_heads, int k_neurons,
+                         int kv_len);
+
+/* 1 if dv_layer_decode_persistent (the streaming kernel) serves this shape
+ * and batch on the current device for every k_heads, k_neurons and kv_len,
+ * else 0. */
 int dv_layer_decode_persistent_ok(const dv_layer_desc *desc, int batch);
 
 /*
@@ -196,8 +204,14 @@ int dv_sparse_mlp(const dv_layer_desc *desc, const dv_layer_weights *w, const fl
  * k_heads, k_neurons).)
  *   h1: optional device output [B, d] of the attention block's result
  *       (NULL keeps it in the workspace).
- * Seven kernels (the predictors, QKV, attention, out-projection, fc1, fc2),
- * chained by programmatic dependent launch.
+ * Binary16 layers with 128-wide heads at batches 1 and 2 run as ONE
+ * persistent streaming kernel (dv_layer_decode_plan() == 1): a producer warp
+ * per SM streams every selected weight row into a shared-memory ring with
+ * bulk copies while the other warps compute, and the steps hand over
+ * through counters in the workspace (bounded waits; DV_ERR_TIMEOUT in the
+ * status word if one ran out).  Every other call runs the chained decode
+ * (dv_layer_decode_chained).  Both give the same selections; the streaming
+ * kernel sums in a different order, so outputs agree to rounding.
  */
 int dv_layer_decode(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x,
                     const float *x_pred, int batch, int k_heads, int k_neurons, void *k_cache,
@@ -205,15 +219,22 @@ int dv_layer_decode(const dv_layer_desc *desc, const dv_layer_weights *w, const 
                     void *ws, size_t ws_bytes, void *stream);
 
 /*
- * dv_layer_decode_persistent -- dv_layer_decode as one persistent
- * cooperative kernel: one CTA per SM runs the seven steps as phases ordered
- * by counters in the workspace instead of kernel boundaries (every wait
- * bounded: DV_ERR_TIMEOUT in the status word if one ran out).  Serves
- * binary16 layers with head_dim 128 at batch 1 or 2 where one CTA per SM
- * fits (dv_layer_decode_persistent_ok); DV_ERR_UNSUPPORTED otherwise,
- * launching nothing.  Arguments as dv_layer_decode.  The selections and the
- * KV append are identical to dv_layer_decode's; out-projection partial sums
- * are grouped over one CTA fewer, so y agrees to rounding, not bitwise.
+ * dv_layer_decode_chained -- dv_layer_decode as seven kernels (the
+ * predictors, QKV, attention, out-projection, fc1, fc2) chained by
+ * programmatic dependent launch (plain stream order for binary16 layers from
+ * 3 batch rows, where QKV, fc1, out-projection and fc2 use tensor cores).
+ * Serves every shape and batch.  Arguments as dv_layer_decode.
+ */
+int dv_layer_decode_chained(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x,
+                            const float *x_pred, int batch, int k_heads, int k_neurons,
+                            void *k_cache, void *v_cache, int kv_len, const dv_selection *sel,
+                            float *h1, float *y, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * dv_layer_decode_persistent -- dv_layer_decode through the streaming
+ * kernel only: DV_ERR_UNSUPPORTED, launching nothing, where it does not
+ * serve (see dv_layer_decode_persistent_ok / dv_layer_decode_plan).
+ * Arguments as dv_layer_decode.
  */
 int dv_layer_decode_persistent(const dv_layer_desc *desc, const dv_layer_weights *w,
                                const float *x, const float *x_pred, int batch, int k_heads,
@@ -263,6 +284,23 @@ int dv_layer_decode_host(const dv_layer_desc *desc, const dv_layer_weights *w, c
                          float *y_host, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * dv_test_hold_wait -- TEST SUPPORT for the bounded waits of the streaming
+ * kernel.  Arms the workspace so that the next streaming decode on it (see
+ * dv_layer_decode_plan) gives every device-side wait a budget of `budget_us`
+ * microseconds (> 0) and makes its wait number `wait_id` never complete:
+ *   1 first predictor stage done      4 QKV done (attention starts)
+ *   2 neuron scores done              5 attention done (out-projection)
+ *   3 neuron selection pass done      6 out-projection partials of a group
+ *   7 h1 and its norm statistics      8 fc1 done    9 fc2 partials of a group
+ * That wait runs out: the kernel records DV_ERR_TIMEOUT in the status word
+ * (dv_check), skips the rest of its work (outputs undefined), still returns,
+ * and disarms the workspace and leaves it ready for the next call.
+ * wait_id 0 disarms.  Enqueued on `stream` (a host-to-device copy of two
+ * words into the workspace's control block).
+ */
+int dv_test_hold_wait(void *ws, size_t ws_bytes, int wait_id, int budget_us, void *stream);
+
+/*
  * dv_hbm_copy -- copy `bytes` (a multiple of 16; both pointers 16-byte
  * aligned) from src to dst with a 16-byte-vector streaming kernel.  Used to
  * measure the copy bandwidth that serves as the roofline denominator.
@@ -288,16 +326,22 @@ int dv_hbm_copy(void *dst, const void *src, size_t bytes, void *stream);
  * nothing is launched; at the OPT-175B shape (N = 49152, r = 1000) the limit
  * is reached above batch 16.
  * Set-up: the first call on a device, with that device current, looks up the
- * scratch's device address (which may load the library's device code); make
- * that first call before any stream capture begins.
+ * scratch's device address (which may load the library's device code); the
+ * address is kept per device and looked up again only when the device's CUDA
+ * context has changed (for instance after cudaDeviceReset).  Make the first
+ * call on a device before any stream capture begins.
  * Zeroing: every call first zeroes, on `stream`, the part of the scratch
  * that the kernels require to start at zero (status word, first-digit
  * histograms, candidate counters, row counters); everything else is written
  * before it is read.
  * Concurrency: calls whose execution overlaps on one device (different
  * streams, or different host threads) share the scratch and race; the
- * results are then wrong.  Serialise them.  Device-side faults recorded in
- * the scratch status word are not reported.
+ * results are then wrong.  Serialise them.
+ * Device-side status: none of the kernels this entry point runs records a
+ * fault -- the predictor kernels read only whole weight rows inside their
+ * matrices and the selection kernels take no caller indices -- so there is no
+ * status word to read back (the workspace entries' dv_check has nothing to
+ * report for this path either).
  */
 #define DV_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 

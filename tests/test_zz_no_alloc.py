@@ -6,6 +6,7 @@ shared scratch ready for the next one.  Kept in its own file, collected last.
 """
 import os
 import sys
+from fractions import Fraction
 
 import pytest
 import torch
@@ -69,16 +70,38 @@ def test_noalloc_matches_workspace_entry(dv, name, B):
         assert got["u_n"].numel() >= cfg.k_neurons and got["u_h"].numel() >= cfg.k_heads
 
 
+# A narrow layer with a very wide MLP (binary32, d = 16, r = 8, N = 2^19):
+# the neuron predictor's scores, row counters and bitmaps grow with N and the
+# batch, so at batch 2 the scratch needs about 8.3 MiB (more than the fixed
+# 8 MiB) while batch 1 needs about 4.2 MiB.  Every buffer is sized for this
+# descriptor, so nothing depends on the refusal happening before a launch.
+WIDE = dv_inputs.LayerConfig("wide_ffn", 16, 2, 8, 1 << 19, 8, 4, 1, "f32", Fraction(1, 100),
+                             k_heads_fixed=1)
+
+
 def test_noalloc_rejects_shapes_beyond_its_scratch(dv):
-    # the 175B shape at batch 32 needs more than the fixed scratch
-    cfg = dv_inputs.CONFIGS["opt175b"].with_(batch=32)
-    desc = dv.desc_from_config(cfg)
-    small = dv_inputs.CONFIGS["tiny"]
-    layer_w = dv_inputs.make_weights(small, seed=0, device="cuda")
-    x = torch.zeros((32, cfg.d_model), device="cuda")
-    sel = dv.SelectionBuffers(desc, 32, cfg.k_heads, cfg.k_neurons)
+    dev = torch.device("cuda", 0)
+    desc = dv.desc_from_config(WIDE)
+    layer = dv.Layer(desc, dv_inputs.make_weights(WIDE, seed=3, device=dev))
+    k_h, k_n = WIDE.k_heads, WIDE.k_neurons
+
+    # batch 2: refused, nothing launched, the buffers untouched
+    x2 = dv_inputs.make_x(WIDE, 2, seed=4, device=dev)
+    sel2 = dv.SelectionBuffers(desc, 2, k_h, k_n)
+    sel2.n_u_n.fill_(-7)
     with pytest.raises(dv.DvError) as e:
-        # weight pointers are only checked for alignment before the size check
-        dv.dv_predict_topk_noalloc(dv.Layer(desc, layer_w), x, cfg.k_heads,
-                                   cfg.k_neurons, sel)
+        dv.dv_predict_topk_noalloc(layer, x2, k_h, k_n, sel2)
     assert e.value.status == dv.DV_ERR_SCRATCH_LIMIT
+    torch.cuda.synchronize()
+    assert int(sel2.n_u_n.item()) == -7
+
+    # batch 1 of the same layer fits and equals the workspace entry
+    x1 = x2[:1].contiguous()
+    ws = dv.Workspace(desc, 1)
+    ref = dv.SelectionBuffers(desc, 1, k_h, k_n)
+    dv.dv_predict_topk(layer, x1, k_h, k_n, ref, ws)
+    sel1 = dv.SelectionBuffers(desc, 1, k_h, k_n)
+    dv.dv_predict_topk_noalloc(layer, x1, k_h, k_n, sel1)
+    torch.cuda.synchronize()
+    assert torch.equal(sel1.idx_n, ref.idx_n) and torch.equal(sel1.idx_h, ref.idx_h)
+    assert torch.equal(sel1.unions()[1], ref.unions()[1])

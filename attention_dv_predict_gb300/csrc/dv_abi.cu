@@ -95,6 +95,14 @@ struct Launch {
     void *const *events;  // optional trace events
     int n_events;
     int next_event;
+    unsigned long long *stamps;  // optional chain timeline [kernels][nsm][kChainStamps]
+    int next_kernel;
+
+    // the timeline slots of the next kernel (NULL when not stamping)
+    unsigned long long *kernel_stamps()
+    {
+        return stamps ? stamps + (size_t)(next_kernel++) * nsm * kChainStamps : nullptr;
+    }
 
     dv_status mark()
     {
@@ -124,6 +132,8 @@ dv_status make_launch(void *stream, void *const *events, int n_events, Launch *L
     L->events = events;
     L->n_events = n_events;
     L->next_event = 0;
+    L->stamps = nullptr;
+    L->next_kernel = 0;
     return DV_OK;
 }
 
@@ -186,12 +196,9 @@ size_t set_mma(RowArgs &a, const dv_layer_desc &D, void *ws, const WsLayout &L)
 // cross-stream event wait before the call is not covered by PRED1's grid
 // wait (a lookahead predictor on a second stream then overwrote a selection
 // still in use), and the gain measured was within noise.
-// plan != nullptr: fill the persistent layer kernel's arguments instead of
-// launching (here and in run_attn / run_mlp).
 dv_status run_scores(const dv_layer_desc &D, const dv_layer_weights &w, const float *xp, int B,
                      float *sh_user, float *sn_user, void *ws, const WsLayout &L, Launch &lc,
-                     const PredSide *side = nullptr, bool pdl_first = false,
-                     LayerArgs *plan = nullptr)
+                     const PredSide *side = nullptr, bool pdl_first = false)
 {
     const int d = D.d_model, H = D.n_heads, N = D.d_ffn, r = D.pred_rank;
     int *ctl = at<int>(ws, L.ctl);
@@ -214,15 +221,14 @@ dv_status run_scores(const dv_layer_desc &D, const dv_layer_weights &w, const fl
     a.part = at<float>(ws, L.part_pred1);
     a.rowcnt = at<int>(ws, L.cnt_pred1);
     a.status = ctl;
+    a.stamps = lc.kernel_stamps();
     if (side)
         a.side_flag = ctl + kSideFlagWord;
     dim3 grid(lc.nsm, ceil_div(B, nb));
     dv_status s = lc.mark();
     if (s)
         return s;
-    if (plan)
-        plan->pred1 = a;
-    else if (launch_rowdot(RK_PRED1, D.dtype, nb, a, grid, rowdot_smem(RK_PRED1, nb, d), lc.st,
+    if (launch_rowdot(RK_PRED1, D.dtype, nb, a, grid, rowdot_smem(RK_PRED1, nb, d), lc.st,
                            lc.pdl && pdl_first) != cudaSuccess)
         return DV_ERR_CUDA;
 
@@ -242,6 +248,7 @@ dv_status run_scores(const dv_layer_desc &D, const dv_layer_weights &w, const fl
     b2.part = at<float>(ws, L.part_pred1);
     b2.rowcnt = at<int>(ws, L.cnt_pred1);
     b2.status = ctl;
+    b2.stamps = lc.kernel_stamps();
     if (side) {
         b2.side_cta = 1;
         b2.side = *side;
@@ -250,9 +257,7 @@ dv_status run_scores(const dv_layer_desc &D, const dv_layer_weights &w, const fl
     grid = dim3(lc.nsm, ceil_div(B, nb));
     if ((s = lc.mark()))
         return s;
-    if (plan)
-        plan->pred2 = b2;
-    else if (launch_rowdot(RK_PRED2, D.dtype, nb, b2, grid, rowdot_smem(RK_PRED2, nb, r), lc.st,
+    if (launch_rowdot(RK_PRED2, D.dtype, nb, b2, grid, rowdot_smem(RK_PRED2, nb, r), lc.st,
                            lc.pdl) != cudaSuccess)
         return DV_ERR_CUDA;
     return DV_OK;
@@ -265,7 +270,7 @@ dv_status run_scores(const dv_layer_desc &D, const dv_layer_weights &w, const fl
 dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const float *x, int B,
                    const int32_t *u_h, const int32_t *n_u_h, int max_u_h, void *kc, void *vc,
                    int kv_len, float *h1, void *ws, const WsLayout &L, Launch &lc, bool first,
-                   const NeuronSel *ns, LayerArgs *plan = nullptr)
+                   const NeuronSel *ns)
 {
     const int d = D.d_model, H = D.n_heads, dh = D.head_dim;
     int *ctl = at<int>(ws, L.ctl);
@@ -300,6 +305,7 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     a.part = at<float>(ws, L.part_qkv);
     a.rowcnt = at<int>(ws, L.cnt_qkv);
     a.status = ctl;
+    a.stamps = lc.kernel_stamps();
     size_t smem = rowdot_smem(RK_QKV, nb, d);
     if (ns) {
         // heads and norm(x) come from the stage-2 predictor kernel's side CTA;
@@ -318,9 +324,7 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     dv_status s = lc.mark();
     if (s)
         return s;
-    if (plan) {
-        plan->qkv = a;
-    } else if (use_mma(D, B)) {
+    if (use_mma(D, B)) {
         size_t sm = set_mma(a, D, ws, L);
         if (ns && select_final_smem(D.d_ffn) > sm)
             sm = select_final_smem(D.d_ffn);
@@ -347,9 +351,8 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     t.kc = kc;
     t.vc = vc;
     const int L1 = kv_len + 1;
-    // chunks per (batch row, head): enough CTAs to cover the SMs once (in
-    // the persistent kernel attention runs on all CTAs but the last)
-    int chunks = (plan ? lc.nsm - 1 : lc.nsm) / (B * max_u_h);
+    // chunks per (batch row, head): enough CTAs to cover the SMs once
+    int chunks = lc.nsm / (B * max_u_h);
     if (chunks < 1)
         chunks = 1;
     if (chunks > L1)
@@ -359,14 +362,13 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     t.splits = chunks;
     t.part = at<float>(ws, L.attn_part);
     t.status = ctl;
+    t.stamps = lc.kernel_stamps();
     if (ns)
         t.side_flag = ctl + kSideFlagWord;
     const int lpk = (int)((size_t)dh * esize(D.dtype) / 16);
     if ((s = lc.mark()))
         return s;
-    if (plan)
-        plan->attn = t;
-    else if (launch_attn(D.dtype, lpk, t, dim3(lc.nsm), lc.st, lc.pdl) != cudaSuccess)
+    if (launch_attn(D.dtype, lpk, t, dim3(lc.nsm), lc.st, lc.pdl) != cudaSuccess)
         return DV_ERR_CUDA;
 
     ColArgs c;
@@ -387,12 +389,11 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     c.part = at<float>(ws, L.cpart_o);
     c.cnt = at<int>(ws, L.ccnt_o);
     c.status = ctl;
+    c.stamps = lc.kernel_stamps();
     nb = colacc_nb(B);
     if ((s = lc.mark()))
         return s;
-    if (plan) {
-        plan->oproj = c;
-    } else if (use_mma(D, B)) {
+    if (use_mma(D, B)) {
         const int nt = colacc_mma_tiles(B);
         if (launch_colacc_mma(CK_OPROJ, nt, c, dim3(lc.nsm, ceil_div(B, 8 * nt)), lc.st, lc.pdl) !=
             cudaSuccess)
@@ -406,7 +407,7 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
 
 dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float *h1, int B,
                   const int32_t *u_n, const int32_t *n_u_n, int max_u_n, float *y, void *ws,
-                  const WsLayout &L, Launch &lc, bool first, LayerArgs *plan = nullptr)
+                  const WsLayout &L, Launch &lc, bool first)
 {
     const int d = D.d_model, N = D.d_ffn;
     int *ctl = at<int>(ws, L.ctl);
@@ -434,12 +435,11 @@ dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float
     a.part = at<float>(ws, L.part_fc1);
     a.rowcnt = at<int>(ws, L.cnt_fc1);
     a.status = ctl;
+    a.stamps = lc.kernel_stamps();
     dv_status s = lc.mark();
     if (s)
         return s;
-    if (plan) {
-        plan->fc1 = a;
-    } else if (use_mma(D, B)) {
+    if (use_mma(D, B)) {
         const size_t sm = set_mma(a, D, ws, L);
         if (launch_rowdot_mma(RK_FC1, a, dim3(lc.nsm, ceil_div(B, 8)), sm, lc.st,
                               lc.pdl && !first) !=
@@ -468,12 +468,11 @@ dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float
     c.part = at<float>(ws, L.cpart_2);
     c.cnt = at<int>(ws, L.ccnt_2);
     c.status = ctl;
+    c.stamps = lc.kernel_stamps();
     nb = colacc_nb(B);
     if ((s = lc.mark()))
         return s;
-    if (plan) {
-        plan->fc2 = c;
-    } else if (use_mma(D, B)) {
+    if (use_mma(D, B)) {
         const int nt = colacc_mma_tiles(B);
         if (launch_colacc_mma(CK_FC2, nt, c, dim3(lc.nsm, ceil_div(B, 8 * nt)), lc.st, lc.pdl) !=
             cudaSuccess)
@@ -499,63 +498,9 @@ bool sel_ok(const dv_selection *sel)
     return sel && sel->idx_h && sel->idx_n && sel->u_h && sel->n_u_h && sel->u_n && sel->n_u_n;
 }
 
-// The persistent layer kernel serves binary16 layers with 128-wide heads at
-// batches of 1 and 2, where every step takes the whole batch as one tile on
-// CUDA cores.  Returns that tile (0: not eligible) and the kernel's dynamic
-// shared memory (the largest of its phases').
-int persistent_plan(const dv_layer_desc &D, int B, int nsm, size_t *smem)
-{
-    if (D.dtype != DV_F16 || D.head_dim != 128 || B > 2 || use_mma(D, B) || nsm < 2)
-        return 0;
-    const int nb = B;
-    if (rowdot_nb(B, D.d_model, RK_PRED1) != nb || rowdot_nb(B, D.pred_rank, RK_PRED2) != nb ||
-        rowdot_nb(B, D.d_model, RK_QKV) != nb || rowdot_nb(B, D.d_model, RK_FC1) != nb ||
-        colacc_nb(B) != nb)
-        return 0;
-    size_t sm = rowdot_smem(RK_PRED1, nb, D.d_model);
-    const size_t parts[] = {rowdot_smem(RK_PRED2, nb, D.pred_rank),
-                            rowdot_smem(RK_QKV, nb, D.d_model), select_final_smem(D.d_ffn),
-                            rowdot_smem(RK_FC1, nb, D.d_model),
-                            colacc_smem_bytes(colacc_block_cols(D.dtype, nb), nb),
-                            attn_smem_bytes(D.head_dim)};
-    for (size_t p : parts)
-        if (p > sm)
-            sm = p;
-    if (sm > kSmemCap)
-        return 0;
-    // one CTA per SM must fit; the answer is kept per device, tile and size
-    struct Fit {
-        int dev, nb;
-        size_t smem;
-        int ctas;
-    };
-    static std::mutex mu;
-    static Fit known[16];
-    static int n_known = 0;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
-        return 0;
-    int ctas = -1;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        for (int i = 0; i < n_known; ++i)
-            if (known[i].dev == dev && known[i].nb == nb && known[i].smem == sm)
-                ctas = known[i].ctas;
-        if (ctas < 0) {
-            ctas = layer_ctas_per_sm(nb, sm);
-            if (n_known < 16)
-                known[n_known++] = Fit{dev, nb, sm, ctas};
-        }
-    }
-    if (ctas < 1)
-        return 0;
-    *smem = sm;
-    return nb;
-}
-
 // The streaming kernel (dv_stream.cu) serves binary16 layers with 128-wide
 // heads at batches of 1 and 2 whose shapes fit its tiling: rows of at most
-// 4 x 512 chunks (d <= 16384), predictor rank <= 1024, a column-group split
+// 6 x 384 chunks (d <= 18432), predictor rank <= 1024, a column-group split
 // of the SMs, and one CTA per SM with the shared memory below.  Fills `a`
 // (all but the call's pointers) and returns true when it serves.
 bool stream_plan(const dv_layer_desc &D, int B, int k_h, int k_n, int kv_len, int G,
@@ -566,7 +511,7 @@ bool stream_plan(const dv_layer_desc &D, int B, int k_h, int k_n, int kv_len, in
         return false;
     const int d = D.d_model, cpr = d / 8;
     const int nseg = ceil_div(cpr, kStreamUnitBytes / 16);
-    if (d % 8 || nseg > 4 || D.pred_rank % 8 || D.pred_rank > 1024 || D.n_heads > 256)
+    if (d % 8 || nseg > 6 || D.pred_rank % 8 || D.pred_rank > 1024 || D.n_heads > 256)
         return false;
     int ncg = 0;
     for (int c : {8, 4, 2, 1})
@@ -582,7 +527,7 @@ bool stream_plan(const dv_layer_desc &D, int B, int k_h, int k_n, int kv_len, in
     C = std::max(1, std::min(C, std::min(kMaxAttnChunks, kv_len + 1)));
     const size_t uni = stream_union_bytes(B, D.d_ffn, max_u_h, max_u_n, cg, gm);
     const size_t fixed = stream_smem_bytes((int)uni, 0);
-    if (fixed + 4 * (size_t)kStreamStageBytes > kStreamSmemMax)
+    if (fixed + 3 * (size_t)kStreamStageBytes > kStreamSmemMax)
         return false;
     const int nst = (int)std::min<size_t>(kStreamMaxStages,
                                           (kStreamSmemMax - fixed) / kStreamStageBytes);
@@ -646,7 +591,8 @@ bool stream_plan(const dv_layer_desc &D, int B, int k_h, int k_n, int kv_len, in
 dv_status stream_launch(const dv_layer_desc &D, const dv_layer_weights &w, const float *x,
                         const float *xp, int B, int k_h, int k_n, void *kc, void *vc, int kv_len,
                         const dv_selection &sel, float *h1, float *y, void *ws, const WsLayout &L,
-                        const Launch &lc, bool *served)
+                        const Launch &lc, bool *served, unsigned long long *stamps = nullptr,
+                        int n_stamps = 0)
 {
     StreamArgs a;
     int ni = 0;
@@ -655,6 +601,9 @@ dv_status stream_launch(const dv_layer_desc &D, const dv_layer_weights &w, const
     if (!stream_plan(D, B, k_h, k_n, kv_len, lc.nsm, &a, &ni, &smem))
         return DV_OK;
     *served = true;
+    if (stamps && n_stamps < lc.nsm * kStreamStamps)
+        return DV_ERR_INVALID_ARG;
+    a.stamps = stamps;
     a.x = x;
     a.x_pred = xp;
     a.ln1_g = w.ln1_g;
@@ -705,7 +654,7 @@ dv_status layer_decode_impl(const dv_layer_desc *desc, const dv_layer_weights *w
                             void *vc, int kv_len, const dv_selection *sel, float *h1, float *y,
                             void *ws, size_t ws_bytes, void *const *events, int n_events,
                             void *stream, bool pdl_first, bool persistent = false,
-                            bool chained = false)
+                            unsigned long long *stamps = nullptr, int n_stamps = 0)
 {
     dv_status s = check_desc(desc);
     if (s)
@@ -748,36 +697,19 @@ dv_status layer_decode_impl(const dv_layer_desc *desc, const dv_layer_weights *w
     side.norm_kind = D.norm;
     side.eps = D.ln_eps;
     side.xn = at<float>(ws, L.xn);
-    if (!events && !chained) {  // the streaming kernel where it serves
+    if (stamps && !persistent) {
+        if ((size_t)n_stamps < (size_t)kLayerLaunches * lc.nsm * kChainStamps)
+            return DV_ERR_INVALID_ARG;
+        lc.stamps = stamps;
+    }
+    if (persistent) {  // the streaming kernel, where it serves
         bool served = false;
-        s = stream_launch(D, *w, x, x_pred ? x_pred : x, batch, k_heads, k_neurons, kc, vc, kv_len,
-                          *sel, h1p, y, ws, L, lc, &served);
+        s = events ? DV_OK
+                   : stream_launch(D, *w, x, x_pred ? x_pred : x, batch, k_heads, k_neurons, kc,
+                                   vc, kv_len, *sel, h1p, y, ws, L, lc, &served, stamps, n_stamps);
         if (s)
             return s;
-        if (served)
-            return cuda_status(cudaGetLastError());
-        if (persistent)
-            return DV_ERR_UNSUPPORTED;
-    }
-    if (persistent) {  // one persistent kernel
-        size_t psmem = 0;
-        const int pnb = events ? 0 : persistent_plan(D, batch, lc.nsm, &psmem);
-        if (!pnb)
-            return DV_ERR_UNSUPPORTED;
-        LayerArgs plan;
-        std::memset(&plan, 0, sizeof(plan));
-        if ((s = run_scores(D, *w, x_pred ? x_pred : x, batch, nullptr, nullptr, ws, L, lc, &side,
-                            false, &plan)) ||
-            (s = run_attn(D, *w, x, batch, sel->u_h, sel->n_u_h, max_u_h, kc, vc, kv_len, h1p, ws,
-                          L, lc, false, &ns, &plan)) ||
-            (s = run_mlp(D, *w, h1p, batch, sel->u_n, sel->n_u_n, max_u_n, y, ws, L, lc, false,
-                         &plan)))
-            return s;
-        plan.bar = at<int>(ws, L.ctl) + kLayerBarWord;
-        plan.status = at<int>(ws, L.ctl);
-        if (launch_layer(pnb, plan, lc.nsm, psmem, lc.st) != cudaSuccess)
-            return DV_ERR_CUDA;
-        return cuda_status(cudaGetLastError());
+        return served ? cuda_status(cudaGetLastError()) : DV_ERR_UNSUPPORTED;
     }
     if ((s = run_scores(D, *w, x_pred ? x_pred : x, batch, nullptr, nullptr, ws, L, lc, &side,
                         pdl_first)))
@@ -945,24 +877,6 @@ int dv_layer_decode_persistent_ok(const dv_layer_desc *desc, int batch)
                        &ni, &sm);
 }
 
-int dv_layer_decode_plan(const dv_layer_desc *desc, int batch, int k_heads, int k_neurons,
-                         int kv_len)
-{
-    if (check_desc(desc) != DV_OK || batch < 1 || batch > DV_MAX_BATCH || k_heads < 1 ||
-        k_heads > desc->n_heads || k_neurons < 1 || k_neurons > desc->d_ffn || kv_len < 0 ||
-        kv_len >= desc->kv_cap)
-        return 0;
-    Launch lc;
-    StreamArgs a;
-    int ni = 0;
-    size_t sm = 0;
-    if (make_launch(nullptr, nullptr, 0, &lc) != DV_OK)
-        return 0;
-    return stream_plan(*desc, batch, k_heads, k_neurons, kv_len, lc.nsm, &a, &ni, &sm)
-               ? 1
-               : kLayerLaunches;
-}
-
 int dv_predict_topk(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x_pred,
                     int batch, int k_heads, int k_neurons, const dv_selection *sel,
                     float *scores_h, float *scores_n, void *ws, size_t ws_bytes, void *stream)
@@ -1099,8 +1013,20 @@ int dv_layer_decode_chained(const dv_layer_desc *desc, const dv_layer_weights *w
                             float *h1, float *y, void *ws, size_t ws_bytes, void *stream)
 {
     return layer_decode_impl(desc, w, x, x_pred, batch, k_heads, k_neurons, k_cache, v_cache,
-                             kv_len, sel, h1, y, ws, ws_bytes, nullptr, 0, stream, false, false,
-                             true);
+                             kv_len, sel, h1, y, ws, ws_bytes, nullptr, 0, stream, false);
+}
+
+int dv_layer_decode_stamped(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x,
+                            const float *x_pred, int batch, int k_heads, int k_neurons,
+                            void *k_cache, void *v_cache, int kv_len, const dv_selection *sel,
+                            float *h1, float *y, void *ws, size_t ws_bytes, int persistent,
+                            unsigned long long *stamps, int n_stamps, void *stream)
+{
+    if (!stamps || (reinterpret_cast<uintptr_t>(stamps) & 7u) || n_stamps < 0)
+        return DV_ERR_INVALID_ARG;
+    return layer_decode_impl(desc, w, x, x_pred, batch, k_heads, k_neurons, k_cache, v_cache,
+                             kv_len, sel, h1, y, ws, ws_bytes, nullptr, 0, stream, false,
+                             persistent != 0, stamps, n_stamps);
 }
 
 int dv_layer_decode_persistent(const dv_layer_desc *desc, const dv_layer_weights *w,

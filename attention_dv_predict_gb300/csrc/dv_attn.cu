@@ -9,7 +9,9 @@ namespace {
 template <typename T, int LPK>
 __global__ void __launch_bounds__(kThreads) k_attn(const AttnArgs a)
 {
-    attn_body<T, LPK>(a, blockIdx.x, gridDim.x, PdlDep{});
+    unsigned long long *s = chain_stamps(a.stamps);
+    attn_body<T, LPK>(a, blockIdx.x, gridDim.x, PdlDep{s});
+    chain_stamp_end(s);
 }
 
 template <typename T, int LPK>

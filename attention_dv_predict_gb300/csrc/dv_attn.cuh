@@ -1,6 +1,5 @@
 // dv_attn.cuh -- decode attention over the selected heads' KV cache (sm_103a):
-// the body shared by its stand-alone kernel (dv_attn.cu) and the persistent
-// layer kernel (dv_layer.cu).
+// the body of its stand-alone kernel (dv_attn.cu).
 //
 // For every batch row b and selected head h ("DejaVu Guide: Contextual
 // Sparsity for LLM Inference", "2. Head-Pruned Attention Dispatch": only the

@@ -8,7 +8,9 @@ namespace {
 template <typename T, int NB, int KIND, int P>
 __global__ void __launch_bounds__(kThreads, 1) k_colacc(const ColArgs a)
 {
-    colacc_body<T, NB, KIND, P>(a, blockIdx.x, gridDim.x, PdlDep{});
+    unsigned long long *s = chain_stamps(a.stamps);
+    colacc_body<T, NB, KIND, P>(a, blockIdx.x, gridDim.x, PdlDep{s});
+    chain_stamp_end(s);
 }
 
 template <typename T, int NB, int KIND>

@@ -1,6 +1,5 @@
 // dv_colacc.cuh -- column-gather GEMV of the sparse layer decode (sm_103a): the
-// body shared by its stand-alone kernels (dv_colacc.cu) and the persistent
-// layer kernel (dv_layer.cu).
+// body of its stand-alone kernels (dv_colacc.cu).
 //
 //   OPROJ  h1[b] = x[b] + b_o + sum over selected heads h and e < dh of
 //          o[b][h][e] * w_oT[h][e][:]       ("DejaVu Guide: Contextual Sparsity

@@ -130,10 +130,10 @@ struct CtaGroup {
     DV_DEV static int size() { return blockDim.x; }
     DV_DEV static void sync() { __syncthreads(); }
 };
-constexpr int kConsumers = 512;
+constexpr int kConsumers = 384;
 struct ConsumerGroup {
     DV_DEV static int size() { return kConsumers; }
-    DV_DEV static void sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+    DV_DEV static void sync() { asm volatile("bar.sync 1, 384;" ::: "memory"); }
 };
 
 // Exclusive prefix sum over the group (a multiple of 32 threads, <= 1024).
@@ -224,19 +224,18 @@ DV_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_depend
 // dependent of the kernel before it.  wait() is the grid dependency, after
 // which the body lets its own dependents launch; trigger() lets them launch
 // without waiting.
+// stamps (optional): this CTA's timeline slots; wait() stamps slot 1.
 struct PdlDep {
+    unsigned long long *stamps = nullptr;
     DV_DEV void wait() const
     {
         pdl_wait();
+        ready();
         pdl_launch_dependents();
     }
     DV_DEV void trigger() const { pdl_launch_dependents(); }
+    DV_DEV void ready() const;
 };
-
-// Polls of a phase counter (each ~64 ns of sleep plus an L2 round trip) and
-// the time after which a wait gives up.
-constexpr int kPhaseSpin = 1 << 20;
-constexpr unsigned long long kPhaseSpinNs = 50ull * 1000 * 1000;
 
 DV_DEV unsigned long long global_ns()
 {
@@ -245,53 +244,30 @@ DV_DEV unsigned long long global_ns()
     return t;
 }
 
-// Poll *c (acquire) until it reaches target; false if the bound ran out.
-DV_DEV bool poll_count(const int *c, int target)
+// Timeline slot i of a CTA (thread 0; nothing when stamps is NULL).
+DV_DEV void chain_stamp(unsigned long long *stamps, int i)
 {
-    const unsigned long long t0 = global_ns();
-    for (int it = 0; it < kPhaseSpin; ++it) {
-        if (ld_acquire_gpu(c) >= target)
-            return true;
-        if ((it & 63) == 63 && global_ns() - t0 > kPhaseSpinNs)
-            return false;
-        __nanosleep(64);
-    }
-    return ld_acquire_gpu(c) >= target;
+    if (stamps && threadIdx.x == 0)
+        stamps[i] = global_ns();
 }
 
-// PhaseDep: the body is one phase of the persistent layer kernel.  wait()
-// returns once up to two phase counters (CTAs that finished the producing
-// phases) reach their targets.  Thread 0 polls with acquire loads, then the
-// CTA barrier passes the ordering on; a wait that runs out records
-// DV_ERR_TIMEOUT and returns, so every CTA still runs to its end.
-struct PhaseDep {
-    const int *c0, *c1;  // NULL: unused
-    int t0, t1;
-    int *status;
-    DV_DEV void wait() const
-    {
-        if (threadIdx.x == 0) {
-            bool ok = true;
-            if (c0)
-                ok = poll_count(c0, t0) && ok;
-            if (c1)
-                ok = poll_count(c1, t1) && ok;
-            if (!ok)
-                set_status(status, DV_ERR_TIMEOUT);
-        }
-        __syncthreads();
-    }
-    DV_DEV void trigger() const {}
-};
+DV_DEV void PdlDep::ready() const { chain_stamp(stamps, 1); }
 
-// A CTA finished a phase: after the barrier, one release add counts it (the
-// release orders every write the CTA made before the barrier ahead of the
-// count; a reader's acquire poll plus barrier orders them before its reads).
-DV_DEV void phase_arrive(int *c)
+// A kernel wrapper's timeline: slot 0 on entry, slot 2 once every thread of
+// the CTA has left the body (the barrier only when stamping).
+DV_DEV unsigned long long *chain_stamps(unsigned long long *base)
 {
-    __syncthreads();
-    if (threadIdx.x == 0)
-        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(c) : "memory");
+    unsigned long long *s =
+        (base && blockIdx.y == 0) ? base + (size_t)blockIdx.x * kChainStamps : nullptr;
+    chain_stamp(s, 0);
+    return s;
+}
+DV_DEV void chain_stamp_end(unsigned long long *s)
+{
+    if (s) {
+        __syncthreads();
+        chain_stamp(s, 2);
+    }
 }
 
 }  // namespace dv

@@ -111,6 +111,12 @@ struct PredSide {
     float *xn;            // out: norm(x) [B][d]
 };
 
+// Timeline of the chained decode (profiling): kernel k of the call writes,
+// for each CTA c of its first batch tile, %globaltimer nanoseconds to
+// stamps[(k * CTAs + c) * kChainStamps + i]: i = 0 the CTA starts, 1 its
+// inputs are ready (the grid dependency or the side flag passed), 2 it ends.
+constexpr int kChainStamps = 4;
+
 // Polls of the side-work flag before the QKV kernel falls back to waiting
 // for the whole stage-2 predictor grid.
 constexpr int kSideSpin = 20000;
@@ -155,6 +161,7 @@ struct RowArgs {
     float *mma_part;
     int *mma_cnt;
     int *status;
+    unsigned long long *stamps;  // optional timeline [CTAs][4] (kChainStamps)
 };
 
 // Column-accumulate kernel: out[b][c] = res[b][c] + bias[c]
@@ -180,6 +187,7 @@ struct ColArgs {
     float *part;          // block partials [tiles][CTAs][2][NB][block columns]
     int *cnt;             // rows accounted per column block [tiles][blocks], zero at rest
     int *status;
+    unsigned long long *stamps;  // optional timeline [CTAs][4] (kChainStamps)
 };
 
 // 16-byte chunks per lane of the column kernel (columns per block = 32 * P *
@@ -210,30 +218,7 @@ struct AttnArgs {
     float *part;          // out: chunk records [B][max_sel][splits][kAttnRec + dh]
     const int *side_flag; // fused decode: set once the head union is published
     int *status;
-};
-
-// Persistent layer kernel (dv_layer.cu): the seven steps of the fused decode
-// as phases of one cooperative grid, one CTA per SM, ordered by counters of
-// the CTAs that finished each phase (workspace control words, zero at rest).
-enum LayerBar {
-    kBarPred1 = 0,  // CTAs done with PRED1 (all)
-    kBarPred2,      // ... PRED2 (all, the side CTA included)
-    kBarQkv,        // ... QKV rows (all but the last CTA)
-    kBarSel,        // the last CTA's neuron selection
-    kBarAttn,       // ... attention (all but the last)
-    kBarOproj,      // ... out-projection (all but the last)
-    kBarFc1,        // ... fc1 (all)
-    kBarExit,       // CTAs at the end; the last resets every counter
-    kBarCount
-};
-constexpr int kLayerBarWord = 8;  // first control word of the counters
-
-struct LayerArgs {
-    RowArgs pred1, pred2, qkv, fc1;
-    AttnArgs attn;
-    ColArgs oproj, fc2;
-    int *bar;      // kBarCount counters
-    int *status;
+    unsigned long long *stamps;  // optional timeline [CTAs][4] (kChainStamps)
 };
 
 // Dynamic shared memory of the attention kernel: the 16 warps' partial
@@ -280,11 +265,6 @@ cudaError_t launch_attn(int dtype, int lanes_per_key, const AttnArgs &a, dim3 gr
 cudaError_t launch_select(const SelectArgs &a, int grid, cudaStream_t st);
 size_t select_final_smem(int N);
 cudaError_t launch_copy(void *dst, const void *src, size_t n16, int grid, cudaStream_t st);
-// Persistent layer kernel (binary16 weights, head_dim 128, one batch tile of
-// nb in {1, 2} rows): cooperative launch of `grid` CTAs.
-cudaError_t launch_layer(int nb, const LayerArgs &a, int grid, size_t smem, cudaStream_t st);
-// CTAs of the persistent layer kernel one SM holds at this shared memory (0 on error).
-int layer_ctas_per_sm(int nb, size_t smem);
 
 // Largest-batch tile each kernel family handles per CTA.
 int rowdot_nb(int B, int K, int kind);
@@ -311,10 +291,11 @@ size_t colacc_mma_smem();
 // persistent cooperative grid whose producer warp streams every selected
 // weight byte into a shared-memory ring (bulk copies) while the consumer warps
 // compute; phases hand over through counters in the workspace control words.
-constexpr int kStreamStageBytes = 16384;  // one ring stage
+constexpr int kStreamStageBytes = 32768;  // one ring stage
 constexpr int kStreamMaxStages = 16;
-constexpr int kStreamThreads = 544;       // 16 consumer warps + the producer warp
-constexpr int kStreamUnitBytes = 8192;    // a row segment: 512 chunks of 16 bytes
+constexpr int kStreamThreads = 416;       // 12 consumer warps + the producer warp
+constexpr int kStreamUnitBytes = 6144;    // a row segment: 384 chunks of 16 bytes
+constexpr int kStreamStamps = 32;         // phase timeline points per CTA
 
 // Control words of the streaming kernel (int offsets into the workspace's
 // control block; all zero at rest).
@@ -351,7 +332,7 @@ struct StreamArgs {
     float *h1, *y;
     // geometry
     int G;       // CTAs (one per SM)
-    int nseg;    // 512-chunk segments of a d-long row
+    int nseg;    // 384-chunk segments of a d-long row
     int ncg;     // column groups of the out-projection and fc2
     int gm;      // CTAs per column group (G / ncg)
     int cg;      // columns of the widest group (groups split the row's 16-byte
@@ -372,6 +353,7 @@ struct StreamArgs {
     unsigned *rowbits, *cand_key;
     int *cand_idx, *cand_cnt;
     int *ctl;         // control block ([0] status)
+    unsigned long long *stamps;  // optional phase timeline [G][kStreamStamps] (globaltimer)
 };
 
 // The streaming kernel's column partials assume at most this many CTAs per
@@ -379,8 +361,8 @@ struct StreamArgs {
 constexpr int kStreamMaxGroupCtas = 32;
 constexpr int kStreamMaxCtas = 512;
 
-// Launch of the streaming kernel for a batch of nb (1 or 2) and ni 512-chunk
-// segments per row (1..4); cooperative, `grid` CTAs of kStreamThreads.
+// Launch of the streaming kernel for a batch of nb (1 or 2) and ni 384-chunk
+// segments per row (1..6); cooperative, `grid` CTAs of kStreamThreads.
 cudaError_t launch_stream(int nb, int ni, const StreamArgs &a, size_t smem, cudaStream_t st);
 // CTAs of the streaming kernel one SM holds at this shared memory (0 on error).
 int stream_ctas_per_sm(int nb, int ni, size_t smem);

@@ -9,7 +9,9 @@ namespace {
 template <typename T, int NB, int KIND, int U>
 __global__ void __launch_bounds__(kThreads, 1) k_rowdot(const RowArgs a)
 {
-    rowdot_body<T, NB, KIND, U>(a, blockIdx.x, gridDim.x, PdlDep{});
+    unsigned long long *s = chain_stamps(a.stamps);
+    rowdot_body<T, NB, KIND, U>(a, blockIdx.x, gridDim.x, PdlDep{s});
+    chain_stamp_end(s);
 }
 
 // ---------------------------------------------------------------------------

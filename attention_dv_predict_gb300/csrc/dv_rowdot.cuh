@@ -1,6 +1,6 @@
 // dv_rowdot.cuh -- the row-dot GEMV of the sparse layer decode (sm_103a):
 // the body shared by its stand-alone kernels (dv_rowdot.cu) and the
-// persistent layer kernel (dv_layer.cu).
+// fused steps that the streaming kernel (dv_stream.cu) restates.
 //
 // One body serves every step whose output element is the dot product of one
 // weight row with an activation vector:
@@ -421,10 +421,12 @@ DV_DEV void rowdot_body(const RowArgs &a, int cta, int nct, const Dep &dep)
                 s_ready = ok;
             }
             __syncthreads();
-            if (!s_ready)
+            if (!s_ready) {
                 dep.wait();
-            else
+            } else {
+                dep.ready();
                 dep.trigger();
+            }
         } else {  // the head union was given by the caller
             dep.wait();
         }

@@ -29,14 +29,17 @@ constexpr int kHeadKPL = kHeadTopkMax / 32;
 constexpr int kScanBatch = 8;    // 16-byte score loads per thread in flight in neuron_select_cta
 
 // Bitmap words (bits[q] for elements q*32 + lane) of the k largest of
-// s[0..n), ties to the lower index.  One warp; n <= kHeadTopkMax.
+// s[0..n), ties to the lower index.  One warp; n <= kHeadTopkMax.  The scores
+// are in global memory (written by other CTAs: read at L2) or, with kShared,
+// in this CTA's shared memory.
+template <bool kShared = false>
 DV_DEV void warp_topk_bits(const float *s, int n, int k, unsigned *bits, int lane)
 {
     unsigned key[kHeadKPL];
 #pragma unroll
     for (int q = 0; q < kHeadKPL; ++q) {
         const int i = q * 32 + lane;
-        key[q] = i < n ? score_key(ld_cg(s + i)) : 0u;
+        key[q] = i < n ? score_key(kShared ? s[i] : ld_cg(s + i)) : 0u;
     }
     unsigned T = 0u;
     for (int bit = 31; bit >= 0; --bit) {
@@ -86,6 +89,8 @@ DV_DEV int warp_compact_bits(const unsigned *bits, int W, int32_t *out, int lane
 // Head selection of all B rows by one warp.  The union goes to su[] (shared
 // memory, ascending) and its length is returned.  When `write` is set the
 // per-row lists, the union and its length are also written to global memory.
+// kShared: the scores s_h are in shared memory.
+template <bool kShared = false>
 DV_DEV int head_select(const float *s_h, int B, int H, int k, unsigned *sbits, int32_t *su,
                        bool write, int32_t *idx_h, int32_t *u_h, int32_t *n_u_h, int lane)
 {
@@ -95,7 +100,7 @@ DV_DEV int head_select(const float *s_h, int B, int H, int k, unsigned *sbits, i
         ubits[lane] = 0u;
     __syncwarp();
     for (int b = 0; b < B; ++b) {
-        warp_topk_bits(s_h + (size_t)b * H, H, k, rowbits, lane);
+        warp_topk_bits<kShared>(s_h + (size_t)b * H, H, k, rowbits, lane);
         if (lane < W)
             ubits[lane] |= rowbits[lane];
         __syncwarp();

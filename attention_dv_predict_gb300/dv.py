@@ -63,7 +63,6 @@ _SIGS = {
     "dv_check": ([_P, _SZ, _P], _I),
     "dv_layer_decode_launches": ([_D, _I], _I),
     "dv_layer_decode_persistent_ok": ([_D, _I], _I),
-    "dv_layer_decode_plan": ([_D, _I, _I, _I, _I], _I),
     "dv_predict_topk": ([_D, _W, _P, _I, _I, _I, _S, _P, _P, _P, _SZ, _P], _I),
     "dv_predict_topk_noalloc": ([_D, _W, _P, _I, _I, _I, _S, _P, _P, _P], _I),
     "dv_sparse_attn": ([_D, _W, _P, _I, _P, _P, _I, _P, _P, _I, _P, _P, _SZ, _P], _I),
@@ -73,6 +72,8 @@ _SIGS = {
                                     _P], _I),
     "dv_layer_decode_chained": ([_D, _W, _P, _P, _I, _I, _I, _P, _P, _I, _S, _P, _P, _P, _SZ,
                                  _P], _I),
+    "dv_layer_decode_stamped": ([_D, _W, _P, _P, _I, _I, _I, _P, _P, _I, _S, _P, _P, _P, _SZ,
+                                 _I, _P, _I, _P], _I),
     "dv_layer_decode_presel": ([_D, _W, _P, _I, _P, _P, _I, _P, _P, _I, _P, _P, _I, _P, _P, _P,
                                 _SZ, _P], _I),
     "dv_layer_decode_traced": ([_D, _W, _P, _P, _I, _I, _I, _P, _P, _I, _S, _P, _P, _P, _SZ,
@@ -211,13 +212,6 @@ def dv_layer_decode_persistent_ok(desc: LayerDesc, batch: int) -> bool:
     return bool(_lib.dv_layer_decode_persistent_ok(C.byref(desc), int(batch)))
 
 
-def dv_layer_decode_plan(desc: LayerDesc, batch: int, k_heads: int, k_neurons: int,
-                         kv_len: int) -> int:
-    """Kernel launches of one dv_layer_decode call (1: the streaming kernel)."""
-    return int(_lib.dv_layer_decode_plan(C.byref(desc), int(batch), int(k_heads), int(k_neurons),
-                                         int(kv_len)))
-
-
 def dv_predict_topk(layer: Layer, x_pred: torch.Tensor, k_heads: int, k_neurons: int,
                     sel: SelectionBuffers, ws: Workspace, scores_h: Optional[torch.Tensor] = None,
                     scores_n: Optional[torch.Tensor] = None, stream=None):
@@ -278,6 +272,21 @@ def dv_layer_decode_chained(layer: Layer, x: torch.Tensor, k_heads: int, k_neuro
         C.byref(layer.desc), C.byref(layer.c), _ptr(x), _ptr(x_pred), B, k_heads, k_neurons,
         _ptr(k_cache), _ptr(v_cache), kv_len, C.byref(sel.c), _ptr(h1), _ptr(y), ws.cptr,
         ws.nbytes, _stream(stream)))
+
+
+def dv_layer_decode_stamped(layer: Layer, x: torch.Tensor, k_heads: int, k_neurons: int,
+                            k_cache: torch.Tensor, v_cache: torch.Tensor, kv_len: int,
+                            sel: SelectionBuffers, y: torch.Tensor, ws: Workspace,
+                            stamps: torch.Tensor, x_pred: Optional[torch.Tensor] = None,
+                            h1: Optional[torch.Tensor] = None, persistent: bool = False,
+                            stream=None):
+    """The decode with its timeline in ``stamps`` (int64): [7, SMs, 4] for the
+    chain, [SMs, 32] for the persistent streaming kernel."""
+    B = x.shape[0]
+    _check("dv_layer_decode_stamped", _lib.dv_layer_decode_stamped(
+        C.byref(layer.desc), C.byref(layer.c), _ptr(x), _ptr(x_pred), B, k_heads, k_neurons,
+        _ptr(k_cache), _ptr(v_cache), kv_len, C.byref(sel.c), _ptr(h1), _ptr(y), ws.cptr,
+        ws.nbytes, int(bool(persistent)), _ptr(stamps), stamps.numel(), _stream(stream)))
 
 
 def dv_layer_decode_persistent(layer: Layer, x: torch.Tensor, k_heads: int, k_neurons: int,

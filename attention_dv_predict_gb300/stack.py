@@ -21,6 +21,11 @@ C ABI (`dv.py`); this module only orders the calls and the events.
 
 `serial=True` runs the same calls on one stream (predict then decode for
 each layer), the reference point for the overlap.
+
+`fused=True` runs each layer as one dv_layer_decode call on the main
+stream with x_pred = the previous layer's input: the same lookahead sets,
+predicted inside the layer's own launch sequence instead of on the side
+stream.
 """
 from typing import List, Optional, Sequence
 
@@ -66,13 +71,34 @@ class LayerStack:
                                   "u_h": s.u_h.clone(), "n_u_h": s.n_u_h.clone(),
                                   "u_n": s.u_n.clone(), "n_u_n": s.n_u_n.clone()})
 
+    def _enqueue_fused(self, x0, caches, kv_len):
+        n = len(self.layers)
+        main = self.main
+        self.kept = []
+        main.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(main):
+            self.x[0].copy_(x0)
+        for l in range(n):
+            kc, vc = caches[l]
+            dv.dv_layer_decode(self.layers[l], self.x[l], self.k_heads, self.k_neurons, kc, vc,
+                               kv_len, self.sel[l % 2], self.x[l + 1], self.ws_main,
+                               x_pred=self.x[max(l - 1, 0)], stream=main)
+            self._keep(l, main)
+        torch.cuda.current_stream().wait_stream(main)
+        return self.x[n]
+
     def enqueue(self, x0: torch.Tensor, caches: Sequence[Sequence[torch.Tensor]], kv_len: int,
-                serial: bool = False):
+                serial: bool = False, fused: bool = False):
         """Enqueue one token step; the output is ``self.x[-1]`` once ``self.main`` reaches it.
 
         x0 [B, d] binary32 (any stream that ``self.main`` is ordered after);
-        caches[l] = (k_cache, v_cache) of layer l.
+        caches[l] = (k_cache, v_cache) of layer l.  fused: one
+        dv_layer_decode call per layer (the predictor inside it); else the
+        predictor on the side stream (or on the main one, serial) beside
+        dv_layer_decode_presel.
         """
+        if fused:
+            return self._enqueue_fused(x0, caches, kv_len)
         n = len(self.layers)
         main, side = self.main, (self.main if serial else self.side)
         self.kept = []
@@ -99,9 +125,10 @@ class LayerStack:
         torch.cuda.current_stream().wait_stream(main)
         return self.x[n]
 
-    def run(self, x0: torch.Tensor, caches, kv_len: int, serial: bool = False) -> torch.Tensor:
+    def run(self, x0: torch.Tensor, caches, kv_len: int, serial: bool = False,
+            fused: bool = False) -> torch.Tensor:
         """One token step, synchronised; returns a copy of the stack output."""
-        y = self.enqueue(x0, caches, kv_len, serial=serial)
+        y = self.enqueue(x0, caches, kv_len, serial=serial, fused=fused)
         torch.cuda.synchronize()
         return y.clone()
 

@@ -5,7 +5,9 @@ One step = one sparse decode of one OPT-175B-shaped layer (d=12288, 96 heads
 x 128, N=49152, predictor rank 1000, fp16 storage, fp32 arithmetic, batch 1,
 KV length 2048, keep 2458 neurons / 20 heads): predictor + top-k, head-sparse
 QKV + KV append, decode attention over the selected heads, head-sparse
-out-projection, fc1 gather + ReLU, fc2 gather, both residuals.
+out-projection, fc1 gather + ReLU, fc2 gather, both residuals: seven
+kernels chained by programmatic dependent launch (dv_layer_decode).  The
+persistent streaming kernel (one launch) is timed beside it for comparison.
 
 Inputs are synthetic (seeded torch RNG on the device) and resident in HBM
 before timing.  Each step decodes the next of `--copies` distinct layer
@@ -284,9 +286,14 @@ def run_cuda(args):
     rank_us = ms_max * 1000.0 / args.steps
     achieved = step_bytes.total / (rank_us * 1e-6) / 1e9
 
-    # per-kernel durations: the same steps with an event before every kernel
+    kb = traffic.kernel_bytes(cfg.d_model, cfg.n_heads, cfg.head_dim, cfg.d_ffn, cfg.pred_rank,
+                              2 if cfg.dtype == "f16" else 4, B, n_u_h, n_u_n, cfg.kv_len)
     kt = min(args.steps, 200)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_launch + 1)] for _ in range(kt)]
+
+    # the same steps with an event before every kernel: each kernel's
+    # duration (the events serialise the kernels)
+    n_chain = dv.dv_layer_decode_launches(desc, B)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_chain + 1)] for _ in range(kt)]
     with torch.cuda.stream(stream):
         for i in range(kt):
             kc, vc = caches[i % copies]
@@ -294,18 +301,48 @@ def run_cuda(args):
                                       y, ws, evs[i], stream=stream)
     stream.synchronize()
     per_kernel = [statistics.mean(evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(kt))
-                  for k in range(n_launch)]
-    traced_step_ms = statistics.mean(evs[i][0].elapsed_time(evs[i][n_launch]) for i in range(kt))
-    kb = traffic.kernel_bytes(cfg.d_model, cfg.n_heads, cfg.head_dim, cfg.d_ffn, cfg.pred_rank,
-                              2 if cfg.dtype == "f16" else 4, B, n_u_h, n_u_n, cfg.kv_len)
-    dom = max(range(n_launch), key=lambda k: per_kernel[k])
-    dom_bytes = kb[KERNEL_BYTES_KEY[dom]]
-    dom_gbs = dom_bytes / (per_kernel[dom] * 1e-3) / 1e9
+                  for k in range(n_chain)]
+    traced_step_ms = statistics.mean(evs[i][0].elapsed_time(evs[i][n_chain]) for i in range(kt))
     kernels = {KERNELS[k]: {"us": round(per_kernel[k] * 1e3, 2),
                             "share": round(per_kernel[k] / sum(per_kernel), 4),
                             "alg_bytes": kb[KERNEL_BYTES_KEY[k]],
                             "gbs": round(kb[KERNEL_BYTES_KEY[k]] / (per_kernel[k] * 1e-3) / 1e9, 1)}
-               for k in range(n_launch)}
+               for k in range(n_chain)}
+
+    dom = max(range(n_chain), key=lambda k: per_kernel[k])
+    kern_ms, dom_name, dom_bytes = per_kernel[dom], KERNELS[dom], kb[KERNEL_BYTES_KEY[dom]]
+    dom_gbs = dom_bytes / (kern_ms * 1e-3) / 1e9
+
+    # the same decode as one persistent streaming kernel, where it serves,
+    # timed like the step (graph replays), for comparison
+    persistent = None
+    if dv.dv_layer_decode_persistent_ok(desc, B):
+        p_graphs = []
+        with torch.cuda.stream(stream):
+            for i in range(copies):
+                g = torch.cuda.CUDAGraph()
+                kc, vc = caches[i]
+                with torch.cuda.graph(g, stream=stream):
+                    dv.dv_layer_decode_persistent(layers[i], x, k_h, k_n, kc, vc, cfg.kv_len,
+                                                  sel, y, ws, stream=stream)
+                p_graphs.append(g)
+            for i in range(3):
+                p_graphs[i % copies].replay()
+            c0 = torch.cuda.Event(enable_timing=True)
+            c1 = torch.cuda.Event(enable_timing=True)
+            c0.record(stream)
+            for i in range(kt):
+                p_graphs[i % copies].replay()
+            c1.record(stream)
+        c1.synchronize()
+        p_us = c0.elapsed_time(c1) * 1e3 / kt
+        del p_graphs
+        if dv.dv_check(ws, stream) != dv.DV_OK:
+            raise RuntimeError("device status set by the persistent decode")
+        persistent = {"us_per_decode": round(p_us, 2),
+                      "achieved_gbs": round(step_bytes.total / (p_us * 1e-6) / 1e9, 1),
+                      "note": "the same decode as one persistent streaming kernel "
+                              "(dv_layer_decode_persistent), graph replays"}
 
     line = {
         "metric": METRIC, "value": round(us_per_decode, 3), "unit": "µs per layer-decode",
@@ -319,12 +356,15 @@ def run_cuda(args):
         "roofline_frac_step": round(achieved / peak, 4),
         "required_bytes_per_step": step_bytes.total,
         "union": {"heads": n_u_h, "neurons": n_u_n},
-        "roofline": {"bound": "hbm", "kernel": KERNELS[dom], "achieved": round(dom_gbs, 1),
+        "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": round(dom_gbs, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
-                     "traffic": profile_traffic(KERNELS[dom]), "peak_source": peak_src,
-                     "alg_bytes_per_launch": dom_bytes},
+                     "traffic": profile_traffic(dom_name), "peak_source": peak_src,
+                     "alg_bytes_per_launch": dom_bytes,
+                     "launch_us": round(kern_ms * 1e3, 2)},
+        "kernels_per_step": n_launch,
         "kernels": kernels,
         "traced_step_us": round(traced_step_ms * 1e3, 2),
+        "persistent": persistent,
         "gpu_launches": args.steps * n_launch,
         "clocks": clocks,
     }
@@ -416,9 +456,9 @@ def extras(args, dv, traffic, cfg, desc, layers, caches, x, sel, ws, stream, ran
 
 
 def stack_bench(args, dv, traffic, cfg, device):
-    """Tokens/s of an L-layer stack of this layer shape, lookahead predictor on
-    a side stream (attention_dv_predict_gb300/stack.py), one CUDA graph per
-    token step; at batch 1 also the same calls on one stream (no overlap)."""
+    """Tokens/s of an L-layer stack of this layer shape with the lookahead
+    predictor (attention_dv_predict_gb300/stack.py), one CUDA graph per token
+    step; at batch 1 also the chained modes for comparison."""
     import torch
 
     import dv_inputs
@@ -430,8 +470,9 @@ def stack_bench(args, dv, traffic, cfg, device):
     layers = stack.layers_from_weights(desc, weights)
     P = 2 if cfg.dtype == "f16" else 4
     out = {"layers": n, "shape": cfg.name, "kv_len": cfg.kv_len,
-           "note": "layer l+1's selection predicted from layer l's input on a side stream; "
-                   "one CUDA graph per token step; GB/s on the stack's required bytes",
+           "note": "layer l+1's selection predicted from layer l's input (overlap: on a side "
+                   "stream beside the decode; fused: inside each layer's dv_layer_decode "
+                   "call); one CUDA graph per token step; GB/s on the stack's required bytes",
            "batches": []}
     for B in [int(b) for b in args.stack_batches.split(",") if b]:
         caches = stack.stack_caches(cfg, n, B, device=device, seed0=100)
@@ -445,13 +486,19 @@ def stack_bench(args, dv, traffic, cfg, device):
                   for k in st.kept)
         st.keep_selection = False
         entry = {"batch": B, "required_bytes": req}
-        for mode in (("overlap", "serial") if B == 1 else ("overlap",)):
+        # the default mode (predictor on a side stream), plus the other two
+        # at batch 1 for comparison
+        modes = [("overlap", False)]
+        if B == 1:
+            modes += [("fused", True), ("serial", False)]
+        entry["mode"] = modes[0][0]
+        for mode, fused in modes:
             serial = mode == "serial"
-            st.run(x0, caches, cfg.kv_len, serial=serial)
+            st.run(x0, caches, cfg.kv_len, serial=serial, fused=fused)
             cs = torch.cuda.Stream(device=device)
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=cs):
-                st.enqueue(x0, caches, cfg.kv_len, serial=serial)
+                st.enqueue(x0, caches, cfg.kv_len, serial=serial, fused=fused)
             reps = max(3, 40 // B)
             for _ in range(2):
                 g.replay()
@@ -464,11 +511,11 @@ def stack_bench(args, dv, traffic, cfg, device):
             b.record()
             b.synchronize()
             ms = a.elapsed_time(b) / reps
-            key = "" if mode == "overlap" else "serial_"
+            key = "" if mode == entry["mode"] else mode + "_"
             entry[key + "ms_per_token_step"] = round(ms, 4)
             entry[key + "tokens_per_s"] = round(B / (ms * 1e-3), 1)
             entry[key + "us_per_layer"] = round(ms * 1e3 / n, 2)
-            if mode == "overlap":
+            if not key:
                 entry["achieved_gbs"] = round(req / (ms * 1e-3) / 1e9, 1)
             del g
         out["batches"].append(entry)

@@ -129,15 +129,10 @@ int dv_workspace_init(void *ws, size_t ws_bytes, void *stream);
  * it.  Returns DV_OK if nothing was recorded. */
 int dv_check(void *ws, size_t ws_bytes, void *stream);
 
-/* Kernel launches of the chained decode (dv_layer_decode_chained, and the
- * events dv_layer_decode_traced records around them). */
+/* Kernel launches one dv_layer_decode call enqueues (the events
+ * dv_layer_decode_traced records sit around them).  0 if desc or batch is
+ * invalid. */
 int dv_layer_decode_launches(const dv_layer_desc *desc, int batch);
-
-/* Kernel launches one dv_layer_decode call with these arguments enqueues on
- * the current device: 1 where the streaming kernel serves it, else the
- * chained decode's count.  0 for invalid arguments. */
-int dv_layer_decode_plan(const dv_layer_desc *desc, int batch, int k_heads, int k_neurons,
-                         int kv_len);
 
 /* 1 if dv_layer_decode_persistent (the streaming kernel) serves this shape
  * and batch on the current device for every k_heads, k_neurons and kv_len,
@@ -204,14 +199,10 @@ int dv_sparse_mlp(const dv_layer_desc *desc, const dv_layer_weights *w, const fl
  * k_heads, k_neurons).)
  *   h1: optional device output [B, d] of the attention block's result
  *       (NULL keeps it in the workspace).
- * Binary16 layers with 128-wide heads at batches 1 and 2 run as ONE
- * persistent streaming kernel (dv_layer_decode_plan() == 1): a producer warp
- * per SM streams every selected weight row into a shared-memory ring with
- * bulk copies while the other warps compute, and the steps hand over
- * through counters in the workspace (bounded waits; DV_ERR_TIMEOUT in the
- * status word if one ran out).  Every other call runs the chained decode
- * (dv_layer_decode_chained).  Both give the same selections; the streaming
- * kernel sums in a different order, so outputs agree to rounding.
+ * Seven kernels (the predictors, QKV, attention, out-projection, fc1, fc2)
+ * chained by programmatic dependent launch; plain stream order for binary16
+ * layers from 3 batch rows, where QKV, fc1, out-projection and fc2 use
+ * tensor cores.  Serves every shape and batch.
  */
 int dv_layer_decode(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x,
                     const float *x_pred, int batch, int k_heads, int k_neurons, void *k_cache,
@@ -219,11 +210,8 @@ int dv_layer_decode(const dv_layer_desc *desc, const dv_layer_weights *w, const 
                     void *ws, size_t ws_bytes, void *stream);
 
 /*
- * dv_layer_decode_chained -- dv_layer_decode as seven kernels (the
- * predictors, QKV, attention, out-projection, fc1, fc2) chained by
- * programmatic dependent launch (plain stream order for binary16 layers from
- * 3 batch rows, where QKV, fc1, out-projection and fc2 use tensor cores).
- * Serves every shape and batch.  Arguments as dv_layer_decode.
+ * dv_layer_decode_chained -- the same call as dv_layer_decode (the name
+ * states the launch structure for callers that compare the two paths).
  */
 int dv_layer_decode_chained(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x,
                             const float *x_pred, int batch, int k_heads, int k_neurons,
@@ -231,9 +219,16 @@ int dv_layer_decode_chained(const dv_layer_desc *desc, const dv_layer_weights *w
                             float *h1, float *y, void *ws, size_t ws_bytes, void *stream);
 
 /*
- * dv_layer_decode_persistent -- dv_layer_decode through the streaming
- * kernel only: DV_ERR_UNSUPPORTED, launching nothing, where it does not
- * serve (see dv_layer_decode_persistent_ok / dv_layer_decode_plan).
+ * dv_layer_decode_persistent -- dv_layer_decode as ONE persistent streaming
+ * kernel (binary16 layers with 128-wide heads, batches 1 and 2, shapes that
+ * fit its tiling: see dv_layer_decode_persistent_ok; DV_ERR_UNSUPPORTED,
+ * launching nothing, elsewhere).  A producer warp per SM streams every
+ * selected weight row into a shared-memory ring with bulk copies while the
+ * other warps compute; the steps hand over through counters in the
+ * workspace (bounded waits; DV_ERR_TIMEOUT in the status word if one ran
+ * out).  Same selections as the chain; sums in a different order, so the
+ * outputs agree to rounding.  Measured slower than the chain at the
+ * OPT-175B shape (about 250 against 128 us at batch 1), so not the default.
  * Arguments as dv_layer_decode.
  */
 int dv_layer_decode_persistent(const dv_layer_desc *desc, const dv_layer_weights *w,
@@ -241,6 +236,37 @@ int dv_layer_decode_persistent(const dv_layer_desc *desc, const dv_layer_weights
                                int k_neurons, void *k_cache, void *v_cache, int kv_len,
                                const dv_selection *sel, float *h1, float *y, void *ws,
                                size_t ws_bytes, void *stream);
+
+/*
+ * dv_layer_decode_stamped -- dv_layer_decode (persistent == 0) or
+ * dv_layer_decode_persistent (persistent != 0) that also records a timeline
+ * in stamps (device, 8-byte aligned): %globaltimer nanoseconds, G = the
+ * device's SM count.  Points a CTA does not reach are left as they were.
+ *   persistent == 0: n_stamps >= 7 * G * 4; kernel k of the chain (0 the
+ *     first predictor, 1 the second, 2 QKV, 3 attention, 4 out-projection,
+ *     5 fc1, 6 fc2) writes for each of its CTAs c (first batch tile)
+ *     stamps[(k * G + c) * 4 + i]: i = 0 the CTA starts, 1 its inputs are
+ *     ready, 2 it ends.  The tensor-core kernels (binary16 layers from 3
+ *     batch rows) record nothing.
+ *   persistent != 0: n_stamps >= 32 G; stamps[c * 32 + i] for CTA c at
+ *     fixed points: its consumer warps: 0 start, 1 first predictor stage
+ *     done, 2 predictor results complete, 3 neuron scoring starts, 4 done, 5
+ *     selection pass done, 6/7 QKV start/done (last CTA: neuron selection
+ *     start/done), 8/9 attention start/done, 10/11 out-projection
+ *     coefficients start/done, 12 out-projection done, 13/14 h1 slice
+ *     start/done, 15 norm statistics complete, 16 fc1 starts, 17 fc1 done,
+ *     18 fc2 starts, 19 fc2 done, 20/21 y slice start/done; its producer
+ *     warp: 24 + p when it starts issuing the copies of phase p (p = 0
+ *     predictor, 1 neuron scorer, 2 QKV, 3 out-projection, 4 fc1, 5 fc2),
+ *     30 when it has issued its last copy.  DV_ERR_UNSUPPORTED where the
+ *     streaming kernel does not serve.
+ * For profiling.
+ */
+int dv_layer_decode_stamped(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x,
+                            const float *x_pred, int batch, int k_heads, int k_neurons,
+                            void *k_cache, void *v_cache, int kv_len, const dv_selection *sel,
+                            float *h1, float *y, void *ws, size_t ws_bytes, int persistent,
+                            unsigned long long *stamps, int n_stamps, void *stream);
 
 /*
  * dv_layer_decode_presel -- the layer decode on a selection computed earlier:
@@ -285,8 +311,8 @@ int dv_layer_decode_host(const dv_layer_desc *desc, const dv_layer_weights *w, c
 
 /*
  * dv_test_hold_wait -- TEST SUPPORT for the bounded waits of the streaming
- * kernel.  Arms the workspace so that the next streaming decode on it (see
- * dv_layer_decode_plan) gives every device-side wait a budget of `budget_us`
+ * kernel.  Arms the workspace so that the next streaming decode on it
+ * (dv_layer_decode_persistent) gives every device-side wait a budget of `budget_us`
  * microseconds (> 0) and makes its wait number `wait_id` never complete:
  *   1 first predictor stage done      4 QKV done (attention starts)
  *   2 neuron scores done              5 attention done (out-projection)

@@ -33,8 +33,10 @@ def mods():
     return dv, stack
 
 
-@pytest.mark.parametrize("name,B,n_layers", [("tiny", 2, 4), ("opt6.7b", 1, 3), ("opt6.7b", 4, 2)])
-def test_stack_layers_match_oracle(mods, name, B, n_layers):
+@pytest.mark.parametrize("name,B,n_layers,fused", [("tiny", 2, 4, False), ("opt6.7b", 1, 3, False),
+                                                   ("opt6.7b", 1, 3, True), ("opt6.7b", 2, 2, True),
+                                                   ("opt6.7b", 4, 2, False)])
+def test_stack_layers_match_oracle(mods, name, B, n_layers, fused):
     dv, stack = mods
     cfg = dv_inputs.CONFIGS[name].with_(batch=B)
     desc = dv.desc_from_config(cfg)
@@ -45,7 +47,7 @@ def test_stack_layers_match_oracle(mods, name, B, n_layers):
     x0 = dv_inputs.make_x(cfg, B, seed=7, device="cuda")
     st = stack.LayerStack(desc, layers, B, cfg.k_heads, cfg.k_neurons)
     st.keep_selection = True
-    y = st.run(x0, caches, cfg.kv_len)
+    y = st.run(x0, caches, cfg.kv_len, fused=fused)
     xs = [t.cpu().numpy() for t in st.x]
     D = oracle.desc_from_config(cfg)
     for l in range(n_layers):
@@ -67,6 +69,21 @@ def test_stack_layers_match_oracle(mods, name, B, n_layers):
     assert np.array_equal(y.cpu().numpy(), xs[-1])
 
 
+def test_stack_fused_is_deterministic(mods):
+    dv, stack = mods
+    cfg = dv_inputs.CONFIGS["opt6.7b"].with_(batch=2)
+    desc = dv.desc_from_config(cfg)
+    ws = stack.make_stack_weights(cfg, 3, device="cuda", seed0=91)
+    layers = stack.layers_from_weights(desc, ws)
+    x0 = dv_inputs.make_x(cfg, 2, seed=4, device="cuda")
+    st = stack.LayerStack(desc, layers, 2, cfg.k_heads, cfg.k_neurons)
+    outs = []
+    for _ in range(2):
+        caches = stack.stack_caches(cfg, 3, 2, device="cuda", seed0=91)
+        outs.append(st.run(x0, caches, cfg.kv_len, fused=True))
+    assert torch.equal(outs[0], outs[1])
+
+
 def test_stack_overlap_equals_serial(mods):
     dv, stack = mods
     cfg = dv_inputs.CONFIGS["opt6.7b"].with_(batch=2)
@@ -78,5 +95,5 @@ def test_stack_overlap_equals_serial(mods):
     outs = []
     for serial in (False, True, False):
         caches = stack.stack_caches(cfg, 3, 2, device="cuda", seed0=90)
-        outs.append(st.run(x0, caches, cfg.kv_len, serial=serial))
+        outs.append(st.run(x0, caches, cfg.kv_len, serial=serial, fused=False))
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])

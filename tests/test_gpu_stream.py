@@ -1,6 +1,7 @@
-"""GPU parity of the streaming layer kernel (one persistent launch per decode
-for binary16 layers with 128-wide heads at batches 1 and 2) against the CPU
-oracle and against the seven chained kernels, plus its bounded waits."""
+"""GPU parity of the streaming layer kernel (dv_layer_decode_persistent: one
+persistent launch per decode for binary16 layers with 128-wide heads at
+batches 1 and 2) against the CPU oracle and against the seven chained
+kernels (dv_layer_decode), plus its bounded waits."""
 
 import time
 
@@ -36,35 +37,30 @@ def dv():
     return mod
 
 
-def _plan(dv, cfg, B, k_h=None, k_n=None, kv_len=None):
-    desc = dv.desc_from_config(cfg)
-    return dv.dv_layer_decode_plan(desc, B, k_h or cfg.k_heads, k_n or cfg.k_neurons,
-                                   cfg.kv_len if kv_len is None else kv_len)
+P = "dv_layer_decode_persistent"
+
+
+def _serves(dv, cfg, B):
+    return dv.dv_layer_decode_persistent_ok(dv.desc_from_config(cfg), B)
 
 
 def test_where_the_streaming_kernel_serves(dv):
-    d175 = dv.desc_from_config(CFG["opt175b"])
-    assert dv.dv_layer_decode_persistent_ok(d175, 1)
-    assert dv.dv_layer_decode_persistent_ok(d175, 2)
-    assert not dv.dv_layer_decode_persistent_ok(d175, 3)
-    assert dv.dv_layer_decode_launches(d175, 1) == 7  # the chained decode
+    assert dv.dv_layer_decode_launches(dv.desc_from_config(CFG["opt175b"]), 1) == 7
     for name in ("opt6.7b", "opt66b", "opt175b"):
-        assert _plan(dv, CFG[name], 1) == 1 and _plan(dv, CFG[name], 2) == 1
-        assert _plan(dv, CFG[name], 3) == 7
-    assert _plan(dv, RAGGED128, 1) == 1 and _plan(dv, LONGROW, 2) == 1
-    # binary32 weights and 64-wide heads take the chained path
-    assert _plan(dv, CFG["tiny"], 1) == 7
+        assert _serves(dv, CFG[name], 1) and _serves(dv, CFG[name], 2)
+        assert not _serves(dv, CFG[name], 3)
+    assert _serves(dv, RAGGED128, 1) and _serves(dv, LONGROW, 2)
+    # binary32 weights and 64-wide heads are not served
+    assert not _serves(dv, CFG["tiny"], 1)
     ragged64 = RAGGED128.with_(head_dim=64)
-    assert _plan(dv, ragged64, 1) == 7
-    assert not dv.dv_layer_decode_persistent_ok(dv.desc_from_config(ragged64), 1)
+    assert not _serves(dv, ragged64, 1)
     case = make_case(ragged64, B=1, seed=1)
     with pytest.raises(dv.DvError) as e:
-        run_gpu_layer(dv, case, entry="dv_layer_decode_persistent")
+        run_gpu_layer(dv, case, entry=P)
     assert e.value.status == dv.DV_ERR_UNSUPPORTED
 
 
-@pytest.mark.parametrize("entry", ["dv_layer_decode", "dv_layer_decode_persistent",
-                                   "dv_layer_decode_chained"])
+@pytest.mark.parametrize("entry", ["dv_layer_decode", P, "dv_layer_decode_chained"])
 @pytest.mark.parametrize("B", [1, 2])
 def test_ragged_shape(dv, entry, B):
     case = make_case(RAGGED128, B=B, seed=10 + B, separate_x_pred=(B == 2))
@@ -75,29 +71,28 @@ def test_ragged_shape(dv, entry, B):
 @pytest.mark.parametrize("B", [1, 2])
 def test_long_rows_partial_last_segment(dv, B):
     case = make_case(LONGROW, B=B, seed=40 + B, separate_x_pred=(B == 2))
-    g = run_gpu_layer(dv, case)
+    g = run_gpu_layer(dv, case, entry=P)
     check_layer_parity(case, g)
 
 
 @pytest.mark.parametrize("kv_len", [0, 1, 15, 16, 17, 160])
 def test_kv_length_edges(dv, kv_len):
     case = make_case(RAGGED128, B=2, kv_len=kv_len, kv_cap=kv_len + 3, seed=kv_len)
-    assert _plan(dv, case.cfg, 2, kv_len=kv_len) == 1
-    g = run_gpu_layer(dv, case)
+    g = run_gpu_layer(dv, case, entry=P)
     check_layer_parity(case, g)
 
 
 @pytest.mark.parametrize("norm", ["layernorm", "rmsnorm"])
 def test_norms_and_k_equals_one(dv, norm):
     case = make_case(RAGGED128.with_(norm=norm), B=2, k_h=1, k_n=1, seed=6)
-    g = run_gpu_layer(dv, case)
+    g = run_gpu_layer(dv, case, entry=P)
     check_layer_parity(case, g)
 
 
 def test_select_everything_equals_dense_oracle(dv):
     cfg = RAGGED128
     case = make_case(cfg, B=2, k_h=cfg.n_heads, k_n=cfg.d_ffn, seed=9)
-    g = run_gpu_layer(dv, case)
+    g = run_gpu_layer(dv, case, entry=P)
     D = oracle.desc_from_config(case.cfg, case.kv_cap)
     h1, y, _, _, _ = oracle.dense_layer(D, case.w_host, case.x, case.kc, case.vc, case.kv_len)
     assert np.array_equal(g["u_h"], np.arange(cfg.n_heads))
@@ -108,28 +103,28 @@ def test_select_everything_equals_dense_oracle(dv):
 
 def test_opt67b_batch2(dv):
     case = make_case(CFG["opt6.7b"], B=2, gen_device="cuda", norm_affine=True)
-    g = run_gpu_layer(dv, case)
+    g = run_gpu_layer(dv, case, entry=P)
     check_layer_parity(case, g)
 
 
 def test_opt175b_batch2(dv):
     case = make_case(CFG["opt175b"], B=2, gen_device="cuda", norm_affine=False,
                      separate_x_pred=True)
-    g = run_gpu_layer(dv, case)
+    g = run_gpu_layer(dv, case, entry=P)
     check_layer_parity(case, g)
 
 
-def test_opt175b_chained(dv):
-    # the streaming path at this shape is test_gpu_parity.test_opt175b_full
+def test_opt175b_batch1(dv):
+    # the chained path at this shape is test_gpu_parity.test_opt175b_full
     case = make_case(CFG["opt175b"], gen_device="cuda", norm_affine=False)
-    g = run_gpu_layer(dv, case, entry="dv_layer_decode_chained")
+    g = run_gpu_layer(dv, case, entry=P)
     check_layer_parity(case, g)
 
 
 def test_streaming_matches_chained(dv):
     case = make_case(CFG["opt66b"], B=1, gen_device="cuda", norm_affine=True)
-    gs = run_gpu_layer(dv, case)
-    gc = run_gpu_layer(dv, case, entry="dv_layer_decode_chained")
+    gs = run_gpu_layer(dv, case, entry=P)
+    gc = run_gpu_layer(dv, case)
     # both select within the tie band of the oracle's scores
     D = oracle.desc_from_config(case.cfg, case.kv_cap)
     p = oracle.predict(D, case.w_host, case.x, case.k_h, case.k_n)
@@ -148,7 +143,7 @@ def test_streaming_matches_chained(dv):
 
 def test_deterministic_graph_replay_and_words_at_rest(dv):
     case = make_case(RAGGED128, B=2, seed=3, separate_x_pred=True)
-    ref = run_gpu_layer(dv, case)
+    ref = run_gpu_layer(dv, case, entry=P)
     desc = dv.desc_from_config(case.cfg, case.kv_cap)
     layer = dv.Layer(desc, case.w_dev)
     sel = dv.SelectionBuffers(desc, case.B, case.k_h, case.k_n)
@@ -164,8 +159,8 @@ def test_deterministic_graph_replay_and_words_at_rest(dv):
     with torch.cuda.stream(s):
         with torch.cuda.graph(graph, stream=s):
             for _ in range(5):  # each decode rewrites the same KV slot and y
-                dv.dv_layer_decode(layer, x, case.k_h, case.k_n, kc, vc, case.kv_len, sel, y, ws,
-                                   x_pred=xp, stream=s)
+                dv.dv_layer_decode_persistent(layer, x, case.k_h, case.k_n, kc, vc, case.kv_len,
+                                              sel, y, ws, x_pred=xp, stream=s)
     for _ in range(20):
         y.zero_()
         graph.replay()
@@ -182,7 +177,7 @@ def test_deterministic_graph_replay_and_words_at_rest(dv):
 @pytest.mark.parametrize("wait_id", [1, 4, 7])
 def test_a_wait_that_runs_out_reports_and_the_next_call_is_correct(dv, wait_id):
     case = make_case(RAGGED128, B=1, seed=21)
-    ref = run_gpu_layer(dv, case)
+    ref = run_gpu_layer(dv, case, entry=P)
     desc = dv.desc_from_config(case.cfg, case.kv_cap)
     layer = dv.Layer(desc, case.w_dev)
     sel = dv.SelectionBuffers(desc, case.B, case.k_h, case.k_n)
@@ -193,7 +188,8 @@ def test_a_wait_that_runs_out_reports_and_the_next_call_is_correct(dv, wait_id):
     def decode():
         kc = torch.from_numpy(case.kc).cuda()
         vc = torch.from_numpy(case.vc).cuda()
-        dv.dv_layer_decode(layer, x, case.k_h, case.k_n, kc, vc, case.kv_len, sel, y, ws)
+        dv.dv_layer_decode_persistent(layer, x, case.k_h, case.k_n, kc, vc, case.kv_len, sel, y,
+                                      ws)
         return kc, vc
 
     dv.dv_test_hold_wait(ws, wait_id, 2000)  # 2 ms per wait

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdv.so")
 SOURCES = ["dv_abi.cu", "dv_rowdot.cu", "dv_colacc.cu", "dv_colacc_mma.cu", "dv_attn.cu",
-           "dv_select.cu", "dv_stream.cu"]
+           "dv_select.cu", "dv_stream.cu", "dv_mlp.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

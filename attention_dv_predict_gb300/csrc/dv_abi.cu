@@ -412,6 +412,45 @@ dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float
     const int d = D.d_model, N = D.d_ffn;
     int *ctl = at<int>(ws, L.ctl);
 
+    if (!use_mma(D, B) && mlp_fused_ok(D, B, max_u_n, lc.nsm)) {
+        // one pass over the selected fc1 rows and fc2 columns, then the
+        // partials' sum
+        MlpArgs m;
+        std::memset(&m, 0, sizeof(m));
+        m.d = d;
+        m.N = N;
+        m.B = B;
+        m.sel = u_n;
+        m.n_sel = n_u_n;
+        m.max_sel = max_u_n;
+        m.h1 = h1;
+        m.norm_g = w.ln2_g;
+        m.norm_b = w.ln2_b;
+        m.norm_kind = D.norm;
+        m.eps = D.ln_eps;
+        m.w1 = w.w1;
+        m.b1 = w.b1;
+        m.w2T = w.w2T;
+        m.b2 = w.b2;
+        m.part = at<float>(ws, L.mlp_part);
+        m.out = y;
+        m.status = ctl;
+        m.stamps = lc.kernel_stamps();
+        m.red_stamps = lc.kernel_stamps();
+        if (mlp_reduce_groups(d) > lc.nsm)
+            m.red_stamps = nullptr;  // more CTAs than timeline slots
+        dv_status s = lc.mark();
+        if (s)
+            return s;
+        if (launch_mlp(D.dtype, m, lc.nsm, lc.st, lc.pdl && !first) != cudaSuccess)
+            return DV_ERR_CUDA;
+        if ((s = lc.mark()))
+            return s;
+        if (launch_mlp_reduce(D.dtype, m, lc.nsm, lc.st) != cudaSuccess)
+            return DV_ERR_CUDA;
+        return DV_OK;
+    }
+
     RowArgs a;
     std::memset(&a, 0, sizeof(a));
     int nb = rowdot_nb(B, d, RK_FC1);
@@ -796,6 +835,7 @@ bool ws_layout(const dv_layer_desc &D, int B, WsLayout *L)
         L->st_partO = take(bs * kStreamMaxGroupCtas * (d + 64) * 4);
         L->st_partY = take(bs * kStreamMaxGroupCtas * (d + 64) * 4);
         L->st_stats = take(bs * kStreamMaxCtas * 4 * 4);
+        L->mlp_part = take(bs * kMlpMaxCtas * d * 4);
     }
     L->total = off;
     L->bpad = (int)bp;
@@ -862,6 +902,16 @@ int dv_layer_decode_launches(const dv_layer_desc *desc, int batch)
     if (check_desc(desc) != DV_OK || batch < 1 || batch > DV_MAX_BATCH)
         return 0;
     return kLayerLaunches;
+}
+
+int dv_mlp_one_pass(const dv_layer_desc *desc, int batch, int max_u_n)
+{
+    if (check_desc(desc) != DV_OK || batch < 1 || batch > DV_MAX_BATCH || max_u_n < 1)
+        return 0;
+    Launch lc;
+    if (make_launch(nullptr, nullptr, 0, &lc) != DV_OK)
+        return 0;
+    return !use_mma(*desc, batch) && mlp_fused_ok(*desc, batch, max_u_n, lc.nsm);
 }
 
 int dv_layer_decode_persistent_ok(const dv_layer_desc *desc, int batch)

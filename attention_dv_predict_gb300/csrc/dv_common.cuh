@@ -260,6 +260,11 @@ DV_DEV unsigned long long *chain_stamps(unsigned long long *base)
     unsigned long long *s =
         (base && blockIdx.y == 0) ? base + (size_t)blockIdx.x * kChainStamps : nullptr;
     chain_stamp(s, 0);
+    if (s && threadIdx.x == 0) {
+        unsigned sm;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+        s[3] = sm;
+    }
     return s;
 }
 DV_DEV void chain_stamp_end(unsigned long long *s)

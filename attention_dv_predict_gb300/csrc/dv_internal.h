@@ -114,7 +114,8 @@ struct PredSide {
 // Timeline of the chained decode (profiling): kernel k of the call writes,
 // for each CTA c of its first batch tile, %globaltimer nanoseconds to
 // stamps[(k * CTAs + c) * kChainStamps + i]: i = 0 the CTA starts, 1 its
-// inputs are ready (the grid dependency or the side flag passed), 2 it ends.
+// inputs are ready (the grid dependency or the side flag passed), 2 it ends;
+// slot 3 holds the SM it ran on.
 constexpr int kChainStamps = 4;
 
 // Polls of the side-work flag before the QKV kernel falls back to waiting
@@ -221,6 +222,33 @@ struct AttnArgs {
     unsigned long long *stamps;  // optional timeline [CTAs][4] (kChainStamps)
 };
 
+// Sparse MLP block as one pass (dv_mlp.cu; batches 1 and 2): CTA c computes
+// the activations of its share of the neuron union and accumulates their
+// fc2 rows into part[c][b][d]; a second kernel adds the partials, h1 and b2.
+struct MlpArgs {
+    int d, N, B;
+    const int32_t *sel;   // u_n
+    const int32_t *n_sel;
+    int max_sel;
+    const float *h1;      // [B][d] (the attention block's output)
+    const void *norm_g, *norm_b;
+    int norm_kind;
+    float eps;
+    const void *w1, *b1, *w2T, *b2;
+    float *part;          // [CTAs][B][d]
+    float *out;           // y [B][d]
+    int *status;
+    unsigned long long *stamps;      // optional timeline of the first kernel
+    unsigned long long *red_stamps;  // ... and of the second
+};
+constexpr int kMlpMaxRows = 64;   // neurons per CTA
+constexpr int kMlpMaxSeg = 8;     // fc1 row segments
+constexpr int kMlpMaxCtas = 256;  // workspace sizing of the partials
+inline int mlp_reduce_groups(int d) { return (d / 4 + 31) / 32; }
+bool mlp_fused_ok(const dv_layer_desc &D, int B, int max_u_n, int nsm);
+cudaError_t launch_mlp(int dtype, const MlpArgs &a, int grid, cudaStream_t st, bool pdl);
+cudaError_t launch_mlp_reduce(int dtype, const MlpArgs &a, int nparts, cudaStream_t st);
+
 // Dynamic shared memory of the attention kernel: the 16 warps' partial
 // outputs of dh floats.
 __host__ __device__ constexpr size_t attn_smem_bytes(int dh) { return (size_t)kWarpsPerBlock * dh * 4; }
@@ -246,6 +274,7 @@ struct WsLayout {
     // streaming kernel: segment sums of the predictor, QKV and fc1 rows,
     // column partials of the out-projection and fc2, norm statistics
     size_t st_part1, st_partQ, st_partF, st_partO, st_partY, st_stats;
+    size_t mlp_part;  // one-pass MLP: per-CTA partials of y
     size_t total;
     int bpad;         // batch rounded up to the largest batch tile (8)
     int attn_splits_max;

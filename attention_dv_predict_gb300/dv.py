@@ -63,6 +63,7 @@ _SIGS = {
     "dv_check": ([_P, _SZ, _P], _I),
     "dv_layer_decode_launches": ([_D, _I], _I),
     "dv_layer_decode_persistent_ok": ([_D, _I], _I),
+    "dv_mlp_one_pass": ([_D, _I, _I], _I),
     "dv_predict_topk": ([_D, _W, _P, _I, _I, _I, _S, _P, _P, _P, _SZ, _P], _I),
     "dv_predict_topk_noalloc": ([_D, _W, _P, _I, _I, _I, _S, _P, _P, _P], _I),
     "dv_sparse_attn": ([_D, _W, _P, _I, _P, _P, _I, _P, _P, _I, _P, _P, _SZ, _P], _I),
@@ -206,6 +207,11 @@ def dv_check(ws: Workspace, stream=None) -> int:
 
 def dv_layer_decode_launches(desc: LayerDesc, batch: int) -> int:
     return int(_lib.dv_layer_decode_launches(C.byref(desc), int(batch)))
+
+
+def dv_mlp_one_pass(desc: LayerDesc, batch: int, max_u_n: int) -> bool:
+    """The MLP half runs as one pass plus the partials' sum (two kernels)."""
+    return bool(_lib.dv_mlp_one_pass(C.byref(desc), int(batch), int(max_u_n)))
 
 
 def dv_layer_decode_persistent_ok(desc: LayerDesc, batch: int) -> bool:

@@ -95,17 +95,25 @@ def dense_step_bytes(d_model: int, n_heads: int, head_dim: int, d_ffn: int, p_by
 
 def kernel_bytes(d_model: int, n_heads: int, head_dim: int, d_ffn: int, pred_rank: int,
                  p_bytes: int, batch: int, n_u_heads: int, n_u_neurons: int,
-                 kv_len: int) -> Dict[str, int]:
-    """Algorithmic bytes per launch of each kernel of the layer decode."""
+                 kv_len: int, n_parts: int = 0) -> Dict[str, int]:
+    """Algorithmic bytes per launch of each kernel of the layer decode.
+
+    "mlp" is the one-pass MLP kernel (fc1 and fc2 together); "mlp_reduce"
+    the kernel that adds its n_parts per-CTA partials of y (the partials are
+    read once, h1 read, y written)."""
     d, H, dh, N, r, P, B = d_model, n_heads, head_dim, d_ffn, pred_rank, p_bytes, batch
     uh, un = n_u_heads, n_u_neurons
+    fc1 = P * un * (d + 1) + P * 2 * d + 4 * B * (d + un)
+    fc2 = P * un * d + P * d + 4 * B * (2 * d + un)
     return {
+        "mlp": P * un * (2 * d + 1) + P * 3 * d + 4 * B * 2 * d,
+        "mlp_reduce": 4 * B * d * (n_parts + 2) + P * d,
         "pred_stage1": P * (H + r) * d + 4 * B * d + 4 * B * (H + r),
         "pred_stage2": P * N * r + 4 * B * r + 4 * B * N,
         "qkv": P * 3 * uh * dh * (d + 1) + P * 2 * d + 4 * B * d + 4 * B * uh * dh
         + P * 2 * B * uh * dh,
         "attn": P * 2 * B * uh * (kv_len + 1) * dh + 4 * 2 * B * uh * dh,
         "oproj": P * uh * dh * d + P * d + 4 * B * (2 * d + uh * dh),
-        "fc1": P * un * (d + 1) + P * 2 * d + 4 * B * (d + un),
-        "fc2": P * un * d + P * d + 4 * B * (2 * d + un),
+        "fc1": fc1,
+        "fc2": fc2,
     }

@@ -38,6 +38,7 @@ if ROOT not in sys.path:
 KERNELS = ["pred_stage1_head_topk", "pred_stage2_neuron_topk", "qkv_ln1_kv_append",
            "attn_decode", "oproj_residual", "fc1_ln2_relu", "fc2_residual"]
 KERNEL_BYTES_KEY = ["pred_stage1", "pred_stage2", "qkv", "attn", "oproj", "fc1", "fc2"]
+GRAPH_STEPS = 64
 METRIC = "µs per sparse layer-decode and achieved HBM GB/s (% roofline) at OPT-175B shape"
 
 
@@ -238,19 +239,28 @@ def run_cuda(args):
     u_h, u_n = sel.unions()
     n_u_h, n_u_n = int(u_h.numel()), int(u_n.numel())
 
-    # one CUDA graph per layer copy; a step is one graph replay
-    graphs = []
-    with torch.cuda.stream(stream):
-        for i in range(copies):
-            g = torch.cuda.CUDAGraph()
+    # the steps run from CUDA graphs of up to GRAPH_STEPS consecutive decodes
+    # (step i decodes layer copy i % copies), as a serving loop replays one
+    # graph per token over all layers: no host launch gaps between steps
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
             with torch.cuda.graph(g, stream=stream):
-                step(i, stream)
-            graphs.append(g)
+                for i in range(n):
+                    step(i, stream)
+        return g
+
+    def plan(n):
+        full, rem = divmod(n, GRAPH_STEPS)
+        return ([capture(GRAPH_STEPS)] * full if full else []) + ([capture(rem)] if rem else [])
+
+    warm_graphs = plan(args.warmup)
+    timed_graphs = plan(args.steps)
     stream.synchronize()
 
     with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            graphs[i % copies].replay()
+        for g in warm_graphs:
+            g.replay()
     stream.synchronize()
 
     uuid = None
@@ -266,8 +276,8 @@ def run_cuda(args):
     t1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         t0.record(stream)
-        for i in range(args.steps):
-            graphs[i % copies].replay()
+        for g in timed_graphs:
+            g.replay()
         t1.record(stream)
     t1.synchronize()
     torch.cuda.synchronize()
@@ -287,7 +297,8 @@ def run_cuda(args):
     achieved = step_bytes.total / (rank_us * 1e-6) / 1e9
 
     kb = traffic.kernel_bytes(cfg.d_model, cfg.n_heads, cfg.head_dim, cfg.d_ffn, cfg.pred_rank,
-                              2 if cfg.dtype == "f16" else 4, B, n_u_h, n_u_n, cfg.kv_len)
+                              2 if cfg.dtype == "f16" else 4, B, n_u_h, n_u_n, cfg.kv_len,
+                              n_parts=torch.cuda.get_device_properties(dev).multi_processor_count)
     kt = min(args.steps, 200)
 
     # the same steps with an event before every kernel: each kernel's
@@ -303,14 +314,18 @@ def run_cuda(args):
     per_kernel = [statistics.mean(evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(kt))
                   for k in range(n_chain)]
     traced_step_ms = statistics.mean(evs[i][0].elapsed_time(evs[i][n_chain]) for i in range(kt))
-    kernels = {KERNELS[k]: {"us": round(per_kernel[k] * 1e3, 2),
-                            "share": round(per_kernel[k] / sum(per_kernel), 4),
-                            "alg_bytes": kb[KERNEL_BYTES_KEY[k]],
-                            "gbs": round(kb[KERNEL_BYTES_KEY[k]] / (per_kernel[k] * 1e-3) / 1e9, 1)}
+    names, keys = list(KERNELS), list(KERNEL_BYTES_KEY)
+    if dv.dv_mlp_one_pass(desc, B, min(B * k_n, cfg.d_ffn)):
+        names[5:7] = ["mlp_fc1_fc2_partials", "mlp_partials_sum"]
+        keys[5:7] = ["mlp", "mlp_reduce"]
+    kernels = {names[k]: {"us": round(per_kernel[k] * 1e3, 2),
+                          "share": round(per_kernel[k] / sum(per_kernel), 4),
+                          "alg_bytes": kb[keys[k]],
+                          "gbs": round(kb[keys[k]] / (per_kernel[k] * 1e-3) / 1e9, 1)}
                for k in range(n_chain)}
 
     dom = max(range(n_chain), key=lambda k: per_kernel[k])
-    kern_ms, dom_name, dom_bytes = per_kernel[dom], KERNELS[dom], kb[KERNEL_BYTES_KEY[dom]]
+    kern_ms, dom_name, dom_bytes = per_kernel[dom], names[dom], kb[keys[dom]]
     dom_gbs = dom_bytes / (kern_ms * 1e-3) / 1e9
 
     # the same decode as one persistent streaming kernel, where it serves,

@@ -134,6 +134,13 @@ int dv_check(void *ws, size_t ws_bytes, void *stream);
  * invalid. */
 int dv_layer_decode_launches(const dv_layer_desc *desc, int batch);
 
+/* 1 if dv_sparse_mlp (and the MLP half of dv_layer_decode) with a neuron
+ * union of at most max_u_n runs as one pass over the selected fc1 rows and
+ * fc2 columns plus a kernel that adds the per-CTA partials of y, on the
+ * current device; 0 if it runs as the fc1 and fc2 kernels, or for invalid
+ * arguments. */
+int dv_mlp_one_pass(const dv_layer_desc *desc, int batch, int max_u_n);
+
 /* 1 if dv_layer_decode_persistent (the streaming kernel) serves this shape
  * and batch on the current device for every k_heads, k_neurons and kv_len,
  * else 0. */
@@ -246,8 +253,8 @@ int dv_layer_decode_persistent(const dv_layer_desc *desc, const dv_layer_weights
  *     first predictor, 1 the second, 2 QKV, 3 attention, 4 out-projection,
  *     5 fc1, 6 fc2) writes for each of its CTAs c (first batch tile)
  *     stamps[(k * G + c) * 4 + i]: i = 0 the CTA starts, 1 its inputs are
- *     ready, 2 it ends.  The tensor-core kernels (binary16 layers from 3
- *     batch rows) record nothing.
+ *     ready, 2 it ends; slot 3 is the SM it ran on (%smid).  The tensor-core
+ *     kernels (binary16 layers from 3 batch rows) record nothing.
  *   persistent != 0: n_stamps >= 32 G; stamps[c * 32 + i] for CTA c at
  *     fixed points: its consumer warps: 0 start, 1 first predictor stage
  *     done, 2 predictor results complete, 3 neuron scoring starts, 4 done, 5

@@ -50,5 +50,10 @@ def test_opt175b_required_bytes():
     assert b.fc1 + b.fc2 == 2 * 2 * 2458 * 12288
     assert b.kv_read == 2 * 2 * 20 * 2049 * 128
     assert 518.9e6 < b.total < 519.0e6
-    kb = traffic.kernel_bytes(12288, 96, 128, 49152, 1000, 2, 1, 20, 2458, 2048)
-    assert abs(sum(kb.values()) - b.total) < 0.01 * b.total
+    kb = traffic.kernel_bytes(12288, 96, 128, 49152, 1000, 2, 1, 20, 2458, 2048, n_parts=152)
+    chain = ["pred_stage1", "pred_stage2", "qkv", "attn", "oproj", "fc1", "fc2"]
+    assert abs(sum(kb[k] for k in chain) - b.total) < 0.01 * b.total
+    # the one-pass MLP reads the same weights as fc1 + fc2; its second kernel
+    # reads one partial of y per CTA
+    assert abs(kb["mlp"] - (kb["fc1"] + kb["fc2"])) < 0.001 * kb["mlp"]
+    assert kb["mlp_reduce"] == 4 * 12288 * (152 + 2) + 2 * 12288

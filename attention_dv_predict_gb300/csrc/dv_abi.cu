@@ -431,14 +431,21 @@ dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float
         m.w1 = w.w1;
         m.b1 = w.b1;
         m.w2T = w.w2T;
-        m.b2 = w.b2;
         m.part = at<float>(ws, L.mlp_part);
-        m.out = y;
         m.status = ctl;
         m.stamps = lc.kernel_stamps();
-        m.red_stamps = lc.kernel_stamps();
-        if (mlp_reduce_groups(d) > lc.nsm)
-            m.red_stamps = nullptr;  // more CTAs than timeline slots
+        PartSumArgs ps;
+        std::memset(&ps, 0, sizeof(ps));
+        ps.d = d;
+        ps.B = B;
+        ps.nparts = lc.nsm;
+        ps.res = h1;
+        ps.bias = w.b2;
+        ps.part = m.part;
+        ps.out = y;
+        ps.stamps = lc.kernel_stamps();
+        if (part_sum_groups(d) > lc.nsm)
+            ps.stamps = nullptr;  // more CTAs than timeline slots
         dv_status s = lc.mark();
         if (s)
             return s;
@@ -446,7 +453,7 @@ dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float
             return DV_ERR_CUDA;
         if ((s = lc.mark()))
             return s;
-        if (launch_mlp_reduce(D.dtype, m, lc.nsm, lc.st) != cudaSuccess)
+        if (launch_part_sum(D.dtype, ps, lc.st) != cudaSuccess)
             return DV_ERR_CUDA;
         return DV_OK;
     }
@@ -835,7 +842,7 @@ bool ws_layout(const dv_layer_desc &D, int B, WsLayout *L)
         L->st_partO = take(bs * kStreamMaxGroupCtas * (d + 64) * 4);
         L->st_partY = take(bs * kStreamMaxGroupCtas * (d + 64) * 4);
         L->st_stats = take(bs * kStreamMaxCtas * 4 * 4);
-        L->mlp_part = take(bs * kMlpMaxCtas * d * 4);
+        L->mlp_part = take(bs * kPartMaxCtas * d * 4);
     }
     L->total = off;
     L->bpad = (int)bp;

@@ -115,8 +115,9 @@ struct PredSide {
 // for each CTA c of its first batch tile, %globaltimer nanoseconds to
 // stamps[(k * CTAs + c) * kChainStamps + i]: i = 0 the CTA starts, 1 its
 // inputs are ready (the grid dependency or the side flag passed), 2 it ends;
-// slot 3 holds the SM it ran on.
-constexpr int kChainStamps = 4;
+// slot 3 holds the SM it ran on; 4 .. 7 are points inside a kernel (the
+// one-pass MLP: 4 its activations summed).
+constexpr int kChainStamps = 8;
 
 // Polls of the side-work flag before the QKV kernel falls back to waiting
 // for the whole stage-2 predictor grid.
@@ -234,20 +235,30 @@ struct MlpArgs {
     const void *norm_g, *norm_b;
     int norm_kind;
     float eps;
-    const void *w1, *b1, *w2T, *b2;
+    const void *w1, *b1, *w2T;
     float *part;          // [CTAs][B][d]
-    float *out;           // y [B][d]
     int *status;
-    unsigned long long *stamps;      // optional timeline of the first kernel
-    unsigned long long *red_stamps;  // ... and of the second
+    unsigned long long *stamps;  // optional timeline
 };
 constexpr int kMlpMaxRows = 64;   // neurons per CTA
 constexpr int kMlpMaxSeg = 8;     // fc1 row segments
-constexpr int kMlpMaxCtas = 256;  // workspace sizing of the partials
-inline int mlp_reduce_groups(int d) { return (d / 4 + 31) / 32; }
 bool mlp_fused_ok(const dv_layer_desc &D, int B, int max_u_n, int nsm);
 cudaError_t launch_mlp(int dtype, const MlpArgs &a, int grid, cudaStream_t st, bool pdl);
-cudaError_t launch_mlp_reduce(int dtype, const MlpArgs &a, int nparts, cudaStream_t st);
+
+// Sum of the per-CTA partials of a one-pass column accumulation
+// (dv_partials.cuh): out[b][col] = res[b][col] + bias[col] + sum_c
+// part[c][b][col].
+struct PartSumArgs {
+    int d, B, nparts;
+    const float *res;
+    const void *bias;
+    const float *part;    // [nparts][B][d]
+    float *out;           // [B][d]
+    unsigned long long *stamps;
+};
+constexpr int kPartMaxCtas = 256;  // CTAs of a one-pass kernel (partials' workspace)
+inline int part_sum_groups(int d) { return (d / 4 + 31) / 32; }
+cudaError_t launch_part_sum(int dtype, const PartSumArgs &a, cudaStream_t st);
 
 // Dynamic shared memory of the attention kernel: the 16 warps' partial
 // outputs of dh floats.

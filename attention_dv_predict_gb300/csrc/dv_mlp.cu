@@ -16,6 +16,7 @@
 // barrier, and the fc2 loads are in flight while the activations are summed.
 // A second kernel adds the CTAs' partials in a fixed order (results do not
 // depend on scheduling), the residual and the bias.
+#include "dv_partials.cuh"
 #include "dv_rowdot.cuh"
 
 namespace dv {
@@ -23,13 +24,14 @@ namespace {
 
 constexpr int kMlpU = 8;  // 16-byte chunks per lane in one fc1 segment
 
-// Dynamic shared memory: staged norm(h1) [NB][d], then the per-segment sums
-// [kMlpMaxRows][kMlpMaxSeg][NB], the activations [kMlpMaxRows][NB] and the
-// neuron ids [kMlpMaxRows].
+// Dynamic shared memory: the w2T row offsets [kMlpMaxRows], staged norm(h1)
+// [NB][d], then the per-segment sums [kMlpMaxRows][kMlpMaxSeg][NB], the
+// activations [kMlpMaxRows][NB] and the neuron ids [kMlpMaxRows].
 __host__ __device__ constexpr size_t mlp_smem(int nb, int d)
 {
-    return (size_t)nb * d * 4 + (size_t)kMlpMaxRows * kMlpMaxSeg * nb * 4 +
-           (size_t)kMlpMaxRows * nb * 4 + (size_t)kMlpMaxRows * 4;
+    return (size_t)kMlpMaxRows * 8 + (size_t)nb * d * 4 +
+           (size_t)kMlpMaxRows * kMlpMaxSeg * nb * 4 + (size_t)kMlpMaxRows * nb * 4 +
+           (size_t)kMlpMaxRows * 4;
 }
 
 template <typename T, int NB, int CJ>
@@ -44,7 +46,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_mlp(const MlpArgs a)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d = a.d, cpr = d / EPC, G = gridDim.x, cta = blockIdx.x;
     const int nsu = (cpr + 32 * U - 1) / (32 * U);
-    float *xs = smem;
+    long long *soff = reinterpret_cast<long long *>(smem);
+    float *xs = smem + 2 * kMlpMaxRows;
     float *upart = xs + (size_t)NB * d;                    // [row][seg][b]
     float *act = upart + (size_t)kMlpMaxRows * kMlpMaxSeg * NB;  // [row][b]
     int *ssel = reinterpret_cast<int *>(act + (size_t)kMlpMaxRows * NB);
@@ -60,6 +63,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_mlp(const MlpArgs a)
         const int h = ld_cg(a.sel + n0 + tid);
         const bool ok = h >= 0 && h < a.N;
         ssel[tid] = ok ? h : -1;
+        soff[tid] = ok ? (long long)h * d : -1;
         if (!ok)
             set_status(a.status, DV_ERR_DEVICE_INDEX);
     }
@@ -122,49 +126,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_mlp(const MlpArgs a)
             cur[j] = nxt[j];
     }
 
-    // fc2: a ring of four rows in flight per thread (row r + 3 loads while
-    // row r is used); the first three rows' loads go out before the
-    // activations are summed
-    float acc[CJ][EPC][NB];
-#pragma unroll
-    for (int j = 0; j < CJ; ++j)
-#pragma unroll
-        for (int e = 0; e < EPC; ++e)
-#pragma unroll
-            for (int b = 0; b < NB; ++b)
-                acc[j][e][b] = 0.f;
-    auto load2 = [&](int r, uint4 (&v)[CJ]) {
-        const int h = (r < nr) ? ssel[r] : -1;
-        const T *p = W2 + (size_t)(h < 0 ? 0 : h) * d;
-#pragma unroll
-        for (int j = 0; j < CJ; ++j) {
-            const int c = tid + kThreads * j;
-            v[j] = (h >= 0 && c < cpr) ? ld_stream(p + (size_t)c * EPC)
-                                       : make_uint4(0u, 0u, 0u, 0u);
-        }
-    };
-    auto use2 = [&](int r, const uint4 (&v)[CJ]) {
-        if (r >= nr)
-            return;
-        float cf[NB];
-#pragma unroll
-        for (int b = 0; b < NB; ++b)
-            cf[b] = act[r * NB + b];
-#pragma unroll
-        for (int j = 0; j < CJ; ++j) {
-            float f[EPC];
-            Elem<T>::unpack(v[j], f);
-#pragma unroll
-            for (int e = 0; e < EPC; ++e)
-#pragma unroll
-                for (int b = 0; b < NB; ++b)
-                    acc[j][e][b] = fmaf(cf[b], f[e], acc[j][e][b]);
-        }
-    };
-    uint4 w0[CJ], w1[CJ], w2[CJ], w3[CJ];
-    load2(0, w0);
-    load2(1, w1);
-    load2(2, w2);
+    // fc2: a ring of four rows in flight per thread; the first three rows'
+    // loads go out before the activations are summed
+    uint4 w0[CJ], w1[CJ], w2[CJ];
+    col_ring_load<T, NB, CJ>(W2, 0 < nr ? soff[0] : -1, d, w0);
+    col_ring_load<T, NB, CJ>(W2, 1 < nr ? soff[1] : -1, d, w1);
+    col_ring_load<T, NB, CJ>(W2, 2 < nr ? soff[2] : -1, d, w2);
     __syncthreads();  // every segment sum is in shared memory
     if (tid < nr * NB) {
         const int row = tid / NB, b = tid - row * NB;
@@ -176,94 +143,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_mlp(const MlpArgs a)
         act[row * NB + b] = (h >= 0 && b < a.B) ? fmaxf(s + bias, 0.f) : 0.f;
     }
     __syncthreads();
-    for (int r = 0; r < nr; r += 4) {
-        load2(r + 3, w3);
-        use2(r, w0);
-        load2(r + 4, w0);
-        use2(r + 1, w1);
-        load2(r + 5, w1);
-        use2(r + 2, w2);
-        load2(r + 6, w2);
-        use2(r + 3, w3);
-    }
+    chain_stamp(stamps, 4);
     // this CTA's partial (zeros when it owns no neuron)
-#pragma unroll
-    for (int j = 0; j < CJ; ++j) {
-        const int c = tid + kThreads * j;
-        if (c >= cpr)
-            continue;
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            float *o = a.part + ((size_t)cta * NB + b) * d + (size_t)c * EPC;
-#pragma unroll
-            for (int e = 0; e < EPC; e += 4)
-                *reinterpret_cast<float4 *>(o + e) =
-                    make_float4(acc[j][e][b], acc[j][e + 1][b], acc[j][e + 2][b], acc[j][e + 3][b]);
-        }
-    }
-    chain_stamp_end(stamps);
-}
-
-// y[b][col] = h1[b][col] + b2[col] + sum over CTAs c (in order of slice, then
-// c) of part[c][b][col].  CTA (g, b): columns [128 g, 128 g + 128) of row b;
-// thread (s, q) sums the partials c = s, s + 16, ... of column quad q, then
-// 32 threads add the 16 slices in order.
-constexpr int kRedSlices = 16;
-
-template <typename T, int NB>
-__global__ void __launch_bounds__(kThreads) k_mlp_reduce(const MlpArgs a, int nparts)
-{
-    unsigned long long *stamps = chain_stamps(a.red_stamps);
-    __shared__ float4 sred[kRedSlices][32];
-    const int tid = threadIdx.x, q = tid & 31, s = tid >> 5;
-    const int b = blockIdx.y, col = (blockIdx.x * 32 + q) * 4;
-    const bool in = col < a.d && b < a.B;
-    float4 base = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (in && s == 0) {  // inputs two launches back or older
-        const float4 h = __ldcg(reinterpret_cast<const float4 *>(a.h1 + (size_t)b * a.d + col));
-        const T *b2 = static_cast<const T *>(a.b2);
-        base = make_float4(h.x + Elem<T>::load(b2, col), h.y + Elem<T>::load(b2, col + 1),
-                           h.z + Elem<T>::load(b2, col + 2), h.w + Elem<T>::load(b2, col + 3));
-    }
-    pdl_wait();
-    chain_stamp(stamps, 1);
-    pdl_launch_dependents();
-    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (in) {
-        // every partial of the thread's slice in flight at once (CTAs <=
-        // kMlpMaxCtas = 16 slices x 16)
-        constexpr int kBatch = kMlpMaxCtas / kRedSlices;
-        for (int c0 = s; c0 < nparts; c0 += kBatch * kRedSlices) {
-            float4 v[kBatch];
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                const int c = c0 + k * kRedSlices;
-                v[k] = c < nparts ? __ldcg(reinterpret_cast<const float4 *>(
-                                        a.part + ((size_t)c * NB + b) * a.d + col))
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                sum.x += v[k].x;
-                sum.y += v[k].y;
-                sum.z += v[k].z;
-                sum.w += v[k].w;
-            }
-        }
-    }
-    sred[s][q] = sum;
-    __syncthreads();
-    if (s == 0 && in) {
-        float4 t = base;
-        for (int k = 0; k < kRedSlices; ++k) {
-            const float4 v = sred[k][q];
-            t.x += v.x;
-            t.y += v.y;
-            t.z += v.z;
-            t.w += v.w;
-        }
-        *reinterpret_cast<float4 *>(a.out + (size_t)b * a.d + col) = t;
-    }
+    col_ring<T, NB, CJ>(W2, soff, act, nr, d, w0, w1, w2, a.part + (size_t)cta * NB * d);
     chain_stamp_end(stamps);
 }
 
@@ -309,21 +191,6 @@ cudaError_t dispatch_cj(int cj, const MlpArgs &a, int grid, cudaStream_t st, boo
     }
 }
 
-template <typename T, int NB>
-cudaError_t launch_reduce_t(const MlpArgs &a, int nparts, cudaStream_t st)
-{
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(mlp_reduce_groups(a.d), a.B);
-    cfg.blockDim = dim3(kThreads);
-    cfg.stream = st;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_mlp_reduce<T, NB>, a, nparts);
-}
-
 }  // namespace
 
 int mlp_chunk_cols(int dtype, int d)
@@ -336,7 +203,7 @@ int mlp_chunk_cols(int dtype, int d)
 
 bool mlp_fused_ok(const dv_layer_desc &D, int B, int max_u_n, int nsm)
 {
-    if (B < 1 || B > 2 || nsm > kMlpMaxCtas || D.d_model % 4)
+    if (B < 1 || B > 2 || nsm > kPartMaxCtas || D.d_model % 4)
         return false;
     const int epc = D.dtype == DV_F16 ? 8 : 4;
     const int cpr = D.d_model / epc;
@@ -359,13 +226,13 @@ cudaError_t launch_mlp(int dtype, const MlpArgs &a, int grid, cudaStream_t st, b
                     : dispatch_cj<float, 2>(cj, a, grid, st, pdl);
 }
 
-cudaError_t launch_mlp_reduce(int dtype, const MlpArgs &a, int nparts, cudaStream_t st)
+cudaError_t launch_part_sum(int dtype, const PartSumArgs &a, cudaStream_t st)
 {
+    if (a.nparts > kPartMaxCtas || a.B < 1 || a.B > 2)
+        return cudaErrorInvalidValue;
     if (dtype == DV_F16)
-        return a.B == 1 ? launch_reduce_t<__half, 1>(a, nparts, st)
-                        : launch_reduce_t<__half, 2>(a, nparts, st);
-    return a.B == 1 ? launch_reduce_t<float, 1>(a, nparts, st)
-                    : launch_reduce_t<float, 2>(a, nparts, st);
+        return a.B == 1 ? launch_part_sum_t<__half, 1>(a, st) : launch_part_sum_t<__half, 2>(a, st);
+    return a.B == 1 ? launch_part_sum_t<float, 1>(a, st) : launch_part_sum_t<float, 2>(a, st);
 }
 
 }  // namespace dv

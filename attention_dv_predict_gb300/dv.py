@@ -286,7 +286,7 @@ def dv_layer_decode_stamped(layer: Layer, x: torch.Tensor, k_heads: int, k_neuro
                             stamps: torch.Tensor, x_pred: Optional[torch.Tensor] = None,
                             h1: Optional[torch.Tensor] = None, persistent: bool = False,
                             stream=None):
-    """The decode with its timeline in ``stamps`` (int64): [7, SMs, 4] for the
+    """The decode with its timeline in ``stamps`` (int64): [7, SMs, 8] for the
     chain, [SMs, 32] for the persistent streaming kernel."""
     B = x.shape[0]
     _check("dv_layer_decode_stamped", _lib.dv_layer_decode_stamped(

@@ -141,6 +141,8 @@ int dv_layer_decode_launches(const dv_layer_desc *desc, int batch);
  * arguments. */
 int dv_mlp_one_pass(const dv_layer_desc *desc, int batch, int max_u_n);
 
+
+
 /* 1 if dv_layer_decode_persistent (the streaming kernel) serves this shape
  * and batch on the current device for every k_heads, k_neurons and kv_len,
  * else 0. */
@@ -249,12 +251,14 @@ int dv_layer_decode_persistent(const dv_layer_desc *desc, const dv_layer_weights
  * dv_layer_decode_persistent (persistent != 0) that also records a timeline
  * in stamps (device, 8-byte aligned): %globaltimer nanoseconds, G = the
  * device's SM count.  Points a CTA does not reach are left as they were.
- *   persistent == 0: n_stamps >= 7 * G * 4; kernel k of the chain (0 the
+ *   persistent == 0: n_stamps >= 7 * G * 8; kernel k of the chain (0 the
  *     first predictor, 1 the second, 2 QKV, 3 attention, 4 out-projection,
- *     5 fc1, 6 fc2) writes for each of its CTAs c (first batch tile)
- *     stamps[(k * G + c) * 4 + i]: i = 0 the CTA starts, 1 its inputs are
- *     ready, 2 it ends; slot 3 is the SM it ran on (%smid).  The tensor-core
- *     kernels (binary16 layers from 3 batch rows) record nothing.
+ *     5 fc1 or the one-pass MLP, 6 fc2 or the sum of the MLP's partials)
+ *     writes for each of its CTAs c (first batch tile)
+ *     stamps[(k * G + c) * 8 + i]: i = 0 the CTA starts, 1 its inputs are
+ *     ready, 2 it ends, 3 the SM it ran on (%smid); 4 .. 7 points inside a
+ *     kernel (the one-pass MLP: 4 its activations summed).  The tensor-core kernels (binary16 layers from 3 batch rows)
+ *     record nothing.
  *   persistent != 0: n_stamps >= 32 G; stamps[c * 32 + i] for CTA c at
  *     fixed points: its consumer warps: 0 start, 1 first predictor stage
  *     done, 2 predictor results complete, 3 neuron scoring starts, 4 done, 5

@@ -20,8 +20,10 @@
 //
 // The head list was published before the previous kernel ran (flag) or
 // given by the caller, so the CTAs read it and place their work before the
-// grid wait; q and the appended position come from the QKV kernel, so all
-// K/V loads follow the wait.
+// grid wait.  q and the appended position come from the QKV kernel: the warp
+// whose range holds the appended position loads after the wait, the other
+// warps issue their first two batches of older positions before it (hiding
+// the first round trip: measured 2 us per OPT-175B decode).
 #pragma once
 
 #include "dv_common.cuh"
@@ -88,16 +90,16 @@ DV_DEV void attn_body(const AttnArgs &a, int cta, int nct, const Dep &dep)
         const int p0 = c0 + (int)((long long)(c1 - c0) * warp / kWarpsPerBlock);
         const int p1 = c0 + (int)((long long)(c1 - c0) * (warp + 1) / kWarpsPerBlock);
         const size_t base = ((size_t)b * a.H + h) * (size_t)a.kv_cap * DH + (size_t)dc * EPC;
-        if (!waited) {
-            // q and the appended K/V come from the previous kernel.  (Loading
-            // the older positions before this wait was measured: the extra
-            // traffic beside the QKV kernel's tail made the step slower.)
-            dep.wait();
-            waited = true;
-        }
         const int nbatch = (p1 - p0 + KPW * UK - 1) / (KPW * UK);
         // the warp whose range holds position kv_len reads all its rows at L2
         const bool coh = p0 <= a.kv_len && a.kv_len < p1;  // uniform over the warp
+        // q and the appended K/V come from the previous kernel: the warp
+        // holding position kv_len waits before its loads; the others load
+        // their older positions (inputs no kernel writes) first
+        if (!waited && coh) {
+            dep.wait();
+            waited = true;
+        }
         auto ldkv = [&](const T *row) { return coh ? ld_stream_coherent(row) : ld_stream(row); };
         uint4 kc[UK], vc[UK], kn[UK], vn[UK];
 #pragma unroll
@@ -111,6 +113,10 @@ DV_DEV void attn_body(const AttnArgs &a, int cta, int nct, const Dep &dep)
             const int p = p0 + (UK + uu) * KPW + ks;
             kn[uu] = p < p1 ? ldkv(Kc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
             vn[uu] = p < p1 ? ldkv(Vc + base + (size_t)p * DH) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (!waited) {
+            dep.wait();
+            waited = true;
         }
         float q[EPC];
         {
@@ -130,6 +136,8 @@ DV_DEV void attn_body(const AttnArgs &a, int cta, int nct, const Dep &dep)
             o[e] = 0.f;
 
         for (int bt = 0; bt < nbatch; ++bt) {
+            if (bt == 1)
+                chain_stamp(dep.stamps, 4);  // warp 0's first batch consumed
             const int pb = p0 + bt * KPW * UK;
 #pragma unroll
             for (int uu = 0; uu < UK; ++uu) {
@@ -183,6 +191,7 @@ DV_DEV void attn_body(const AttnArgs &a, int cta, int nct, const Dep &dep)
             }
             m = mn;
         }
+        chain_stamp(dep.stamps, 5);  // warp 0's keys done
         if (ks == 0) {
 #pragma unroll
             for (int e = 0; e < EPC; ++e)
@@ -213,6 +222,7 @@ DV_DEV void attn_body(const AttnArgs &a, int cta, int nct, const Dep &dep)
             r[0] = M;
             r[1] = Ls;
         }
+        chain_stamp(dep.stamps, 6);  // record written (thread 0)
         __syncthreads();
     }
     if (!waited) {  // no unit: still order this grid after the previous one

@@ -115,8 +115,9 @@ struct PredSide {
 // for each CTA c of its first batch tile, %globaltimer nanoseconds to
 // stamps[(k * CTAs + c) * kChainStamps + i]: i = 0 the CTA starts, 1 its
 // inputs are ready (the grid dependency or the side flag passed), 2 it ends;
-// slot 3 holds the SM it ran on; 4 .. 7 are points inside a kernel (the
-// one-pass MLP: 4 its activations summed).
+// slot 3 holds the SM it ran on; 4 .. 7 are points inside a kernel
+// (attention: 4 warp 0's first batch of keys consumed, 5 warp 0's keys done,
+// 6 the chunk record written; the one-pass MLP: 4 its activations summed).
 constexpr int kChainStamps = 8;
 
 // Polls of the side-work flag before the QKV kernel falls back to waiting

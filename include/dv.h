@@ -257,7 +257,9 @@ int dv_layer_decode_persistent(const dv_layer_desc *desc, const dv_layer_weights
  *     writes for each of its CTAs c (first batch tile)
  *     stamps[(k * G + c) * 8 + i]: i = 0 the CTA starts, 1 its inputs are
  *     ready, 2 it ends, 3 the SM it ran on (%smid); 4 .. 7 points inside a
- *     kernel (the one-pass MLP: 4 its activations summed).  The tensor-core kernels (binary16 layers from 3 batch rows)
+ *     kernel (attention: 4 warp 0's first batch of keys consumed, 5 warp
+ *     0's keys done, 6 the chunk record written; the one-pass MLP: 4 its
+ *     activations summed).  The tensor-core kernels (binary16 layers from 3 batch rows)
  *     record nothing.
  *   persistent != 0: n_stamps >= 32 G; stamps[c * 32 + i] for CTA c at
  *     fixed points: its consumer warps: 0 start, 1 first predictor stage

@@ -82,7 +82,18 @@ dv_status check_weights(const dv_layer_weights *w)
 
 bool ptr_ok(const void *p) { return p && aligned16(p); }
 
-dv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DV_OK : DV_ERR_CUDA; }
+thread_local int t_cuda_error = 0;  // the CUDA error behind this thread's last DV_ERR_CUDA
+
+// e failed: keep it for dv_cuda_error.
+bool failed(cudaError_t e)
+{
+    if (e == cudaSuccess)
+        return false;
+    t_cuda_error = (int)e;
+    return true;
+}
+
+dv_status cuda_status(cudaError_t e) { return failed(e) ? DV_ERR_CUDA : DV_OK; }
 
 struct Launch {
     cudaStream_t st;
@@ -175,6 +186,9 @@ bool use_mma(const dv_layer_desc &D, int B)
     return D.dtype == DV_F16 && B >= kMmaMinBatch && D.d_model % 32 == 0;
 }
 
+// Kernel launches of the fused (chained) decode.
+int layer_launches(const dv_layer_desc &, int) { return kLayerLaunches; }
+
 // Fills the tensor-core fields of a; returns its dynamic shared memory.
 size_t set_mma(RowArgs &a, const dv_layer_desc &D, void *ws, const WsLayout &L)
 {
@@ -228,8 +242,8 @@ dv_status run_scores(const dv_layer_desc &D, const dv_layer_weights &w, const fl
     dv_status s = lc.mark();
     if (s)
         return s;
-    if (launch_rowdot(RK_PRED1, D.dtype, nb, a, grid, rowdot_smem(RK_PRED1, nb, d), lc.st,
-                           lc.pdl && pdl_first) != cudaSuccess)
+    if (failed(launch_rowdot(RK_PRED1, D.dtype, nb, a, grid, rowdot_smem(RK_PRED1, nb, d), lc.st,
+                           lc.pdl && pdl_first)))
         return DV_ERR_CUDA;
 
     RowArgs b2;
@@ -257,8 +271,8 @@ dv_status run_scores(const dv_layer_desc &D, const dv_layer_weights &w, const fl
     grid = dim3(lc.nsm, ceil_div(B, nb));
     if ((s = lc.mark()))
         return s;
-    if (launch_rowdot(RK_PRED2, D.dtype, nb, b2, grid, rowdot_smem(RK_PRED2, nb, r), lc.st,
-                           lc.pdl) != cudaSuccess)
+    if (failed(launch_rowdot(RK_PRED2, D.dtype, nb, b2, grid, rowdot_smem(RK_PRED2, nb, r), lc.st,
+                           lc.pdl)))
         return DV_ERR_CUDA;
     return DV_OK;
 }
@@ -328,12 +342,10 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
         size_t sm = set_mma(a, D, ws, L);
         if (ns && select_final_smem(D.d_ffn) > sm)
             sm = select_final_smem(D.d_ffn);
-        if (launch_rowdot_mma(RK_QKV, a, dim3(lc.nsm, ceil_div(B, 8)), sm, lc.st,
-                              lc.pdl && !first) !=
-            cudaSuccess)
+        if (failed(launch_rowdot_mma(RK_QKV, a, dim3(lc.nsm, ceil_div(B, 8)), sm, lc.st,
+                              lc.pdl && !first)))
             return DV_ERR_CUDA;
-    } else if (launch_rowdot(RK_QKV, D.dtype, nb, a, grid, smem, lc.st, lc.pdl && !first) !=
-               cudaSuccess) {
+    } else if (failed(launch_rowdot(RK_QKV, D.dtype, nb, a, grid, smem, lc.st, lc.pdl && !first))) {
         return DV_ERR_CUDA;
     }
 
@@ -368,7 +380,7 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     const int lpk = (int)((size_t)dh * esize(D.dtype) / 16);
     if ((s = lc.mark()))
         return s;
-    if (launch_attn(D.dtype, lpk, t, dim3(lc.nsm), lc.st, lc.pdl) != cudaSuccess)
+    if (failed(launch_attn(D.dtype, lpk, t, dim3(lc.nsm), lc.st, lc.pdl)))
         return DV_ERR_CUDA;
 
     ColArgs c;
@@ -395,11 +407,10 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
         return s;
     if (use_mma(D, B)) {
         const int nt = colacc_mma_tiles(B);
-        if (launch_colacc_mma(CK_OPROJ, nt, c, dim3(lc.nsm, ceil_div(B, 8 * nt)), lc.st, lc.pdl) !=
-            cudaSuccess)
+        if (failed(launch_colacc_mma(CK_OPROJ, nt, c, dim3(lc.nsm, ceil_div(B, 8 * nt)), lc.st, lc.pdl)))
             return DV_ERR_CUDA;
-    } else if (launch_colacc(CK_OPROJ, D.dtype, nb, c, dim3(lc.nsm, ceil_div(B, nb)), lc.st,
-                             lc.pdl) != cudaSuccess) {
+    } else if (failed(launch_colacc(CK_OPROJ, D.dtype, nb, c, dim3(lc.nsm, ceil_div(B, nb)), lc.st,
+                             lc.pdl))) {
         return DV_ERR_CUDA;
     }
     return DV_OK;
@@ -449,11 +460,11 @@ dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float
         dv_status s = lc.mark();
         if (s)
             return s;
-        if (launch_mlp(D.dtype, m, lc.nsm, lc.st, lc.pdl && !first) != cudaSuccess)
+        if (failed(launch_mlp(D.dtype, m, lc.nsm, lc.st, lc.pdl && !first)))
             return DV_ERR_CUDA;
         if ((s = lc.mark()))
             return s;
-        if (launch_part_sum(D.dtype, ps, lc.st) != cudaSuccess)
+        if (failed(launch_part_sum(D.dtype, ps, lc.st)))
             return DV_ERR_CUDA;
         return DV_OK;
     }
@@ -487,12 +498,11 @@ dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float
         return s;
     if (use_mma(D, B)) {
         const size_t sm = set_mma(a, D, ws, L);
-        if (launch_rowdot_mma(RK_FC1, a, dim3(lc.nsm, ceil_div(B, 8)), sm, lc.st,
-                              lc.pdl && !first) !=
-            cudaSuccess)
+        if (failed(launch_rowdot_mma(RK_FC1, a, dim3(lc.nsm, ceil_div(B, 8)), sm, lc.st,
+                              lc.pdl && !first)))
             return DV_ERR_CUDA;
-    } else if (launch_rowdot(RK_FC1, D.dtype, nb, a, dim3(lc.nsm, ceil_div(B, nb)),
-                             rowdot_smem(RK_FC1, nb, d), lc.st, lc.pdl && !first) != cudaSuccess) {
+    } else if (failed(launch_rowdot(RK_FC1, D.dtype, nb, a, dim3(lc.nsm, ceil_div(B, nb)),
+                             rowdot_smem(RK_FC1, nb, d), lc.st, lc.pdl && !first))) {
         return DV_ERR_CUDA;
     }
 
@@ -520,11 +530,10 @@ dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float
         return s;
     if (use_mma(D, B)) {
         const int nt = colacc_mma_tiles(B);
-        if (launch_colacc_mma(CK_FC2, nt, c, dim3(lc.nsm, ceil_div(B, 8 * nt)), lc.st, lc.pdl) !=
-            cudaSuccess)
+        if (failed(launch_colacc_mma(CK_FC2, nt, c, dim3(lc.nsm, ceil_div(B, 8 * nt)), lc.st, lc.pdl)))
             return DV_ERR_CUDA;
-    } else if (launch_colacc(CK_FC2, D.dtype, nb, c, dim3(lc.nsm, ceil_div(B, nb)), lc.st,
-                             lc.pdl) != cudaSuccess) {
+    } else if (failed(launch_colacc(CK_FC2, D.dtype, nb, c, dim3(lc.nsm, ceil_div(B, nb)), lc.st,
+                             lc.pdl))) {
         return DV_ERR_CUDA;
     }
     return DV_OK;
@@ -714,14 +723,14 @@ dv_status layer_decode_impl(const dv_layer_desc *desc, const dv_layer_weights *w
     if (!ptr_ok(x) || (x_pred && !ptr_ok(x_pred)) || !ptr_ok(y) || (h1 && !ptr_ok(h1)) ||
         !ptr_ok(kc) || !ptr_ok(vc) || !sel_ok(sel))
         return DV_ERR_INVALID_ARG;
-    if (events && n_events < kLayerLaunches + 1)
-        return DV_ERR_INVALID_ARG;
     WsLayout L;
     if ((s = check_ws(D, batch, ws, ws_bytes, &L)))
         return s;
     Launch lc;
     if ((s = make_launch(stream, events, n_events, &lc)))
         return s;
+    if (events && n_events < layer_launches(D, batch) + 1)
+        return DV_ERR_INVALID_ARG;
     lc.pdl = !use_mma(D, batch);
     float *h1p = h1 ? h1 : at<float>(ws, L.h1);
     const int max_u_h = batch * k_heads < D.n_heads ? batch * k_heads : D.n_heads;
@@ -755,7 +764,7 @@ dv_status layer_decode_impl(const dv_layer_desc *desc, const dv_layer_weights *w
                                    vc, kv_len, *sel, h1p, y, ws, L, lc, &served, stamps, n_stamps);
         if (s)
             return s;
-        return served ? cuda_status(cudaGetLastError()) : DV_ERR_UNSUPPORTED;
+        return served ? DV_OK : DV_ERR_UNSUPPORTED;
     }
     if ((s = run_scores(D, *w, x_pred ? x_pred : x, batch, nullptr, nullptr, ws, L, lc, &side,
                         pdl_first)))
@@ -767,7 +776,7 @@ dv_status layer_decode_impl(const dv_layer_desc *desc, const dv_layer_weights *w
         return s;
     if ((s = lc.mark()))
         return s;
-    return cuda_status(cudaGetLastError());
+    return DV_OK;
 }
 
 }  // namespace
@@ -854,6 +863,18 @@ bool ws_layout(const dv_layer_desc &D, int B, WsLayout *L)
 
 extern "C" {
 
+// Every launch's own return code is checked where it is made; the entry
+// points do not end with cudaGetLastError(), whose per-thread slot the
+// process shares with every other user of the same CUDA runtime library (an
+// error another component left there is not this call's).  The error behind
+// the last DV_ERR_CUDA of this thread is kept in t_cuda_error instead.
+int dv_cuda_error(void)
+{
+    const int e = t_cuda_error;
+    t_cuda_error = 0;
+    return e;
+}
+
 const char *dv_status_string(int status)
 {
     switch (status) {
@@ -894,7 +915,7 @@ int dv_check(void *ws, size_t ws_bytes, void *stream)
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < 256)
         return DV_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (cudaStreamSynchronize(st) != cudaSuccess)
+    if (failed(cudaStreamSynchronize(st)))
         return DV_ERR_CUDA;
     int v = 0;
     if (cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
@@ -908,7 +929,7 @@ int dv_layer_decode_launches(const dv_layer_desc *desc, int batch)
 {
     if (check_desc(desc) != DV_OK || batch < 1 || batch > DV_MAX_BATCH)
         return 0;
-    return kLayerLaunches;
+    return layer_launches(*desc, batch);
 }
 
 int dv_mlp_one_pass(const dv_layer_desc *desc, int batch, int max_u_n)
@@ -965,9 +986,9 @@ int dv_predict_topk(const dv_layer_desc *desc, const dv_layer_weights *w, const 
     sa.u_h = sel->u_h;
     sa.n_u_h = sel->n_u_h;
     sa.ns = make_neuron_sel(D, batch, k_neurons, *sel, ws, L);
-    if (launch_select(sa, lc.nsm, lc.st) != cudaSuccess)
+    if (failed(launch_select(sa, lc.nsm, lc.st)))
         return DV_ERR_CUDA;
-    return cuda_status(cudaGetLastError());
+    return DV_OK;
 }
 
 int dv_sparse_attn(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x, int batch,
@@ -994,7 +1015,7 @@ int dv_sparse_attn(const dv_layer_desc *desc, const dv_layer_weights *w, const f
     if ((s = run_attn(D, *w, x, batch, u_h, n_u_h, max_u_h, k_cache, v_cache, kv_len, h1, ws, L,
                       lc, true, nullptr)))
         return s;
-    return cuda_status(cudaGetLastError());
+    return DV_OK;
 }
 
 int dv_sparse_mlp(const dv_layer_desc *desc, const dv_layer_weights *w, const float *h1, int batch,
@@ -1019,7 +1040,7 @@ int dv_sparse_mlp(const dv_layer_desc *desc, const dv_layer_weights *w, const fl
     lc.pdl = !use_mma(D, batch);
     if ((s = run_mlp(D, *w, h1, batch, u_n, n_u_n, max_u_n, y, ws, L, lc, true)))
         return s;
-    return cuda_status(cudaGetLastError());
+    return DV_OK;
 }
 
 int dv_layer_decode_presel(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x,
@@ -1052,7 +1073,7 @@ int dv_layer_decode_presel(const dv_layer_desc *desc, const dv_layer_weights *w,
         return s;
     if ((s = run_mlp(D, *w, h1p, batch, u_n, n_u_n, max_u_n, y, ws, L, lc, false)))
         return s;
-    return cuda_status(cudaGetLastError());
+    return DV_OK;
 }
 
 int dv_layer_decode(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x,
@@ -1272,7 +1293,7 @@ unsigned long long current_context_id()
 dv_status noalloc_base(void **out)
 {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
+    if (failed(cudaGetDevice(&dev)))
         return DV_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices)
         return DV_ERR_UNSUPPORTED;
@@ -1336,9 +1357,9 @@ int dv_predict_topk_noalloc(const dv_layer_desc *desc, const dv_layer_weights *w
     sa.u_h = sel->u_h;
     sa.n_u_h = sel->n_u_h;
     sa.ns = make_neuron_sel(D, batch, k_neurons, *sel, ws, L);
-    if (launch_select(sa, lc.nsm, lc.st) != cudaSuccess)
+    if (failed(launch_select(sa, lc.nsm, lc.st)))
         return DV_ERR_CUDA;
-    return cuda_status(cudaGetLastError());
+    return DV_OK;
 }
 
 }  // extern "C"

@@ -77,9 +77,12 @@ cudaError_t launch_attn(int dtype, int lanes_per_key, const AttnArgs &a, dim3 gr
 
 cudaError_t launch_copy(void *dst, const void *src, size_t n16, int grid, cudaStream_t st)
 {
-    k_copy<<<grid, kThreads, 0, st>>>(static_cast<uint4 *>(dst), static_cast<const uint4 *>(src),
-                                      n16);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = st;
+    return cudaLaunchKernelEx(&cfg, k_copy, static_cast<uint4 *>(dst),
+                              static_cast<const uint4 *>(src), n16);
 }
 
 }  // namespace dv

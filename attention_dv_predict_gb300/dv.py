@@ -57,6 +57,7 @@ _S = C.POINTER(Selection)
 
 _SIGS = {
     "dv_status_string": ([_I], C.c_char_p),
+    "dv_cuda_error": ([], _I),
     "dv_abi_version": ([], _I),
     "dv_workspace_size": ([_D, _I], _SZ),
     "dv_workspace_init": ([_P, _SZ, _P], _I),
@@ -92,9 +93,11 @@ EXPORTED = tuple(_SIGS)
 
 
 class DvError(RuntimeError):
-    def __init__(self, fn: str, status: int):
+    def __init__(self, fn: str, status: int, cuda_error: int = 0):
         self.status = status
-        super().__init__(f"{fn}: {status_string(status)} ({status})")
+        self.cuda_error = cuda_error
+        extra = f", cudaError {cuda_error}" if cuda_error else ""
+        super().__init__(f"{fn}: {status_string(status)} ({status}{extra})")
 
 
 def status_string(status: int) -> str:
@@ -106,6 +109,8 @@ def abi_version() -> int:
 
 
 def _check(fn: str, status: int):
+    if status == DV_ERR_CUDA:
+        raise DvError(fn, status, int(_lib.dv_cuda_error()))
     if status != DV_OK:
         raise DvError(fn, status)
 

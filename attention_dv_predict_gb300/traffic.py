@@ -105,13 +105,15 @@ def kernel_bytes(d_model: int, n_heads: int, head_dim: int, d_ffn: int, pred_ran
     uh, un = n_u_heads, n_u_neurons
     fc1 = P * un * (d + 1) + P * 2 * d + 4 * B * (d + un)
     fc2 = P * un * d + P * d + 4 * B * (2 * d + un)
+    pred2 = P * N * r + 4 * B * r + 4 * B * N
+    qkv = (P * 3 * uh * dh * (d + 1) + P * 2 * d + 4 * B * d + 4 * B * uh * dh
+           + P * 2 * B * uh * dh)
     return {
         "mlp": P * un * (2 * d + 1) + P * 3 * d + 4 * B * 2 * d,
         "mlp_reduce": 4 * B * d * (n_parts + 2) + P * d,
         "pred_stage1": P * (H + r) * d + 4 * B * d + 4 * B * (H + r),
-        "pred_stage2": P * N * r + 4 * B * r + 4 * B * N,
-        "qkv": P * 3 * uh * dh * (d + 1) + P * 2 * d + 4 * B * d + 4 * B * uh * dh
-        + P * 2 * B * uh * dh,
+        "pred_stage2": pred2,
+        "qkv": qkv,
         "attn": P * 2 * B * uh * (kv_len + 1) * dh + 4 * 2 * B * uh * dh,
         "oproj": P * uh * dh * d + P * d + 4 * B * (2 * d + uh * dh),
         "fc1": fc1,

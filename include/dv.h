@@ -113,6 +113,10 @@ typedef struct {
 /* Static description of a status code (never NULL). */
 const char *dv_status_string(int status);
 
+/* The CUDA runtime's error code behind the last DV_ERR_CUDA returned on
+ * this host thread (reading it clears it; 0 if none).  Diagnostic. */
+int dv_cuda_error(void);
+
 /* DV_ABI_VERSION of the built library. */
 int dv_abi_version(void);
 

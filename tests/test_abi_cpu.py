@@ -76,6 +76,8 @@ def test_workspace_size_validates_desc(dv):
     assert dv.workspace_size(dv.make_desc(256, 8, 32, 1024, 32, dv.DV_F32, 0), 1) == 0
     assert dv.workspace_size(dv.make_desc(256, 8, 32, 1024, 32, dv.DV_F32, 65, ln_eps=0.0), 1) == 0
     assert dv.dv_layer_decode_launches(good, 1) == 7
+    assert dv.dv_layer_decode_launches(good, 3) == 7
+    assert dv.dv_layer_decode_launches(good, 0) == 0
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="fake-pointer checks run only without a GPU")

@@ -236,6 +236,19 @@ def test_invalid_arguments_launch_nothing(dv):
     assert torch.all(y == 7.0)
 
 
+def test_shared_memory_opt_in_per_kernel_variant(dv):
+    # a binary32 decode first, then a binary16 one whose stage-2 + QKV kernel
+    # needs more than the 48 KB of shared memory a kernel gets without
+    # opting in (the neuron selection's buffers at N = 36864): each kernel
+    # variant must make its own opt-in
+    tiny = make_case(CFG["tiny"], B=1, seed=30)
+    check_layer_parity(tiny, run_gpu_layer(dv, tiny))
+    wide = dv_inputs.LayerConfig("wideN", 264, 6, 64, 36864, 40, 37, 1, "f16",
+                                 dv_inputs.Fraction(1, 20), k_heads_fixed=3)
+    case = make_case(wide, B=1, seed=31)
+    check_layer_parity(case, run_gpu_layer(dv, case))
+
+
 # ---------------------------------------------------------------------------
 # OPT shapes at full size (inputs generated by torch's device RNG, copied to
 # the host for the oracle)

@@ -65,10 +65,16 @@ class LayerConfig:
     zipf_exponent: float = 0.0
     norm: str = "layernorm"
     ln_eps: float = 1e-5
+    neuron_block: int = 0  # 0: neurons selected one by one; > 1: contiguous blocks
+    mlp: str = "relu"      # "relu" (fc1, ReLU, fc2) or "swiglu" (gate, up, down)
 
     @property
     def k_neurons(self) -> int:
-        return keep_count(self.frac_neurons, self.d_ffn)
+        # blocked selection keeps whole blocks: the count rounded up to one
+        k = keep_count(self.frac_neurons, self.d_ffn)
+        if self.neuron_block > 1:
+            k = -(-k // self.neuron_block) * self.neuron_block
+        return k
 
     @property
     def k_heads(self) -> int:
@@ -99,6 +105,11 @@ CONFIGS: Dict[str, LayerConfig] = {
     # OPT-175B shape, keep 5% neurons (2458) / 20 heads, Zipf-skewed scores
     "opt175b": LayerConfig("opt175b", 12288, 96, 128, 49152, 1000, 2048, 1, "f16",
                            Fraction(1, 20), Fraction(1, 5), zipf_exponent=1.0),
+    # the OPT-175B shape with neurons kept in blocks of 64 contiguous channels
+    # (5% of 768 blocks, rounded up: 39 blocks = 2496 neurons)
+    "opt175b_blk64": LayerConfig("opt175b_blk64", 12288, 96, 128, 49152, 1000, 2048, 1,
+                                 "f16", Fraction(1, 20), Fraction(1, 5), zipf_exponent=1.0,
+                                 neuron_block=64),
 }
 
 # The 24-layer OPT-175B-shaped stack reuses the opt175b layer shape.

@@ -32,7 +32,8 @@ WEIGHT_FIELDS = ("ln1_g", "ln1_b", "w_qkv", "b_qkv", "w_oT", "b_o", "ln2_g", "ln
 class Desc(C.Structure):
     _fields_ = [("d_model", C.c_int), ("n_heads", C.c_int), ("head_dim", C.c_int),
                 ("d_ffn", C.c_int), ("pred_rank", C.c_int), ("dtype", C.c_int),
-                ("norm", C.c_int), ("eps", C.c_double), ("kv_cap", C.c_int)]
+                ("norm", C.c_int), ("eps", C.c_double), ("kv_cap", C.c_int),
+                ("neuron_block", C.c_int), ("mlp", C.c_int)]
 
 
 class Weights(C.Structure):
@@ -52,6 +53,7 @@ def _load(path: str):
     L.dvo_norm_row.argtypes = [C.POINTER(Desc), _F64P, _P, _P, _F64P]
     L.dvo_norm_row.restype = None
     L.dvo_topk.argtypes = [_F32P, C.c_int, C.c_int, _I32P]
+    L.dvo_block_topk.argtypes = [_F32P, C.c_int, C.c_int, C.c_int, _I32P]
     L.dvo_union.argtypes = [_I32P, C.c_int, C.c_int, C.c_int, _I32P, _I32P]
     L.dvo_predict.argtypes = [C.POINTER(Desc), C.POINTER(Weights), _F32P, C.c_int, C.c_int,
                               C.c_int, _F32P, _F32P, _I32P, _I32P, _I32P, _I32P, _I32P, _I32P]
@@ -68,7 +70,7 @@ def _load(path: str):
                                    _I32P, _I32P, _I32P, _I32P, _I32P, _F64P, _F64P]
     L.dvo_set_threads.argtypes = [C.c_int]
     L.dvo_set_threads.restype = C.c_int
-    for f in ("dvo_topk", "dvo_union", "dvo_predict", "dvo_sparse_attn", "dvo_sparse_mlp",
+    for f in ("dvo_topk", "dvo_block_topk", "dvo_union", "dvo_predict", "dvo_sparse_attn", "dvo_sparse_mlp",
               "dvo_layer", "dvo_dense_layer", "dvo_layer_decode"):
         getattr(L, f).restype = C.c_int
     return L
@@ -109,9 +111,12 @@ def _storage_dtype(dtype: int):
 
 
 def make_desc(d_model, n_heads, head_dim, d_ffn, pred_rank, dtype, kv_cap,
-              norm: int = 0, eps: float = 1e-5) -> Desc:
-    """dtype: 0 binary32 storage, 1 binary16 storage; norm: 0 LayerNorm, 1 RMSNorm."""
-    return Desc(d_model, n_heads, head_dim, d_ffn, pred_rank, dtype, norm, eps, kv_cap)
+              norm: int = 0, eps: float = 1e-5, neuron_block: int = 0, mlp: int = 0) -> Desc:
+    """dtype: 0 binary32 storage, 1 binary16 storage; norm: 0 LayerNorm, 1 RMSNorm;
+    neuron_block: 0/1 neurons one by one, > 1 blocks of that many; mlp: 0 ReLU
+    fc1/fc2, 1 SwiGLU."""
+    return Desc(d_model, n_heads, head_dim, d_ffn, pred_rank, dtype, norm, eps, kv_cap,
+                neuron_block, mlp)
 
 
 def desc_from_config(cfg, kv_cap: Optional[int] = None) -> Desc:
@@ -119,7 +124,8 @@ def desc_from_config(cfg, kv_cap: Optional[int] = None) -> Desc:
     cap = cfg.kv_len + 1 if kv_cap is None else kv_cap
     return make_desc(cfg.d_model, cfg.n_heads, cfg.head_dim, cfg.d_ffn, cfg.pred_rank,
                      0 if cfg.dtype == "f32" else 1, cap,
-                     0 if cfg.norm == "layernorm" else 1, cfg.ln_eps)
+                     0 if cfg.norm == "layernorm" else 1, cfg.ln_eps,
+                     getattr(cfg, "neuron_block", 0), 1 if getattr(cfg, "mlp", "relu") == "swiglu" else 0)
 
 
 class _W:
@@ -162,6 +168,15 @@ def topk(scores: np.ndarray, k: int) -> np.ndarray:
     s = np.ascontiguousarray(scores, dtype=np.float32)
     out = np.empty(k, np.int32)
     _rc(lib().dvo_topk(_ptr(s, _F32P), s.size, k, _ptr(out, _I32P)), "dvo_topk")
+    return out
+
+
+def block_topk(scores: np.ndarray, block: int, k: int) -> np.ndarray:
+    """The neurons of the k / block best blocks (block score: the largest member score)."""
+    s = np.ascontiguousarray(scores, dtype=np.float32)
+    out = np.empty(k, np.int32)
+    _rc(lib().dvo_block_topk(_ptr(s, _F32P), s.size, block, k, _ptr(out, _I32P)),
+        "dvo_block_topk")
     return out
 
 

@@ -117,6 +117,8 @@ typedef struct {
     int norm;   /* 0: LayerNorm, 1: RMSNorm */
     double eps;
     int kv_cap; /* KV positions per (batch row, head) */
+    int neuron_block; /* 0 or 1: neurons selected one by one; > 1: in blocks */
+    int mlp;          /* 0: fc1, ReLU, fc2; 1: SwiGLU (gate, up, down) */
 } dvo_desc;
 
 typedef struct {
@@ -145,7 +147,9 @@ static int desc_ok(const dvo_desc *D)
 {
     return D && D->d_model > 0 && D->n_heads > 0 && D->head_dim > 0 && D->d_ffn > 0 &&
            D->pred_rank > 0 && (D->dtype == 0 || D->dtype == 1) &&
-           (D->norm == 0 || D->norm == 1) && D->kv_cap > 0;
+           (D->norm == 0 || D->norm == 1) && D->kv_cap > 0 && D->neuron_block >= 0 &&
+           (D->neuron_block <= 1 || D->d_ffn % D->neuron_block == 0) &&
+           (D->mlp == 0 || D->mlp == 1);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -216,6 +220,42 @@ int dvo_topk(const float *scores, int n, int k, int32_t *out_idx)
     return 0;
 }
 
+/* Blocked top-k ("DejaVu Guide: Contextual Sparsity for LLM Inference",    */
+/* "Core Innovation 2", "1. Blocked Channel Sparsity": neurons are kept in   */
+/* contiguous blocks of 32 or 64 channels, and a block holding highly active */
+/* neurons is loaded whole).  Reading: a block's score is the largest score  */
+/* of its members.  The k / block best blocks are taken as dvo_topk takes    */
+/* scores (ties to the lower block); their neurons are returned ascending.   */
+int dvo_block_topk(const float *scores, int n, int block, int k, int32_t *out_idx)
+{
+    if (!scores || !out_idx || block < 1 || n <= 0 || n % block || k < 1 || k > n ||
+        k % block)
+        return 1;
+    const int nb = n / block, kb = k / block;
+    float *bs = (float *)malloc((size_t)nb * sizeof(float));
+    int32_t *bi = (int32_t *)malloc((size_t)kb * sizeof(int32_t));
+    if (!bs || !bi) {
+        free(bs);
+        free(bi);
+        return 2;
+    }
+    for (int j = 0; j < nb; ++j) {
+        float m = scores[(size_t)j * block];
+        for (int i = 1; i < block; ++i)
+            if (scores[(size_t)j * block + i] > m)
+                m = scores[(size_t)j * block + i];
+        bs[j] = m;
+    }
+    int rc = dvo_topk(bs, nb, kb, bi);
+    if (!rc)
+        for (int q = 0; q < kb; ++q)
+            for (int i = 0; i < block; ++i)
+                out_idx[(size_t)q * block + i] = bi[q] * block + i;
+    free(bs);
+    free(bi);
+    return rc;
+}
+
 /* union of B ascending index rows (each of length k) over [0, n): ascending */
 int dvo_union(const int32_t *idx, int B, int k, int n, int32_t *out, int32_t *n_out)
 {
@@ -282,8 +322,11 @@ int dvo_predict(const dvo_desc *D, const dvo_weights *W, const float *x_pred, in
                 acc += u[q] * ld(W->pred_b, t, (size_t)j * r + q);
             s_n[(size_t)b * N + j] = (float)acc;
         }
+        const int blk = D->neuron_block > 1 ? D->neuron_block : 1;
         if (dvo_topk(s_h + (size_t)b * H, H, k_h, idx_h + (size_t)b * k_h) ||
-            dvo_topk(s_n + (size_t)b * N, N, k_n, idx_n + (size_t)b * k_n)) {
+            (blk == 1 ? dvo_topk(s_n + (size_t)b * N, N, k_n, idx_n + (size_t)b * k_n)
+                      : dvo_block_topk(s_n + (size_t)b * N, N, blk, k_n,
+                                       idx_n + (size_t)b * k_n))) {
             free(u);
             return 2;
         }

@@ -65,7 +65,20 @@ dv_status check_desc(const dv_layer_desc *D)
     if ((long long)3 * D->n_heads * dh > (1 << 24) || D->d_ffn > (1 << 24) ||
         (long long)D->kv_cap * dh > (1LL << 31) / 4)
         return DV_ERR_UNSUPPORTED;
+    if (D->neuron_block < 0 || D->mlp < DV_MLP_RELU || D->mlp > DV_MLP_SWIGLU)
+        return DV_ERR_INVALID_ARG;
+    if (D->neuron_block > 1 &&
+        (D->neuron_block % 32 || D->d_ffn % D->neuron_block || D->d_ffn / D->neuron_block > kTopkCand))
+        return DV_ERR_UNSUPPORTED;
+    if (D->mlp == DV_MLP_SWIGLU)
+        return DV_ERR_UNSUPPORTED;
     return DV_OK;
+}
+
+// The neuron keep count in whole blocks when the layer selects blocks.
+bool k_neurons_ok(const dv_layer_desc &D, int kn)
+{
+    return kn >= 1 && kn <= D.d_ffn && (D.neuron_block <= 1 || kn % D.neuron_block == 0);
 }
 
 dv_status check_weights(const dv_layer_weights *w)
@@ -176,6 +189,7 @@ NeuronSel make_neuron_sel(const dv_layer_desc &D, int B, int kn, const dv_select
     ns.u_n = sel.u_n;
     ns.n_u_n = sel.n_u_n;
     ns.status = at<int>(ws, L.ctl);
+    ns.block = D.neuron_block > 1 ? D.neuron_block : 0;
     return ns;
 }
 
@@ -562,7 +576,7 @@ bool stream_plan(const dv_layer_desc &D, int B, int k_h, int k_n, int kv_len, in
                  StreamArgs *a, int *ni, size_t *smem)
 {
     if (D.dtype != DV_F16 || D.head_dim != 128 || B < 1 || B > 2 || G < 2 ||
-        G > kStreamMaxCtas)
+        G > kStreamMaxCtas || D.neuron_block > 1 || D.mlp != DV_MLP_RELU)
         return false;
     const int d = D.d_model, cpr = d / 8;
     const int nseg = ceil_div(cpr, kStreamUnitBytes / 16);
@@ -718,7 +732,7 @@ dv_status layer_decode_impl(const dv_layer_desc *desc, const dv_layer_weights *w
         return s;
     const dv_layer_desc &D = *desc;
     if (batch < 1 || batch > DV_MAX_BATCH || k_heads < 1 || k_heads > D.n_heads ||
-        k_neurons < 1 || k_neurons > D.d_ffn || kv_len < 0 || kv_len >= D.kv_cap)
+        !k_neurons_ok(D, k_neurons) || kv_len < 0 || kv_len >= D.kv_cap)
         return DV_ERR_INVALID_ARG;
     if (!ptr_ok(x) || (x_pred && !ptr_ok(x_pred)) || !ptr_ok(y) || (h1 && !ptr_ok(h1)) ||
         !ptr_ok(kc) || !ptr_ok(vc) || !sel_ok(sel))
@@ -966,7 +980,7 @@ int dv_predict_topk(const dv_layer_desc *desc, const dv_layer_weights *w, const 
         return DV_ERR_INVALID_ARG;
     const dv_layer_desc &D = *desc;
     if (batch < 1 || batch > DV_MAX_BATCH || k_heads < 1 || k_heads > D.n_heads ||
-        k_neurons < 1 || k_neurons > D.d_ffn || !ptr_ok(x_pred) || !sel_ok(sel))
+        !k_neurons_ok(D, k_neurons) || !ptr_ok(x_pred) || !sel_ok(sel))
         return DV_ERR_INVALID_ARG;
     WsLayout L;
     if ((s = check_ws(D, batch, ws, ws_bytes, &L)))
@@ -1331,7 +1345,7 @@ int dv_predict_topk_noalloc(const dv_layer_desc *desc, const dv_layer_weights *w
         return DV_ERR_INVALID_ARG;
     const dv_layer_desc &D = *desc;
     if (batch < 1 || batch > DV_MAX_BATCH || k_heads < 1 || k_heads > D.n_heads ||
-        k_neurons < 1 || k_neurons > D.d_ffn || !ptr_ok(x_pred) || !sel_ok(sel))
+        !k_neurons_ok(D, k_neurons) || !ptr_ok(x_pred) || !sel_ok(sel))
         return DV_ERR_INVALID_ARG;
     WsLayout L;
     size_t zero_bytes = 0;

@@ -71,6 +71,7 @@ struct NeuronSel {
     int32_t *idx_n;        // [B][k] outputs
     int32_t *u_n, *n_u_n;
     int *status;
+    int block;             // > 1: blocks of this many contiguous neurons (block_select)
 };
 
 struct SelectArgs {

@@ -19,6 +19,8 @@ __global__ void __launch_bounds__(kThreads) k_select_pass(const SelectArgs a)
     if (blockIdx.x == 0 && threadIdx.x < 32)
         head_select(a.s_h, a.ns.B, a.H, a.k_h, hbits, hsel, true, a.idx_h, a.u_h, a.n_u_h,
                     threadIdx.x);
+    if (a.ns.block > 1)  // the final kernel selects the blocks
+        return;
     const int W = (a.ns.N + 31) >> 5;
     const int w0 = (int)((long long)W * blockIdx.x / gridDim.x);
     const int w1 = (int)((long long)W * (blockIdx.x + 1) / gridDim.x);
@@ -31,7 +33,10 @@ __global__ void __launch_bounds__(kThreads) k_select_final(const SelectArgs a)
     __shared__ int fscr[48];
     pdl_wait();
     pdl_launch_dependents();
-    neuron_final(a.ns, final_smem(fsm, a.ns.N, fscr));
+    if (a.ns.block > 1)
+        block_select(a.ns, final_smem(fsm, a.ns.N, fscr));
+    else
+        neuron_final(a.ns, final_smem(fsm, a.ns.N, fscr));
 }
 
 }  // namespace

@@ -409,6 +409,63 @@ DV_DEV void neuron_final(const NeuronSel &ns, const FinalSmem &sm)
     neuron_union_out<Grp>(ns, sm);
 }
 
+// Blocked selection (ns.block > 1: blocks of ns.block contiguous neurons, a
+// multiple of 32; "DejaVu Guide ...", "Core Innovation 2", "1. Blocked
+// Channel Sparsity"): a block's score is the largest score of its members;
+// every row keeps its k / block best blocks, ties to the lower block, ranked
+// exactly by counting the blocks that beat each one (a block stops counting
+// once k / block others beat it).  Writes idx_n, u_n, n_u_n and leaves the
+// histogram and candidate counts zero.  One whole CTA; smem as FinalSmem
+// (ckey holds the block scores).
+template <class Grp = CtaGroup>
+DV_DEV void block_select(const NeuronSel &ns, const FinalSmem &sm)
+{
+    const int tid = threadIdx.x, nt = Grp::size();
+    const int W = (ns.N + 31) >> 5, nb = ns.N / ns.block, kb = ns.k / ns.block;
+    const int wpb = ns.block >> 5;  // bitmap words per block
+    float *bm = reinterpret_cast<float *>(sm.ckey);
+    for (int i = tid; i < W; i += nt)
+        sm.ubits[i] = 0u;
+    for (int b = 0; b < ns.B; ++b) {
+        const float *s = ns.s_n + (size_t)b * ns.N;
+        for (int j = tid; j < nb; j += nt) {
+            const float *p = s + (size_t)j * ns.block;
+            float m = ld_cg(p);
+            for (int i = 1; i < ns.block; ++i) {
+                const float v = ld_cg(p + i);
+                m = v > m ? v : m;
+            }
+            bm[j] = m;
+        }
+        for (int i = tid; i < W; i += nt)
+            sm.rowbits[i] = 0u;
+        Grp::sync();
+        for (int j = tid; j < nb; j += nt) {
+            const float v = bm[j];
+            int r = 0;
+            for (int q = 0; q < nb && r < kb; ++q) {
+                const float w = bm[q];
+                r += (w > v || (w == v && q < j)) ? 1 : 0;
+            }
+            if (r < kb)
+                for (int t = 0; t < wpb; ++t)
+                    sm.rowbits[j * wpb + t] = 0xffffffffu;
+        }
+        Grp::sync();
+        for (int i = tid; i < W; i += nt)
+            sm.ubits[i] |= sm.rowbits[i];
+        block_compact_bits<Grp>(sm.rowbits, W, ns.idx_n + (size_t)b * ns.k, sm.scr);
+        // the scores' histogram is not used here: leave it zero for the next call
+        int *ghist = ns.hist + (size_t)b * kTopkBins;
+        for (int i = tid; i < kTopkBins; i += nt)
+            ghist[i] = 0;
+        if (tid == 0)
+            ns.cand_cnt[b] = 0;
+        Grp::sync();
+    }
+    neuron_union_out<Grp>(ns, sm);
+}
+
 // The whole neuron selection in one CTA: for every row, the bin of the k-th
 // key from the global histogram, one pass over the row's scores into
 // shared-memory bitmaps and candidates, then the finish.  Leaves the global
@@ -418,6 +475,10 @@ DV_DEV void neuron_final(const NeuronSel &ns, const FinalSmem &sm)
 // system is busy.
 static __device__ __noinline__ void neuron_select_cta(const NeuronSel &ns, const FinalSmem &sm)
 {
+    if (ns.block > 1) {
+        block_select(ns, sm);
+        return;
+    }
     const int tid = threadIdx.x, nt = blockDim.x;
     const int W = (ns.N + 31) >> 5;
     const int G = (ns.N + 3) >> 2;  // groups of 4 scores

@@ -28,6 +28,7 @@ DV_OK, DV_ERR_INVALID_ARG, DV_ERR_UNSUPPORTED, DV_ERR_CUDA = 0, 1, 2, 3
 DV_ERR_TIMEOUT, DV_ERR_WORKSPACE, DV_ERR_DEVICE_INDEX, DV_ERR_SCRATCH_LIMIT = 4, 5, 6, 7
 DV_F32, DV_F16 = 0, 1
 DV_LAYERNORM, DV_RMSNORM = 0, 1
+DV_MLP_RELU, DV_MLP_SWIGLU = 0, 1
 DV_MAX_BATCH = 32
 
 WEIGHT_FIELDS = ("ln1_g", "ln1_b", "w_qkv", "b_qkv", "w_oT", "b_o", "ln2_g", "ln2_b",
@@ -37,7 +38,8 @@ WEIGHT_FIELDS = ("ln1_g", "ln1_b", "w_qkv", "b_qkv", "w_oT", "b_o", "ln2_g", "ln
 class LayerDesc(C.Structure):
     _fields_ = [("d_model", C.c_int32), ("n_heads", C.c_int32), ("head_dim", C.c_int32),
                 ("d_ffn", C.c_int32), ("pred_rank", C.c_int32), ("dtype", C.c_int32),
-                ("norm", C.c_int32), ("ln_eps", C.c_float), ("kv_cap", C.c_int32)]
+                ("norm", C.c_int32), ("ln_eps", C.c_float), ("kv_cap", C.c_int32),
+                ("neuron_block", C.c_int32), ("mlp", C.c_int32)]
 
 
 class LayerWeights(C.Structure):
@@ -130,8 +132,9 @@ def _stream(stream: Optional[torch.cuda.Stream]):
 
 
 def make_desc(d_model, n_heads, head_dim, d_ffn, pred_rank, dtype, kv_cap,
-              norm=DV_LAYERNORM, ln_eps=1e-5) -> LayerDesc:
-    return LayerDesc(d_model, n_heads, head_dim, d_ffn, pred_rank, dtype, norm, ln_eps, kv_cap)
+              norm=DV_LAYERNORM, ln_eps=1e-5, neuron_block=0, mlp=0) -> LayerDesc:
+    return LayerDesc(d_model, n_heads, head_dim, d_ffn, pred_rank, dtype, norm, ln_eps, kv_cap,
+                     neuron_block, mlp)
 
 
 def desc_from_config(cfg, kv_cap: Optional[int] = None) -> LayerDesc:
@@ -139,7 +142,9 @@ def desc_from_config(cfg, kv_cap: Optional[int] = None) -> LayerDesc:
     cap = cfg.kv_len + 1 if kv_cap is None else kv_cap
     return make_desc(cfg.d_model, cfg.n_heads, cfg.head_dim, cfg.d_ffn, cfg.pred_rank,
                      DV_F32 if cfg.dtype == "f32" else DV_F16, cap,
-                     DV_LAYERNORM if cfg.norm == "layernorm" else DV_RMSNORM, cfg.ln_eps)
+                     DV_LAYERNORM if cfg.norm == "layernorm" else DV_RMSNORM, cfg.ln_eps,
+                     getattr(cfg, "neuron_block", 0),
+                     1 if getattr(cfg, "mlp", "relu") == "swiglu" else 0)
 
 
 class Layer:

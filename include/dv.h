@@ -59,7 +59,7 @@
 extern "C" {
 #endif
 
-#define DV_ABI_VERSION 1
+#define DV_ABI_VERSION 2
 #define DV_MAX_BATCH 32
 
 typedef enum {
@@ -75,6 +75,10 @@ typedef enum {
 
 typedef enum { DV_F32 = 0, DV_F16 = 1 } dv_dtype;
 typedef enum { DV_LAYERNORM = 0, DV_RMSNORM = 1 } dv_norm;
+/* MLP of the layer: OPT's fc1, ReLU, fc2 (w1 [N, d], w2T [N, d]) or the
+ * LLaMA-style SwiGLU (gate and up rows of neuron j interleaved in w1
+ * [N, 2, d], b1 [N, 2]; down-projection columns in w2T [N, d]). */
+typedef enum { DV_MLP_RELU = 0, DV_MLP_SWIGLU = 1 } dv_mlp;
 
 /* Shape and storage of one layer. */
 typedef struct {
@@ -87,6 +91,15 @@ typedef struct {
     int32_t norm;       /* dv_norm used before attention and before the MLP */
     float ln_eps;
     int32_t kv_cap;     /* KV positions per (batch row, head) */
+    /* 0 or 1: neurons are selected one by one.  32, 64, ... (a multiple of
+     * 32 dividing d_ffn, at most 4096 blocks): neurons are selected in blocks
+     * of that many contiguous channels ("DejaVu Guide ...", "Core Innovation
+     * 2", "1. Blocked Channel Sparsity"): a block's score is the largest
+     * score of its members, each row keeps its k_neurons / neuron_block best
+     * blocks (ties to the lower block), and k_neurons must be a multiple of
+     * neuron_block. */
+    int32_t neuron_block;
+    int32_t mlp;        /* dv_mlp */
 } dv_layer_desc;
 
 /* Device pointers to one layer's weights (shapes in the header comment). */

@@ -66,6 +66,29 @@ def check_topk_rows(gpu_idx, ora_idx, ora_scores, k, what):
     return n_diff
 
 
+def check_block_rows(gpu_idx, ora_idx, ora_scores, block, k, what):
+    """Blocked selection, per row: k entries forming whole aligned blocks,
+    sorted; blocks differing from the oracle's only inside the tie band of
+    the block scores (each block's largest member score)."""
+    gpu_idx = np.asarray(gpu_idx)
+    n_diff = 0
+    for b in range(gpu_idx.shape[0]):
+        g = gpu_idx[b]
+        assert g.size == k and np.all(np.diff(g) > 0), f"{what} row {b}: not sorted/unique"
+        gb = g.reshape(-1, block)
+        assert np.all(gb[:, 0] % block == 0) and np.all(gb == gb[:, :1] + np.arange(block)), \
+            f"{what} row {b}: not whole blocks"
+        bs = np.asarray(ora_scores[b], np.float64).reshape(-1, block).max(axis=1)
+        kb = k // block
+        sk = np.sort(bs)[::-1][kb - 1]
+        band = TIE_REL * max(abs(sk), 1e-6)
+        diff = np.setxor1d(gb[:, 0] // block, np.asarray(ora_idx[b]).reshape(-1, block)[:, 0] // block)
+        n_diff += diff.size
+        bad = diff[np.abs(bs[diff] - sk) > band]
+        assert bad.size == 0, f"{what} row {b}: {bad.size} blocks outside the tie band"
+    return n_diff
+
+
 @dataclasses.dataclass
 class Case:
     cfg: dv_inputs.LayerConfig
@@ -131,7 +154,11 @@ def check_layer_parity(case: Case, g, tight: bool = False):
     xp = case.x if case.x_pred is None else case.x_pred
     p = oracle.predict(D, case.w_host, xp, case.k_h, case.k_n)
     nd_h = check_topk_rows(g["idx_h"], p["idx_h"], p["s_h"], case.k_h, "heads")
-    nd_n = check_topk_rows(g["idx_n"], p["idx_n"], p["s_n"], case.k_n, "neurons")
+    blk = getattr(case.cfg, "neuron_block", 0)
+    if blk > 1:
+        nd_n = check_block_rows(g["idx_n"], p["idx_n"], p["s_n"], blk, case.k_n, "neuron blocks")
+    else:
+        nd_n = check_topk_rows(g["idx_n"], p["idx_n"], p["s_n"], case.k_n, "neurons")
     assert np.array_equal(g["u_h"], np.unique(g["idx_h"]))
     assert np.array_equal(g["u_n"], np.unique(g["idx_n"]))
     # the oracle layer on the (validated) GPU index set

@@ -57,7 +57,7 @@ def test_struct_layouts_match_header(dv, tmp_path):
 
 
 def test_status_strings_and_version(dv):
-    assert dv.abi_version() == 1
+    assert dv.abi_version() == 2
     for s in range(0, 8):
         assert len(dv.status_string(s)) > 0
     assert dv.status_string(0) == "ok"

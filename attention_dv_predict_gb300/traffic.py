@@ -64,21 +64,24 @@ class StepBytes:
 
 def sparse_step_bytes(d_model: int, n_heads: int, head_dim: int, d_ffn: int, pred_rank: int,
                       p_bytes: int, batch: int, n_u_heads: int, n_u_neurons: int,
-                      kv_len: int) -> StepBytes:
+                      kv_len: int, swiglu: bool = False) -> StepBytes:
     """Algorithmic bytes of one sparse layer decode over the given unions.
 
     KV is stored in the weight type; attention reads kv_len + 1 positions
     (the cached ones and the new one) per batch row and selected head.
+    swiglu: the MLP has three matrices (gate and up in fc1's place, two rows
+    and two biases per neuron).
     """
     d, H, dh, N, r, P, B = d_model, n_heads, head_dim, d_ffn, pred_rank, p_bytes, batch
     uh, un = n_u_heads, n_u_neurons
     predictor = P * (H * d + r * d + N * r)
     qkv = P * 3 * uh * dh * d
     oproj = P * uh * dh * d
-    fc1 = P * un * d
+    m1 = 2 if swiglu else 1
+    fc1 = P * m1 * un * d
     fc2 = P * un * d
     kv_read = P * 2 * B * uh * (kv_len + 1) * dh
-    biases = P * (3 * uh * dh + un + 2 * d)
+    biases = P * (3 * uh * dh + m1 * un + 2 * d)
     norms = P * 4 * d
     acts = 4 * B * d * 2          # x in, y out (float32)
     kv_write = P * 2 * B * uh * dh
@@ -86,10 +89,10 @@ def sparse_step_bytes(d_model: int, n_heads: int, head_dim: int, d_ffn: int, pre
 
 
 def dense_step_bytes(d_model: int, n_heads: int, head_dim: int, d_ffn: int, p_bytes: int,
-                     batch: int, kv_len: int) -> int:
+                     batch: int, kv_len: int, swiglu: bool = False) -> int:
     """Bytes of the same layer decoded densely (no predictor, every head and neuron)."""
     b = sparse_step_bytes(d_model, n_heads, head_dim, d_ffn, 0, p_bytes, batch, n_heads, d_ffn,
-                          kv_len)
+                          kv_len, swiglu)
     return b.total - b.predictor
 
 

@@ -447,6 +447,52 @@ def extras(args, dv, traffic, cfg, desc, layers, caches, x, sel, ws, stream, ran
                              "achieved_gbs": round(dense_bytes / (dense_us * 1e-6) / 1e9, 1),
                              "note": "same library, every head and neuron selected"}
 
+    # blocked neuron selection (64-channel blocks, k rounded up to whole
+    # blocks) on the same weights, timed like the step (graph replays)
+    if cfg.d_ffn % 64 == 0 and B <= 2:
+        blk = 64
+        k_nb = -(-k_n // blk) * blk
+        bdesc = dv.make_desc(cfg.d_model, cfg.n_heads, cfg.head_dim, cfg.d_ffn, cfg.pred_rank,
+                             desc.dtype, desc.kv_cap, desc.norm, desc.ln_eps, neuron_block=blk)
+        blayers = [dv.Layer(bdesc, l.weights) for l in layers]
+        bsel = dv.SelectionBuffers(bdesc, B, k_h, k_nb)
+        yb = torch.empty_like(x)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for i in range(copies):  # warm, outside the capture
+                kc, vc = caches[i]
+                dv.dv_layer_decode(blayers[i], x, k_h, k_nb, kc, vc, cfg.kv_len, bsel, yb, ws,
+                                   stream=stream)
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(copies):
+                    kc, vc = caches[i]
+                    dv.dv_layer_decode(blayers[i], x, k_h, k_nb, kc, vc, cfg.kv_len, bsel, yb, ws,
+                                       stream=stream)
+            g.replay()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            reps = 10
+            a.record(stream)
+            for _ in range(reps):
+                g.replay()
+            b.record(stream)
+        b.synchronize()
+        if dv.dv_check(ws, stream) != dv.DV_OK:
+            raise RuntimeError("device status set by the blocked decode")
+        blk_us = a.elapsed_time(b) * 1e3 / (reps * copies)
+        bu_h, bu_n = bsel.unions()
+        bbytes = traffic.sparse_step_bytes(cfg.d_model, cfg.n_heads, cfg.head_dim, cfg.d_ffn,
+                                           cfg.pred_rank, 2 if cfg.dtype == "f16" else 4, B,
+                                           int(bu_h.numel()), int(bu_n.numel()), cfg.kv_len).total
+        out["blocked_selection"] = {
+            "block": blk, "k_neurons": k_nb, "union_neurons": int(bu_n.numel()),
+            "us_per_decode": round(blk_us, 2),
+            "achieved_gbs": round(bbytes / (blk_us * 1e-6) / 1e9, 1),
+            "required_bytes_per_step": bbytes,
+            "note": "neurons kept in 64-channel blocks (each scored by its largest member "
+                    "score), same weights, graph replays of consecutive decodes"}
+        del g, blayers
+
     # copy bandwidth of the library's own copy kernel (read + write bytes)
     n = 1 << 30
     src = torch.empty(n, dtype=torch.uint8, device=x.device)

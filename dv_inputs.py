@@ -105,6 +105,14 @@ CONFIGS: Dict[str, LayerConfig] = {
     # OPT-175B shape, keep 5% neurons (2458) / 20 heads, Zipf-skewed scores
     "opt175b": LayerConfig("opt175b", 12288, 96, 128, 49152, 1000, 2048, 1, "f16",
                            Fraction(1, 20), Fraction(1, 5), zipf_exponent=1.0),
+    # LLaMA-style layers (RMSNorm, SwiGLU MLP): a tiny one, and the LLaMA-3-70B
+    # shape the guide's traffic arithmetic uses (d 8192, d_ffn 28672, keep 25%
+    # of the neurons and 20% of the heads; all 64 heads full width, the
+    # grouped KV heads of the real model not modelled)
+    "llama_tiny": LayerConfig("llama_tiny", 256, 8, 32, 704, 32, 64, 1, "f32",
+                              Fraction(1, 4), k_heads_fixed=2, norm="rmsnorm", mlp="swiglu"),
+    "llama3_70b": LayerConfig("llama3_70b", 8192, 64, 128, 28672, 1024, 2048, 1, "f16",
+                              Fraction(1, 4), Fraction(1, 5), norm="rmsnorm", mlp="swiglu"),
     # the OPT-175B shape with neurons kept in blocks of 64 contiguous channels
     # (5% of 768 blocks, rounded up: 39 blocks = 2496 neurons)
     "opt175b_blk64": LayerConfig("opt175b_blk64", 12288, 96, 128, 49152, 1000, 2048, 1,
@@ -148,7 +156,9 @@ def make_weights(cfg: LayerConfig, seed: int = 0, device="cpu",
     Layouts (row-major): w_qkv [3, H, dh, d]; b_qkv [3, H, dh];
     w_oT [H, dh, d] (out-projection, transposed so a head's columns are
     contiguous rows); w1 [N, d]; w2T [N, d] (fc2 transposed); pred_h [H, d];
-    pred_a [r, d]; pred_b [N, r]; norms and biases 1-D.
+    pred_a [r, d]; pred_b [N, r]; norms and biases 1-D.  SwiGLU layers
+    (cfg.mlp == "swiglu"): w1 [N, 2, d] (neuron j's gate and up rows side by
+    side), b1 [N, 2]; w2T is the down projection, transposed.
     """
     d, H, dh, N, r = cfg.d_model, cfg.n_heads, cfg.head_dim, cfg.d_ffn, cfg.pred_rank
     dt = _torch_dtype(cfg.dtype)
@@ -156,7 +166,8 @@ def make_weights(cfg: LayerConfig, seed: int = 0, device="cpu",
     shapes = {
         "ln1_g": (d,), "ln1_b": (d,), "w_qkv": (3, H, dh, d), "b_qkv": (3, H, dh),
         "w_oT": (H, dh, d), "b_o": (d,), "ln2_g": (d,), "ln2_b": (d,),
-        "w1": (N, d), "b1": (N,), "w2T": (N, d), "b2": (d,),
+        "w1": (N, 2, d) if cfg.mlp == "swiglu" else (N, d),
+        "b1": (N, 2) if cfg.mlp == "swiglu" else (N,), "w2T": (N, d), "b2": (d,),
         "pred_h": (H, d), "pred_a": (r, d), "pred_b": (N, r),
     }
     out: Dict[str, torch.Tensor] = {}

@@ -428,11 +428,41 @@ int dvo_sparse_attn(const dvo_desc *D, const dvo_weights *W, const float *x, int
 }
 
 /* ------------------------------------------------------------------------ */
+/* Activation of neuron j on the normalised input hn.                        */
+/*  ReLU MLP (OPT):  pre = b1[j] + sum_c hn[c] * W1[j][c];  a = max(0, pre)    */
+/*  SwiGLU (LLaMA-style; "DejaVu Guide ...", "Mathematical Modeling": three   */
+/*  MLP matrices, d_ffn = 8/3 d_model "in SwiGLU"): W1 holds neuron j's gate  */
+/*  row W1[j][0] and up row W1[j][1] side by side, b1[j][0..1] their biases:  */
+/*    g = b1[j][0] + sum_c hn[c] W1[j][0][c],  u = b1[j][1] + sum_c hn[c] W1[j][1][c] */
+/*    a = silu(g) * u,  silu(g) = g / (1 + exp(-g));  pre = g                 */
+/* The down projection W2T[j] is used as fc2's.                               */
+static double neuron_act(const dvo_desc *D, const dvo_weights *W, const double *hn, size_t j,
+                         double *pre)
+{
+    const int d = D->d_model, t = D->dtype;
+    if (D->mlp == 0) {
+        double acc = 0.0;
+        for (int c = 0; c < d; ++c)
+            acc += hn[c] * ld(W->w1, t, j * d + c);
+        const double p = ld(W->b1, t, j) + acc;
+        *pre = p;
+        return p > 0.0 ? p : 0.0;
+    }
+    double ag = 0.0, au = 0.0;
+    for (int c = 0; c < d; ++c) {
+        ag += hn[c] * ld(W->w1, t, (2 * j) * d + c);
+        au += hn[c] * ld(W->w1, t, (2 * j + 1) * d + c);
+    }
+    const double g = ld(W->b1, t, 2 * j) + ag, u = ld(W->b1, t, 2 * j + 1) + au;
+    *pre = g;
+    return g / (1.0 + exp(-g)) * u;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Sparse MLP block ([P1-LST] DejaVuSparseMLP.forward_sparse, R4, R5):        */
-/*   hn = norm2(h1[b])                                                        */
-/*   pre_i = b1[u_n[i]] + sum_c hn[c] * W1[u_n[i]][c];  a_i = max(0, pre_i)    */
+/*   hn = norm2(h1[b]);  a_i = activation of neuron u_n[i] (neuron_act)       */
 /*   y[b][c] = h1[b][c] + b2[c] + sum_i a_i * W2T[u_n[i]][c]                   */
-/* pre (optional) receives pre_i as [B, n_u_n].                                */
+/* pre (optional) receives the pre-activations (gate, for SwiGLU) [B, n_u_n]. */
 int dvo_sparse_mlp(const dvo_desc *D, const dvo_weights *W, const double *h1, int B,
                    const int32_t *u_n, int n_u_n, double *y, double *pre)
 {
@@ -453,14 +483,10 @@ int dvo_sparse_mlp(const dvo_desc *D, const dvo_weights *W, const double *h1, in
         dvo_norm_row(D, hb, W->ln2_g, W->ln2_b, hn);
 #pragma omp parallel for schedule(static)
         for (int i = 0; i < n_u_n; ++i) {
-            size_t j = (size_t)u_n[i];
-            double acc = 0.0;
-            for (int c = 0; c < d; ++c)
-                acc += hn[c] * ld(W->w1, t, j * d + c);
-            double p = ld(W->b1, t, j) + acc;
+            double p;
+            a[i] = neuron_act(D, W, hn, (size_t)u_n[i], &p);
             if (pre)
                 pre[(size_t)b * n_u_n + i] = p;
-            a[i] = p > 0.0 ? p : 0.0;
         }
 #pragma omp parallel for schedule(static)
         for (int c = 0; c < d; ++c) {
@@ -487,7 +513,7 @@ int dvo_layer(const dvo_desc *D, const dvo_weights *W, const float *x, int B,
 
 /* ------------------------------------------------------------------------ */
 /* Dense layer, written out on its own (no index lists): every head appends  */
-/* and attends, every neuron fires through ReLU.  Loop orders (heads, then    */
+/* and attends, every neuron fires (neuron_act).  Loop orders (heads, then    */
 /* neurons, ascending) match the sparse functions', so selecting every head   */
 /* and neuron must reproduce it bit for bit.  pre (optional): [B, N].         */
 int dvo_dense_layer(const dvo_desc *D, const dvo_weights *W, const float *x, int B,
@@ -559,13 +585,10 @@ int dvo_dense_layer(const dvo_desc *D, const dvo_weights *W, const float *x, int
         }
         dvo_norm_row(D, hb, W->ln2_g, W->ln2_b, xn);
         for (int j = 0; j < N; ++j) {
-            double acc = 0.0;
-            for (int c = 0; c < d; ++c)
-                acc += xn[c] * ld(W->w1, t, (size_t)j * d + c);
-            double p = ld(W->b1, t, j) + acc;
+            double p;
+            a[j] = neuron_act(D, W, xn, (size_t)j, &p);
             if (pre)
                 pre[(size_t)b * N + j] = p;
-            a[j] = p > 0.0 ? p : 0.0;
         }
         for (int c = 0; c < d; ++c) {
             double acc = 0.0;

@@ -70,8 +70,6 @@ dv_status check_desc(const dv_layer_desc *D)
     if (D->neuron_block > 1 &&
         (D->neuron_block % 32 || D->d_ffn % D->neuron_block || D->d_ffn / D->neuron_block > kTopkCand))
         return DV_ERR_UNSUPPORTED;
-    if (D->mlp == DV_MLP_SWIGLU)
-        return DV_ERR_UNSUPPORTED;
     return DV_OK;
 }
 
@@ -197,7 +195,9 @@ NeuronSel make_neuron_sel(const dv_layer_desc &D, int B, int kn, const dv_select
 // (out-projection, fc2) from kMmaMinBatch batch rows on.
 bool use_mma(const dv_layer_desc &D, int B)
 {
-    return D.dtype == DV_F16 && B >= kMmaMinBatch && D.d_model % 32 == 0;
+    // SwiGLU layers run on CUDA cores at every batch size
+    return D.dtype == DV_F16 && B >= kMmaMinBatch && D.d_model % 32 == 0 &&
+           D.mlp == DV_MLP_RELU;
 }
 
 // Kernel launches of the fused (chained) decode.
@@ -442,6 +442,7 @@ dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float
         // partials' sum
         MlpArgs m;
         std::memset(&m, 0, sizeof(m));
+        m.swiglu = D.mlp == DV_MLP_SWIGLU;
         m.d = d;
         m.N = N;
         m.B = B;
@@ -486,9 +487,11 @@ dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float
     RowArgs a;
     std::memset(&a, 0, sizeof(a));
     int nb = rowdot_nb(B, d, RK_FC1);
+    const int sw = D.mlp == DV_MLP_SWIGLU ? 1 : 0;
+    a.swiglu = sw;
     a.K = d;
     a.geo = rowdot_geometry(d, D.dtype, nb);
-    a.max_rows = max_u_n;
+    a.max_rows = max_u_n << sw;
     a.B = B;
     a.n_sel = n_u_n;
     a.max_sel = max_u_n;
@@ -529,9 +532,10 @@ dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float
     c.sel = u_n;
     c.sel_range = N;
     c.dh = 1;
+    c.swiglu = sw;
     c.w = w.w2T;
     c.coef = at<float>(ws, L.act);
-    c.coef_ld = max_u_n;
+    c.coef_ld = max_u_n << sw;
     c.res = h1;
     c.bias = w.b2;
     c.out = y;
@@ -820,13 +824,13 @@ bool ws_layout(const dv_layer_desc &D, int B, WsLayout *L)
     L->q = take((size_t)B * H * dh * 4);
     L->attn_part = take((size_t)B * H * splits * (kAttnRec + dh) * 4);
     L->h1 = take((size_t)B * d * 4);
-    L->act = take((size_t)B * N * 4);
+    L->act = take((size_t)B * N * 2 * 4);  // two values per neuron for SwiGLU
     L->part_pred1 = take(bp * kMaxWarps * 2 * 4);
     L->part_qkv = take(bp * kMaxWarps * 2 * 4);
     L->part_fc1 = take(bp * kMaxWarps * 2 * 4);
     L->cnt_pred1 = take(bp * (H + r > N ? H + r : N) * 4);
     L->cnt_qkv = take(bp * 3 * H * dh * 4);
-    L->cnt_fc1 = take(bp * N * 4);
+    L->cnt_fc1 = take(bp * N * 2 * 4);  // two rows per neuron for SwiGLU
     // column kernel: two partial slots per CTA, one column block each
     const size_t cb_max = (size_t)colacc_block_cols(D.dtype, 1) * 2;  // NB x block columns
     L->cpart_o = take(bp * (kMaxWarps / kWarpsPerBlock) * 2 * cb_max * 4);

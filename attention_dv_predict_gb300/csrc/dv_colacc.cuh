@@ -115,6 +115,10 @@ DV_DEV float coef_at(const ColArgs &a, int b, int i)
             }
         }
         return OO / LL;
+    } else if (a.swiglu) {  // silu(gate) * up of slot i
+        const float g = __ldcg(a.coef + (size_t)b * a.coef_ld + 2 * i);
+        const float u = __ldcg(a.coef + (size_t)b * a.coef_ld + 2 * i + 1);
+        return g / (1.f + expf(-g)) * u;
     } else {
         return __ldcg(a.coef + (size_t)b * a.coef_ld + i);
     }

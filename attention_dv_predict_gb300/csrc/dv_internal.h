@@ -126,6 +126,7 @@ constexpr int kChainStamps = 8;
 constexpr int kSideSpin = 20000;
 
 struct RowArgs {
+    int swiglu;       // FC1 of a SwiGLU layer: rows 2j, 2j + 1 are slot j's gate and up
     int K;            // row length in elements
     RowGeo geo;
     int B;            // batch rows
@@ -170,7 +171,10 @@ struct RowArgs {
 
 // Column-accumulate kernel: out[b][c] = res[b][c] + bias[c]
 //                                      + sum_i coef[b][i] * W[row(i)][c].
+// FC2 of a SwiGLU layer (swiglu): coef[b][i] = silu(g) u from the pair
+// (g, u) = act[b][2i], act[b][2i + 1].
 struct ColArgs {
+    int swiglu;
     int d;
     int B;
     const int32_t *n_sel;
@@ -229,6 +233,7 @@ struct AttnArgs {
 // the activations of its share of the neuron union and accumulates their
 // fc2 rows into part[c][b][d]; a second kernel adds the partials, h1 and b2.
 struct MlpArgs {
+    int swiglu;           // gate and up rows per neuron, act = silu(gate) * up
     int d, N, B;
     const int32_t *sel;   // u_n
     const int32_t *n_sel;

@@ -25,12 +25,13 @@ namespace {
 constexpr int kMlpU = 8;  // 16-byte chunks per lane in one fc1 segment
 
 // Dynamic shared memory: the w2T row offsets [kMlpMaxRows], staged norm(h1)
-// [NB][d], then the per-segment sums [kMlpMaxRows][kMlpMaxSeg][NB], the
-// activations [kMlpMaxRows][NB] and the neuron ids [kMlpMaxRows].
+// [NB][d], then the per-segment sums of the fc1 rows [2 kMlpMaxRows]
+// [kMlpMaxSeg][NB] (two rows per neuron for SwiGLU), the activations
+// [kMlpMaxRows][NB] and the neuron ids [kMlpMaxRows].
 __host__ __device__ constexpr size_t mlp_smem(int nb, int d)
 {
     return (size_t)kMlpMaxRows * 8 + (size_t)nb * d * 4 +
-           (size_t)kMlpMaxRows * kMlpMaxSeg * nb * 4 + (size_t)kMlpMaxRows * nb * 4 +
+           (size_t)2 * kMlpMaxRows * kMlpMaxSeg * nb * 4 + (size_t)kMlpMaxRows * nb * 4 +
            (size_t)kMlpMaxRows * 4;
 }
 
@@ -48,8 +49,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_mlp(const MlpArgs a)
     const int nsu = (cpr + 32 * U - 1) / (32 * U);
     long long *soff = reinterpret_cast<long long *>(smem);
     float *xs = smem + 2 * kMlpMaxRows;
-    float *upart = xs + (size_t)NB * d;                    // [row][seg][b]
-    float *act = upart + (size_t)kMlpMaxRows * kMlpMaxSeg * NB;  // [row][b]
+    float *upart = xs + (size_t)NB * d;                    // [fc1 row][seg][b]
+    float *act = upart + (size_t)2 * kMlpMaxRows * kMlpMaxSeg * NB;  // [neuron][b]
     int *ssel = reinterpret_cast<int *>(act + (size_t)kMlpMaxRows * NB);
     const T *W1 = static_cast<const T *>(a.w1);
     const T *W2 = static_cast<const T *>(a.w2T);
@@ -71,13 +72,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_mlp(const MlpArgs a)
         set_status(a.status, DV_ERR_INVALID_ARG);
     __syncthreads();
 
-    // fc1 units (row, segment) of this CTA, balanced over its warps
-    const int units = nr * nsu;
+    // fc1 units (row, segment) of this CTA, balanced over its warps; SwiGLU
+    // layers have two fc1 rows per neuron (gate, up), side by side in w1
+    const int sw = a.swiglu ? 1 : 0;
+    const int units = (nr << sw) * nsu;
     const int ub = units * warp / kWarpsPerBlock, ue = units * (warp + 1) / kWarpsPerBlock;
     auto load1 = [&](int u, uint4 (&v)[U]) {
         const int row = u / nsu, sg = u - row * nsu;
-        const int h = (u < ue) ? ssel[row] : -1;
-        const T *p = W1 + (size_t)(h < 0 ? 0 : h) * d;
+        const int h = (u < ue) ? ssel[row >> sw] : -1;
+        const T *p = W1 + ((size_t)(h < 0 ? 0 : h << sw) + (row & sw)) * d;
 #pragma unroll
         for (int j = 0; j < U; ++j) {
             const int c = sg * 32 * U + lane + 32 * j;
@@ -136,11 +139,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_mlp(const MlpArgs a)
     if (tid < nr * NB) {
         const int row = tid / NB, b = tid - row * NB;
         const int h = ssel[row];
-        float s = 0.f;
-        for (int sg = 0; sg < nsu; ++sg)
-            s += upart[((size_t)row * kMlpMaxSeg + sg) * NB + b];
-        const float bias = h >= 0 ? Elem<T>::load(static_cast<const T *>(a.b1), (size_t)h) : 0.f;
-        act[row * NB + b] = (h >= 0 && b < a.B) ? fmaxf(s + bias, 0.f) : 0.f;
+        const T *b1 = static_cast<const T *>(a.b1);
+        float s = 0.f, s2 = 0.f;
+        for (int sg = 0; sg < nsu; ++sg) {
+            s += upart[((size_t)(row << sw) * kMlpMaxSeg + sg) * NB + b];
+            if (sw)
+                s2 += upart[((size_t)((row << 1) + 1) * kMlpMaxSeg + sg) * NB + b];
+        }
+        float v = 0.f;
+        if (h >= 0 && b < a.B) {
+            if (sw) {  // silu(gate) * up
+                const float g = s + Elem<T>::load(b1, (size_t)2 * h);
+                const float u = s2 + Elem<T>::load(b1, (size_t)2 * h + 1);
+                v = g / (1.f + expf(-g)) * u;
+            } else {
+                v = fmaxf(s + Elem<T>::load(b1, (size_t)h), 0.f);
+            }
+        }
+        act[row * NB + b] = v;
     }
     __syncthreads();
     chain_stamp(stamps, 4);

@@ -275,9 +275,13 @@ DV_DEV RowRef row_ref(const RowArgs &a, int row, const int *ssel, int sj0, int s
                   ? (const void *)(w0 + (((size_t)r.t * a.H + r.h) * a.dh + r.e) * a.K)
                   : nullptr;
     } else {
-        r.j = row;
-        r.h = sel_at(a, row, ssel, sj0, sn);
-        r.p = (r.h >= 0 && r.h < a.sel_range) ? (const void *)(w0 + (size_t)r.h * a.K) : nullptr;
+        // FC1 (SwiGLU: rows 2j and 2j + 1 are slot j's gate and up rows)
+        r.j = row >> a.swiglu;
+        r.t = row & a.swiglu;
+        r.h = sel_at(a, r.j, ssel, sj0, sn);
+        r.p = (r.h >= 0 && r.h < a.sel_range)
+                  ? (const void *)(w0 + ((size_t)(r.h << a.swiglu) + r.t) * a.K)
+                  : nullptr;
     }
     return r;
 }
@@ -344,9 +348,12 @@ DV_DEV void finalize(const RowArgs &a, int row, const RowRef &m, const float (&a
                 cache[(((size_t)b * a.H + m.h) * a.kv_cap + a.kv_len) * a.dh + m.e] =
                     Elem<T>::from_float(v);
             }
+        } else if (a.swiglu) {  // the gate or up value; FC2 forms silu(gate) * up
+            v += Elem<T>::load(static_cast<const T *>(a.bias), (size_t)(m.h << 1) + m.t);
+            a.out0[(size_t)b * a.max_rows + row] = v;
         } else {
             v += Elem<T>::load(static_cast<const T *>(a.bias), (size_t)m.h);
-            a.out0[(size_t)b * a.max_sel + row] = fmaxf(v, 0.f);
+            a.out0[(size_t)b * a.max_rows + row] = fmaxf(v, 0.f);
         }
     }
 }
@@ -436,7 +443,7 @@ DV_DEV void rowdot_body(const RowArgs &a, int cta, int nct, const Dep &dep)
     if constexpr (KIND == RK_QKV)
         rows = min(max(ld_cg(a.n_sel), 0), a.max_sel) * 3 * a.dh;
     else if constexpr (KIND == RK_FC1)
-        rows = min(max(ld_cg(a.n_sel), 0), a.max_sel);
+        rows = min(max(ld_cg(a.n_sel), 0), a.max_sel) << a.swiglu;
     const bool seg = g.nsu > 0;
     const int units = seg ? rows * g.nsu : (rows + g.rpu - 1) / g.rpu;
     const int Wt = ncta * kWarpsPerBlock;
@@ -453,8 +460,8 @@ DV_DEV void rowdot_body(const RowArgs &a, int cta, int nct, const Dep &dep)
         if (ce > cb) {
             const int r0 = seg ? cb / g.nsu : cb * g.rpu;
             const int r1 = seg ? (ce - 1) / g.nsu : min(rows, ce * g.rpu) - 1;
-            const int j0 = (KIND == RK_QKV) ? r0 / (3 * a.dh) : r0;
-            const int j1 = (KIND == RK_QKV) ? r1 / (3 * a.dh) : r1;
+            const int j0 = (KIND == RK_QKV) ? r0 / (3 * a.dh) : r0 >> a.swiglu;
+            const int j1 = (KIND == RK_QKV) ? r1 / (3 * a.dh) : r1 >> a.swiglu;
             sj0 = j0;
             sn = min(j1 - j0 + 1, kSelStage);
         }

@@ -68,7 +68,8 @@ dv_status check_desc(const dv_layer_desc *D)
     if (D->neuron_block < 0 || D->mlp < DV_MLP_RELU || D->mlp > DV_MLP_SWIGLU)
         return DV_ERR_INVALID_ARG;
     if (D->neuron_block > 1 &&
-        (D->neuron_block % 32 || D->d_ffn % D->neuron_block || D->d_ffn / D->neuron_block > kTopkCand))
+        (D->neuron_block != 32 && D->neuron_block != 64 && D->neuron_block != 128 ||
+         D->d_ffn % D->neuron_block || D->d_ffn / D->neuron_block > kTopkCand / 2))
         return DV_ERR_UNSUPPORTED;
     return DV_OK;
 }

@@ -412,44 +412,88 @@ DV_DEV void neuron_final(const NeuronSel &ns, const FinalSmem &sm)
 // Blocked selection (ns.block > 1: blocks of ns.block contiguous neurons, a
 // multiple of 32; "DejaVu Guide ...", "Core Innovation 2", "1. Blocked
 // Channel Sparsity"): a block's score is the largest score of its members;
-// every row keeps its k / block best blocks, ties to the lower block, ranked
-// exactly by counting the blocks that beat each one (a block stops counting
-// once k / block others beat it).  Writes idx_n, u_n, n_u_n and leaves the
+// every row keeps its k / block best blocks, ties to the lower block (a
+// bitonic sort of the block keys).  Writes idx_n, u_n, n_u_n and leaves the
 // histogram and candidate counts zero.  One whole CTA; smem as FinalSmem
-// (ckey holds the block scores).
+// (cidx holds the block maxima, ckey the sort keys: at most kTopkCand / 2
+// blocks).
 template <class Grp = CtaGroup>
 DV_DEV void block_select(const NeuronSel &ns, const FinalSmem &sm)
 {
     const int tid = threadIdx.x, nt = Grp::size();
     const int W = (ns.N + 31) >> 5, nb = ns.N / ns.block, kb = ns.k / ns.block;
     const int wpb = ns.block >> 5;  // bitmap words per block
-    float *bm = reinterpret_cast<float *>(sm.ckey);
+    float *bm = reinterpret_cast<float *>(sm.cidx);  // block maxima (<= kTopkCand / 2)
     for (int i = tid; i < W; i += nt)
         sm.ubits[i] = 0u;
+    // block maxima: a warp reads 128 consecutive scores per load (a float4
+    // per lane, kScanBatch loads in flight) and reduces each block's lanes
+    // (ns.block / 4 of them, a power of two up to 32) with shuffles
+    const int lanes = ns.block >> 2, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
+    const int nch = ns.N >> 7;  // 128-score chunks (ns.N is a multiple of the block, >= 32)
     for (int b = 0; b < ns.B; ++b) {
-        const float *s = ns.s_n + (size_t)b * ns.N;
-        for (int j = tid; j < nb; j += nt) {
-            const float *p = s + (size_t)j * ns.block;
-            float m = ld_cg(p);
-            for (int i = 1; i < ns.block; ++i) {
-                const float v = ld_cg(p + i);
-                m = v > m ? v : m;
+        const float4 *s4 = reinterpret_cast<const float4 *>(ns.s_n + (size_t)b * ns.N);
+        for (int c0 = warp; c0 < nch; c0 += nw * kScanBatch) {
+            float4 v[kScanBatch];
+#pragma unroll
+            for (int u = 0; u < kScanBatch; ++u) {
+                const int c = c0 + u * nw;
+                v[u] = c < nch ? __ldcg(s4 + (size_t)c * 32 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
+#pragma unroll
+            for (int u = 0; u < kScanBatch; ++u) {
+                const int c = c0 + u * nw;
+                float m = fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w));
+                for (int off = 1; off < lanes; off <<= 1)
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+                if (c < nch && (lane & (lanes - 1)) == 0)
+                    bm[(c * 128 + lane * 4) / ns.block] = m;
+            }
+        }
+        // a row not a whole number of 128-score chunks: its last blocks one by one
+        for (int j = (nch * 128) / ns.block + tid; j < nb; j += nt) {
+            const float *p = ns.s_n + (size_t)b * ns.N + (size_t)j * ns.block;
+            float m = ld_cg(p);
+            for (int i = 1; i < ns.block; ++i)
+                m = fmaxf(m, ld_cg(p + i));
             bm[j] = m;
         }
         for (int i = tid; i < W; i += nt)
             sm.rowbits[i] = 0u;
         Grp::sync();
-        for (int j = tid; j < nb; j += nt) {
-            const float v = bm[j];
-            int r = 0;
-            for (int q = 0; q < nb && r < kb; ++q) {
-                const float w = bm[q];
-                r += (w > v || (w == v && q < j)) ? 1 : 0;
+        // the blocks in descending order of (score, then lower index first):
+        // a bitonic sort of 64-bit keys (order-preserving score bits above
+        // the complemented block index, so every key is distinct), padded
+        // with zero keys to a power of two; the first kb are kept
+        unsigned long long *key = reinterpret_cast<unsigned long long *>(sm.ckey);
+        int np = 1;
+        while (np < nb)
+            np <<= 1;
+        Grp::sync();
+        for (int j = tid; j < np; j += nt)
+            key[j] = j < nb ? ((unsigned long long)score_key(bm[j]) << 32) |
+                                  (unsigned long long)(0xffffffffu - (unsigned)j)
+                            : 0ull;
+        Grp::sync();
+        for (int size = 2; size <= np; size <<= 1)
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                for (int i = tid; i < (np >> 1); i += nt) {
+                    // pair (lo, lo + stride) of the i-th comparator
+                    const int lo = ((i / stride) * (stride << 1)) + (i % stride);
+                    const int hi = lo + stride;
+                    const bool desc = (lo & size) == 0;  // descending runs first
+                    const unsigned long long a = key[lo], c = key[hi];
+                    if ((a < c) == desc) {
+                        key[lo] = c;
+                        key[hi] = a;
+                    }
+                }
+                Grp::sync();
             }
-            if (r < kb)
-                for (int t = 0; t < wpb; ++t)
-                    sm.rowbits[j * wpb + t] = 0xffffffffu;
+        for (int q = tid; q < kb; q += nt) {
+            const int j = (int)(0xffffffffu - (unsigned)(key[q] & 0xffffffffull));
+            for (int t = 0; t < wpb; ++t)
+                sm.rowbits[j * wpb + t] = 0xffffffffu;
         }
         Grp::sync();
         for (int i = tid; i < W; i += nt)

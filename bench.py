@@ -387,8 +387,10 @@ def run_cuda(args):
     if not args.no_extras:
         line.update(extras(args, dv, traffic, cfg, desc, layers, caches, x, sel, ws, stream,
                            rank, us_per_decode, k_h, k_n, B))
+        del layers, caches
+        torch.cuda.empty_cache()
+        line["variants"] = variant_bench(dv, traffic, x.device, peak)
         if args.stack_layers > 0:
-            del layers, caches
             torch.cuda.empty_cache()
             line["stack"] = stack_bench(args, dv, traffic, cfg, x.device)
     if rank == 0:
@@ -513,6 +515,71 @@ def extras(args, dv, traffic, cfg, desc, layers, caches, x, sel, ws, stream, ran
     if rank == 0:
         out["cpu_baseline"] = cpu_baseline(cfg, layers[0], caches[0], x, k_h, k_n,
                                            args.cpu_budget_s)
+    return out
+
+
+def variant_bench(dv, traffic, device, peak):
+    """The LLaMA-style layer (RMSNorm, SwiGLU MLP) at the LLaMA-3-70B shape of
+    the guide's traffic arithmetic, batch 1, timed like the main step (graph
+    replays of consecutive decodes over 4 layer copies)."""
+    import torch
+
+    import dv_inputs
+
+    out = {}
+    cfg = dv_inputs.CONFIGS["llama3_70b"]
+    desc = dv.desc_from_config(cfg)
+    k_h, k_n, copies, B = cfg.k_heads, cfg.k_neurons, 4, 1
+    layers, caches = [], []
+    for i in range(copies):
+        layers.append(dv.Layer(desc, dv_inputs.make_weights(cfg, seed=200 + i, device=device)))
+        caches.append(dv_inputs.make_kv(cfg, B, seed=200 + i, device=device))
+    x = dv_inputs.make_x(cfg, B, seed=7, device=device)
+    y = torch.empty_like(x)
+    sel = dv.SelectionBuffers(desc, B, k_h, k_n)
+    ws = dv.Workspace(desc, B)
+    stream = torch.cuda.Stream(device=device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for i in range(copies):
+            kc, vc = caches[i]
+            dv.dv_layer_decode(layers[i], x, k_h, k_n, kc, vc, cfg.kv_len, sel, y, ws,
+                               stream=stream)
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(copies):
+                kc, vc = caches[i]
+                dv.dv_layer_decode(layers[i], x, k_h, k_n, kc, vc, cfg.kv_len, sel, y, ws,
+                                   stream=stream)
+        for _ in range(3):
+            g.replay()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        reps = 10
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+    b.synchronize()
+    if dv.dv_check(ws, stream) != dv.DV_OK:
+        raise RuntimeError("device status set by the LLaMA-style decode")
+    us = a.elapsed_time(b) * 1e3 / (reps * copies)
+    u_h, u_n = sel.unions()
+    req = traffic.sparse_step_bytes(cfg.d_model, cfg.n_heads, cfg.head_dim, cfg.d_ffn,
+                                    cfg.pred_rank, 2, B, int(u_h.numel()), int(u_n.numel()),
+                                    cfg.kv_len, swiglu=True).total
+    out["llama3_70b"] = {
+        "us_per_decode": round(us, 2), "required_bytes_per_step": req,
+        "achieved_gbs": round(req / (us * 1e-6) / 1e9, 1),
+        "roofline_frac_step": round(req / (us * 1e-6) / 1e9 / peak, 4),
+        "union": {"heads": int(u_h.numel()), "neurons": int(u_n.numel())},
+        "config": {"d_model": cfg.d_model, "n_heads": cfg.n_heads, "head_dim": cfg.head_dim,
+                   "d_ffn": cfg.d_ffn, "pred_rank": cfg.pred_rank, "kv_len": cfg.kv_len,
+                   "batch": B, "norm": cfg.norm, "mlp": cfg.mlp, "k_heads": k_h,
+                   "k_neurons": k_n},
+        "note": "LLaMA-style layer (RMSNorm, SwiGLU with gate and up rows side by side), "
+                "MHA with all 64 heads; graph replays of consecutive decodes, 4 layer copies"}
+    del g, layers, caches
+    torch.cuda.empty_cache()
     return out
 
 

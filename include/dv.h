@@ -91,8 +91,8 @@ typedef struct {
     int32_t norm;       /* dv_norm used before attention and before the MLP */
     float ln_eps;
     int32_t kv_cap;     /* KV positions per (batch row, head) */
-    /* 0 or 1: neurons are selected one by one.  32, 64, ... (a multiple of
-     * 32 dividing d_ffn, at most 4096 blocks): neurons are selected in blocks
+    /* 0 or 1: neurons are selected one by one.  32, 64 or 128 (dividing
+     * d_ffn, at most 2048 blocks): neurons are selected in blocks
      * of that many contiguous channels ("DejaVu Guide ...", "Core Innovation
      * 2", "1. Blocked Channel Sparsity"): a block's score is the largest
      * score of its members, each row keeps its k_neurons / neuron_block best

@@ -74,3 +74,16 @@ def test_predict_selects_blocks_of_the_neuron_scores():
     p1 = oracle.predict(oracle.desc_from_config(cfg.with_(neuron_block=0)), w, x, cfg.k_heads,
                         cfg.k_neurons)
     assert np.array_equal(p["idx_h"], p1["idx_h"]) and np.array_equal(p["s_n"], p1["s_n"])
+
+
+def test_selecting_every_block_equals_the_dense_layer():
+    cfg = dv_inputs.CONFIGS["tiny"].with_(neuron_block=64)
+    D = oracle.desc_from_config(cfg)
+    w = {k: v.numpy() for k, v in dv_inputs.make_weights(cfg, 6).items()}
+    kc, vc = (t.numpy() for t in dv_inputs.make_kv(cfg, 2, 6))
+    x = dv_inputs.make_x(cfg, 2, 6).numpy()
+    p = oracle.predict(D, w, x, cfg.n_heads, cfg.d_ffn)  # every head, every block
+    assert np.array_equal(p["u_n"], np.arange(cfg.d_ffn))
+    h1d, yd, _, _, _ = oracle.dense_layer(D, w, x, kc, vc, cfg.kv_len)
+    h1s, ys, _, _ = oracle.layer(D, w, x, p["u_h"], p["u_n"], kc, vc, cfg.kv_len)
+    assert np.array_equal(yd, ys) and np.array_equal(h1d, h1s)

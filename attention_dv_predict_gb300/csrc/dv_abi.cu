@@ -18,6 +18,8 @@ namespace {
 
 constexpr int kLayerLaunches = 7;
 constexpr int kSideFlagWord = 1;  // workspace control word of the side-work flag
+constexpr int kSelDoneWord = 2;   // ... CTAs done with their rows of a split neuron selection
+constexpr int kMaxSelCtas = 8;    // CTAs the fused decode's neuron selection is split over
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -110,10 +112,9 @@ dv_status cuda_status(cudaError_t e) { return failed(e) ? DV_ERR_CUDA : DV_OK; }
 struct Launch {
     cudaStream_t st;
     int nsm;
-    // chain the call's kernels by programmatic dependent launch; off for the
-    // tensor-core configuration (binary16 from kMmaMinBatch batch rows),
-    // where the chained step measured ~113 us slower per decode than plain
-    // stream order at batches 4 and 8 (and 13 us faster at batch 1)
+    // chain the call's kernels by programmatic dependent launch (see
+    // run_attn for the one boundary the tensor-core configuration keeps in
+    // stream order)
     bool pdl;
     void *const *events;  // optional trace events
     int n_events;
@@ -151,7 +152,7 @@ dv_status make_launch(void *stream, void *const *events, int n_events, Launch *L
         return DV_ERR_UNSUPPORTED;
     L->st = static_cast<cudaStream_t>(stream);
     L->nsm = nsm;
-    L->pdl = true;
+    L->pdl = true;  // see pdl_for
     L->events = events;
     L->n_events = n_events;
     L->next_event = 0;
@@ -189,11 +190,20 @@ NeuronSel make_neuron_sel(const dv_layer_desc &D, int B, int kn, const dv_select
     ns.n_u_n = sel.n_u_n;
     ns.status = at<int>(ws, L.ctl);
     ns.block = D.neuron_block > 1 ? D.neuron_block : 0;
+    ns.gubits = at<unsigned>(ws, L.sel_ubits);
+    ns.gdone = at<int>(ws, L.ctl) + kSelDoneWord;
     return ns;
 }
 
 // Binary16 layers use the tensor-core row kernel (QKV, FC1) and column kernel
 // (out-projection, fc2) from kMmaMinBatch batch rows on.
+// Programmatic dependent launch between the call's kernels: on, except for
+// the tensor-core configuration from 8 batch rows, where the chained decode
+// measured slower than stream order at OPT-175B (batch 8: 693 against 688 us;
+// batch 16: 1315 against 1288 us; batch 4 gains: 400 against 405 us).
+bool use_mma(const dv_layer_desc &D, int B);
+bool pdl_for(const dv_layer_desc &D, int B) { return !use_mma(D, B) || B < 8; }
+
 bool use_mma(const dv_layer_desc &D, int B)
 {
     // SwiGLU layers run on CUDA cores at every batch size
@@ -342,7 +352,9 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
         a.x = at<float>(ws, L.xn);
         a.norm_g = nullptr;
         a.norm_b = nullptr;
-        a.side_cta = 1;
+        // the last min(B, kMaxSelCtas) CTAs select the neurons, rows split
+        // among them (one CTA takes about 7 us per row at N = 49152)
+        a.side_cta = B < kMaxSelCtas ? B : kMaxSelCtas;
         a.ns = *ns;
         a.side_flag = ctl + kSideFlagWord;
         const size_t fs = select_final_smem(D.d_ffn);
@@ -357,8 +369,13 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
         size_t sm = set_mma(a, D, ws, L);
         if (ns && select_final_smem(D.d_ffn) > sm)
             sm = select_final_smem(D.d_ffn);
-        if (failed(launch_rowdot_mma(RK_QKV, a, dim3(lc.nsm, ceil_div(B, 8)), sm, lc.st,
-                              lc.pdl && !first)))
+        // The stage-2 predictor -> QKV boundary stays in stream order here:
+        // with it and the stage-1 -> stage-2 boundary both programmatic, the
+        // tensor-core QKV kernel's CTAs ran about 80 us longer (median 90 ->
+        // 169 us at OPT-175B, batch 4; the decode 405 -> 498 us), while either
+        // boundary alone, or every other boundary, costs nothing (every
+        // boundary but this one: 400 us).
+        if (failed(launch_rowdot_mma(RK_QKV, a, dim3(lc.nsm, ceil_div(B, 8)), sm, lc.st, false)))
             return DV_ERR_CUDA;
     } else if (failed(launch_rowdot(RK_QKV, D.dtype, nb, a, grid, smem, lc.st, lc.pdl && !first))) {
         return DV_ERR_CUDA;
@@ -748,9 +765,9 @@ dv_status layer_decode_impl(const dv_layer_desc *desc, const dv_layer_weights *w
     Launch lc;
     if ((s = make_launch(stream, events, n_events, &lc)))
         return s;
+    lc.pdl = pdl_for(D, batch);
     if (events && n_events < layer_launches(D, batch) + 1)
         return DV_ERR_INVALID_ARG;
-    lc.pdl = !use_mma(D, batch);
     float *h1p = h1 ? h1 : at<float>(ws, L.h1);
     const int max_u_h = batch * k_heads < D.n_heads ? batch * k_heads : D.n_heads;
     const int max_u_n = batch * k_neurons < D.d_ffn ? batch * k_neurons : D.d_ffn;
@@ -848,6 +865,7 @@ bool ws_layout(const dv_layer_desc &D, int B, WsLayout *L)
     L->sel_u_n = take(N * 4);
     L->sel_n_u_n = take(4);
     L->nbits = take((size_t)B * ((N + 31) / 32) * 4);
+    L->sel_ubits = take(((N + 31) / 32) * 4);
     L->cand_key = take((size_t)B * kTopkCand * 4);
     L->cand_idx = take((size_t)B * kTopkCand * 4);
     L->cand_cnt = take((size_t)B * 4);
@@ -993,7 +1011,7 @@ int dv_predict_topk(const dv_layer_desc *desc, const dv_layer_weights *w, const 
     Launch lc;
     if ((s = make_launch(stream, nullptr, 0, &lc)))
         return s;
-    lc.pdl = !use_mma(D, batch);
+    lc.pdl = pdl_for(D, batch);
     if ((s = run_scores(D, *w, x_pred, batch, scores_h, scores_n, ws, L, lc)))
         return s;
     SelectArgs sa;
@@ -1030,7 +1048,7 @@ int dv_sparse_attn(const dv_layer_desc *desc, const dv_layer_weights *w, const f
     Launch lc;
     if ((s = make_launch(stream, nullptr, 0, &lc)))
         return s;
-    lc.pdl = !use_mma(D, batch);
+    lc.pdl = pdl_for(D, batch);
     if ((s = run_attn(D, *w, x, batch, u_h, n_u_h, max_u_h, k_cache, v_cache, kv_len, h1, ws, L,
                       lc, true, nullptr)))
         return s;
@@ -1056,7 +1074,7 @@ int dv_sparse_mlp(const dv_layer_desc *desc, const dv_layer_weights *w, const fl
     Launch lc;
     if ((s = make_launch(stream, nullptr, 0, &lc)))
         return s;
-    lc.pdl = !use_mma(D, batch);
+    lc.pdl = pdl_for(D, batch);
     if ((s = run_mlp(D, *w, h1, batch, u_n, n_u_n, max_u_n, y, ws, L, lc, true)))
         return s;
     return DV_OK;
@@ -1085,7 +1103,7 @@ int dv_layer_decode_presel(const dv_layer_desc *desc, const dv_layer_weights *w,
     Launch lc;
     if ((s = make_launch(stream, nullptr, 0, &lc)))
         return s;
-    lc.pdl = !use_mma(D, batch);
+    lc.pdl = pdl_for(D, batch);
     float *h1p = h1 ? h1 : at<float>(ws, L.h1);
     if ((s = run_attn(D, *w, x, batch, u_h, n_u_h, max_u_h, k_cache, v_cache, kv_len, h1p, ws, L,
                       lc, true, nullptr)))
@@ -1266,6 +1284,7 @@ size_t noalloc_layout(const dv_layer_desc &D, int B, WsLayout *L, size_t *zero_b
     L->s_n = take((size_t)B * N * 4);
     L->part_pred1 = take(bp * kMaxWarps * 2 * 4);
     L->nbits = take((size_t)B * ((N + 31) / 32) * 4);
+    L->sel_ubits = take(((N + 31) / 32) * 4);
     L->cand_key = take((size_t)B * kTopkCand * 4);
     L->cand_idx = take((size_t)B * kTopkCand * 4);
     L->total = off;
@@ -1362,7 +1381,7 @@ int dv_predict_topk_noalloc(const dv_layer_desc *desc, const dv_layer_weights *w
     Launch lc;
     if ((s = make_launch(stream, nullptr, 0, &lc)))
         return s;
-    lc.pdl = !use_mma(D, batch);
+    lc.pdl = pdl_for(D, batch);
     if (cudaMemsetAsync(ws, 0, zero_bytes, lc.st) != cudaSuccess)
         return DV_ERR_CUDA;
     if ((s = run_scores(D, *w, x_pred, batch, scores_h, scores_n, ws, L, lc)))

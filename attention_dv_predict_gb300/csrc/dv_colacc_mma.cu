@@ -347,7 +347,9 @@ DV_DEV void colacc_mma_body(const ColArgs &a, int cta, int nct, const Dep &dep)
 template <int KIND, int NT>
 __global__ void __launch_bounds__(kThreads, 1) k_colacc_mma(const ColArgs a)
 {
-    colacc_mma_body<KIND, NT>(a, blockIdx.x, gridDim.x, PdlDep{});
+    unsigned long long *s = chain_stamps(a.stamps);
+    colacc_mma_body<KIND, NT>(a, blockIdx.x, gridDim.x, PdlDep{s});
+    chain_stamp_end(s);
 }
 
 }  // namespace

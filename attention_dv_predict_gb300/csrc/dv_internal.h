@@ -72,6 +72,8 @@ struct NeuronSel {
     int32_t *u_n, *n_u_n;
     int *status;
     int block;             // > 1: blocks of this many contiguous neurons (block_select)
+    unsigned *gubits;      // [ceil(N/32)] union of a selection split over CTAs (zero at rest)
+    int *gdone;            // CTAs done with their rows (zero at rest)
 };
 
 struct SelectArgs {
@@ -287,6 +289,7 @@ struct WsLayout {
     size_t stage_x, stage_xp, stage_y;
     size_t sel_idx_h, sel_idx_n, sel_u_h, sel_n_u_h, sel_u_n, sel_n_u_n;
     size_t nbits, cand_key, cand_idx, cand_cnt;  // neuron selection state
+    size_t sel_ubits;  // union bitmap of a selection split over CTAs
     size_t xn;  // normalised input of the attention block (fused decode)
     size_t mma_part, mma_cnt;  // tensor-core row kernel: group partials and counters
     // streaming kernel: segment sums of the predictor, QKV and fc1 rows,

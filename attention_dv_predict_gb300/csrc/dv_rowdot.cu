@@ -64,6 +64,7 @@ template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
 {
     using T = __half;
+    unsigned long long *stamps = chain_stamps(a.stamps);
     extern __shared__ __align__(16) float smem[];
     __shared__ float red[34];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -71,14 +72,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
     int ncta = gridDim.x;
     if constexpr (KIND == RK_QKV) {
         if (a.side_cta) {
-            ncta = gridDim.x - 1;
-            if (blockIdx.x == ncta) {  // the neuron selection (as in k_rowdot)
+            ncta = gridDim.x - a.side_cta;
+            if ((int)blockIdx.x >= ncta) {  // the neuron selection (as in k_rowdot)
                 pdl_wait();
+                chain_stamp(stamps, 1);
                 pdl_launch_dependents();
                 if (tile == 0) {
                     __shared__ int nscr[48];
-                    neuron_select_cta(a.ns, final_smem(smem, a.ns.N, nscr));
+                    neuron_select_cta(a.ns, final_smem(smem, a.ns.N, nscr), blockIdx.x - ncta,
+                                      a.side_cta);
                 }
+                chain_stamp_end(stamps);
                 return;
             }
         }
@@ -96,9 +100,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
             __syncthreads();
             if (!s_ready)
                 pdl_wait();
+            chain_stamp(stamps, 1);
             pdl_launch_dependents();
         } else {
             pdl_wait();
+            chain_stamp(stamps, 1);
             pdl_launch_dependents();
         }
     }
@@ -124,6 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
 
     if constexpr (KIND == RK_FC1) {  // h1 comes from the previous kernel
         pdl_wait();
+        chain_stamp(stamps, 1);
         pdl_launch_dependents();
     }
     // this segment's activations of batch rows b0 .. b0 + 7: hi and lo halves
@@ -249,6 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
                 finalize_one<T, KIND>(a, rb, mb, b0 + 2 * t + 1, acc[3]);
         }
     }
+    chain_stamp_end(stamps);
 }
 
 template <typename T, int NB, int KIND>

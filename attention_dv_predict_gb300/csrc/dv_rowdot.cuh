@@ -400,14 +400,16 @@ DV_DEV void rowdot_body(const RowArgs &a, int cta, int nct, const Dep &dep)
     }
     if constexpr (KIND == RK_QKV) {
         if (a.side_cta) {
-            ncta = nct - 1;
-            if (cta == ncta) {
-                // the last CTA selects the neurons instead: it needs the whole
-                // stage-2 grid (scores and histogram)
+            ncta = nct - a.side_cta;
+            if (cta >= ncta) {
+                // the last side_cta CTAs select the neurons instead (rows
+                // split among them): they need the whole stage-2 grid
+                // (scores and histogram)
                 dep.wait();
                 if (tile == 0) {
                     __shared__ int nscr[48];
-                    neuron_select_cta(a.ns, final_smem(smem, a.ns.N, nscr));
+                    neuron_select_cta(a.ns, final_smem(smem, a.ns.N, nscr), cta - ncta,
+                                      a.side_cta);
                 }
                 return;
             }

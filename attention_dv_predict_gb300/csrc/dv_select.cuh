@@ -418,7 +418,10 @@ DV_DEV void neuron_final(const NeuronSel &ns, const FinalSmem &sm)
 // (cidx holds the block maxima, ckey the sort keys: at most kTopkCand / 2
 // blocks).
 template <class Grp = CtaGroup>
-DV_DEV void block_select(const NeuronSel &ns, const FinalSmem &sm)
+DV_DEV void select_union_out(const NeuronSel &ns, const FinalSmem &sm, int nparts);
+
+template <class Grp = CtaGroup>
+DV_DEV void block_select(const NeuronSel &ns, const FinalSmem &sm, int part = 0, int nparts = 1)
 {
     const int tid = threadIdx.x, nt = Grp::size();
     const int W = (ns.N + 31) >> 5, nb = ns.N / ns.block, kb = ns.k / ns.block;
@@ -431,7 +434,7 @@ DV_DEV void block_select(const NeuronSel &ns, const FinalSmem &sm)
     // (ns.block / 4 of them, a power of two up to 32) with shuffles
     const int lanes = ns.block >> 2, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
     const int nch = ns.N >> 7;  // 128-score chunks (ns.N is a multiple of the block, >= 32)
-    for (int b = 0; b < ns.B; ++b) {
+    for (int b = part; b < ns.B; b += nparts) {
         const float4 *s4 = reinterpret_cast<const float4 *>(ns.s_n + (size_t)b * ns.N);
         for (int c0 = warp; c0 < nch; c0 += nw * kScanBatch) {
             float4 v[kScanBatch];
@@ -507,7 +510,45 @@ DV_DEV void block_select(const NeuronSel &ns, const FinalSmem &sm)
             ns.cand_cnt[b] = 0;
         Grp::sync();
     }
-    neuron_union_out<Grp>(ns, sm);
+    select_union_out<Grp>(ns, sm, nparts);
+}
+
+// The union of the rows after a selection split over nparts CTAs (part p
+// took rows p, p + nparts, ...): each ORs its rows' union into the global
+// bitmap ns.gubits, counts itself in *ns.gdone, and the last to arrive
+// compacts the bitmap to u_n / n_u_n and clears both for the next call.
+// nparts == 1: straight from shared memory.
+template <class Grp>
+DV_DEV void select_union_out(const NeuronSel &ns, const FinalSmem &sm, int nparts)
+{
+    if (nparts <= 1) {
+        neuron_union_out<Grp>(ns, sm);
+        return;
+    }
+    const int tid = threadIdx.x, nt = Grp::size();
+    const int W = (ns.N + 31) >> 5;
+    Grp::sync();
+    for (int i = tid; i < W; i += nt)
+        if (sm.ubits[i])
+            atomicOr(ns.gubits + i, sm.ubits[i]);
+    __threadfence();
+    Grp::sync();
+    if (tid == 0)
+        sm.scr[45] = atomicAdd(ns.gdone, 1) == nparts - 1;
+    Grp::sync();
+    if (!sm.scr[45])
+        return;
+    __threadfence();
+    for (int i = tid; i < W; i += nt)
+        sm.ubits[i] = __ldcg(ns.gubits + i);
+    Grp::sync();
+    const int tot = block_compact_bits<Grp>(sm.ubits, W, ns.u_n, sm.scr);
+    if (tid == 0)
+        *ns.n_u_n = tot;
+    for (int i = tid; i < W; i += nt)
+        ns.gubits[i] = 0u;
+    if (tid == 0)
+        *ns.gdone = 0;
 }
 
 // The whole neuron selection in one CTA: for every row, the bin of the k-th
@@ -517,10 +558,14 @@ DV_DEV void block_select(const NeuronSel &ns, const FinalSmem &sm)
 // scores per load (16 bytes when the row is 16-byte aligned) and kScanBatch
 // such groups at a time, so few requests carry the row even when the memory
 // system is busy.
-static __device__ __noinline__ void neuron_select_cta(const NeuronSel &ns, const FinalSmem &sm)
+//
+// part / nparts: this CTA takes rows part, part + nparts, ... of the batch;
+// the union is finished by select_union_out.
+static __device__ __noinline__ void neuron_select_cta(const NeuronSel &ns, const FinalSmem &sm,
+                                                      int part = 0, int nparts = 1)
 {
     if (ns.block > 1) {
-        block_select(ns, sm);
+        block_select(ns, sm, part, nparts);
         return;
     }
     const int tid = threadIdx.x, nt = blockDim.x;
@@ -529,7 +574,7 @@ static __device__ __noinline__ void neuron_select_cta(const NeuronSel &ns, const
     const bool vec = (ns.N & 3) == 0;
     for (int i = tid; i < W; i += nt)
         sm.ubits[i] = 0u;
-    for (int b = 0; b < ns.B; ++b) {
+    for (int b = part; b < ns.B; b += nparts) {
         const float *s = ns.s_n + (size_t)b * ns.N;
         // the row's histogram first (one 16-byte load per thread), then the bin
         const int4 *gh4 = reinterpret_cast<const int4 *>(ns.hist + (size_t)b * kTopkBins);
@@ -592,7 +637,7 @@ static __device__ __noinline__ void neuron_select_cta(const NeuronSel &ns, const
             ghist[i] = 0;
         __syncthreads();
     }
-    neuron_union_out(ns, sm);
+    select_union_out(ns, sm, nparts);
 }
 
 DV_DEV FinalSmem final_smem(void *base, int N, int *scr)

@@ -218,15 +218,17 @@ int layer_launches(const dv_layer_desc &, int) { return kLayerLaunches; }
 size_t set_mma(RowArgs &a, const dv_layer_desc &D, void *ws, const WsLayout &L)
 {
     int S = 1, ks = 0;
-    rowdot_mma_plan(D.d_model, &S, &ks);
+    const int nt = rowdot_mma_tiles(a.B);
+    rowdot_mma_plan(D.d_model, nt, &S, &ks);
     a.mma_seg = S;
     a.mma_ks = ks;
+    a.mma_nt = nt;
     const int rows_max = 3 * D.n_heads * D.head_dim > D.d_ffn ? 3 * D.n_heads * D.head_dim
                                                                : D.d_ffn;
     a.mma_groups = ceil_div(rows_max, 16);
     a.mma_part = at<float>(ws, L.mma_part);
     a.mma_cnt = at<int>(ws, L.mma_cnt);
-    return rowdot_mma_smem(ks);
+    return rowdot_mma_smem(ks, nt);
 }
 
 // PRED1 (head scores, low-rank factor u) and PRED2 (neuron scores +
@@ -375,7 +377,8 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
         // 169 us at OPT-175B, batch 4; the decode 405 -> 498 us), while either
         // boundary alone, or every other boundary, costs nothing (every
         // boundary but this one: 400 us).
-        if (failed(launch_rowdot_mma(RK_QKV, a, dim3(lc.nsm, ceil_div(B, 8)), sm, lc.st, false)))
+        if (failed(launch_rowdot_mma(RK_QKV, a, dim3(lc.nsm, ceil_div(B, 8 * a.mma_nt)), sm,
+                                     lc.st, false)))
             return DV_ERR_CUDA;
     } else if (failed(launch_rowdot(RK_QKV, D.dtype, nb, a, grid, smem, lc.st, lc.pdl && !first))) {
         return DV_ERR_CUDA;
@@ -533,7 +536,7 @@ dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float
         return s;
     if (use_mma(D, B)) {
         const size_t sm = set_mma(a, D, ws, L);
-        if (failed(launch_rowdot_mma(RK_FC1, a, dim3(lc.nsm, ceil_div(B, 8)), sm, lc.st,
+        if (failed(launch_rowdot_mma(RK_FC1, a, dim3(lc.nsm, ceil_div(B, 8 * a.mma_nt)), sm, lc.st,
                               lc.pdl && !first)))
             return DV_ERR_CUDA;
     } else if (failed(launch_rowdot(RK_FC1, D.dtype, nb, a, dim3(lc.nsm, ceil_div(B, nb)),
@@ -870,13 +873,14 @@ bool ws_layout(const dv_layer_desc &D, int B, WsLayout *L)
     L->cand_idx = take((size_t)B * kTopkCand * 4);
     L->cand_cnt = take((size_t)B * 4);
     L->xn = take((size_t)B * d * 4);
-    {  // tensor-core row kernel (binary16, batch tiles of 8)
+    {  // tensor-core row kernel (binary16, nt batch tiles of 8 per weight pass)
         int S = 1, ks = 0;
-        rowdot_mma_plan(D.d_model, &S, &ks);
-        const size_t tiles = (size_t)ceil_div(B, 8);
+        const int nt = rowdot_mma_tiles(B);
+        rowdot_mma_plan(D.d_model, nt, &S, &ks);
+        const size_t passes = (size_t)ceil_div(B, 8 * nt);
         const size_t groups = (size_t)ceil_div(3 * H * dh > N ? 3 * H * dh : N, 16);
-        L->mma_part = take(tiles * groups * S * 128 * 4);
-        L->mma_cnt = take(tiles * groups * 4);
+        L->mma_part = take(passes * groups * S * 128 * nt * 4);
+        L->mma_cnt = take(passes * groups * 4);
     }
     {  // streaming kernel (binary16, batches 1-2; sized for either when B <= 2)
         const size_t nseg = (size_t)ceil_div(D.d_model / 8, kStreamUnitBytes / 16);

@@ -165,6 +165,7 @@ struct RowArgs {
     // tensor-core variant (k_rowdot_mma): K segments, their length, group
     // partials [tiles][groups][segments][16][8] and arrival counters
     int mma_seg, mma_ks, mma_groups;
+    int mma_nt;       // 8-row batch tiles per weight pass (1, 2 or 4)
     float *mma_part;
     int *mma_cnt;
     int *status;
@@ -325,8 +326,9 @@ size_t rowdot_smem(int kind, int nb, int K);
 // Tensor-core row kernel (binary16 weights, batch tiles of 8; QKV and FC1).
 cudaError_t launch_rowdot_mma(int kind, const RowArgs &a, dim3 grid, size_t smem,
                               cudaStream_t st, bool pdl);
-void rowdot_mma_plan(int K, int *S, int *ks);
-size_t rowdot_mma_smem(int ks);
+void rowdot_mma_plan(int K, int nt, int *S, int *ks);
+size_t rowdot_mma_smem(int ks, int nt);
+int rowdot_mma_tiles(int B);  // batch tiles per weight pass
 constexpr int kMmaMinBatch = 3;  // batches from which binary16 layers use tensor cores
 // Tensor-core column kernel (binary16, nt batch tiles of 8 per CTA;
 // out-projection, fc2): grid.y = ceil(B / (8 nt)).

@@ -60,7 +60,7 @@ DV_DEV void finalize_one(const RowArgs &a, int row, const RowRef &m, int b, floa
     }
 }
 
-template <int KIND>
+template <int KIND, int NT>
 __global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
 {
     using T = __half;
@@ -68,7 +68,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
     extern __shared__ __align__(16) float smem[];
     __shared__ float red[34];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int tile = blockIdx.y, b0 = tile * 8;
+    // NT batch tiles of 8 rows per weight pass: every weight fragment feeds
+    // the MMAs of all of them
+    const int tile = blockIdx.y, b0 = tile * 8 * NT;
     int ncta = gridDim.x;
     if constexpr (KIND == RK_QKV) {
         if (a.side_cta) {
@@ -133,10 +135,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
         chain_stamp(stamps, 1);
         pdl_launch_dependents();
     }
-    // this segment's activations of batch rows b0 .. b0 + 7: hi and lo halves
+    // this segment's activations of batch rows b0 .. b0 + 8 NT - 1: hi and lo halves
     __half *xh = reinterpret_cast<__half *>(smem);
-    __half *xl = xh + 8 * ldx;
-    for (int bi = 0; bi < 8; ++bi) {
+    __half *xl = xh + 8 * NT * ldx;
+    for (int bi = 0; bi < 8 * NT; ++bi) {
         const int b = b0 + bi;
         if (b >= a.B) {
             for (int i = threadIdx.x; i < kn; i += blockDim.x) {
@@ -180,7 +182,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
             set_status(a.status, DV_ERR_DEVICE_INDEX);
         const T *pa = ma.p ? static_cast<const T *>(ma.p) + k0 + 8 * t : nullptr;
         const T *pb = mb.p ? static_cast<const T *>(mb.p) + k0 + 8 * t : nullptr;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        float acc[NT][4];
+#pragma unroll
+        for (int tt = 0; tt < NT; ++tt)
+            acc[tt][0] = acc[tt][1] = acc[tt][2] = acc[tt][3] = 0.f;
         uint4 wa[kMmaBK], wb[kMmaBK];
 #pragma unroll
         for (int i = 0; i < kMmaBK; ++i) {
@@ -199,12 +204,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
             for (int i = 0; i < kMmaBK; ++i) {
                 const int blk = blk0 + i;
                 if (blk < nblk) {
-                    const uint4 h4 = *reinterpret_cast<const uint4 *>(xhr + blk * 32);
-                    const uint4 l4 = *reinterpret_cast<const uint4 *>(xlr + blk * 32);
-                    mma16816(acc, wa[i].x, wb[i].x, wa[i].y, wb[i].y, h4.x, h4.y);
-                    mma16816(acc, wa[i].x, wb[i].x, wa[i].y, wb[i].y, l4.x, l4.y);
-                    mma16816(acc, wa[i].z, wb[i].z, wa[i].w, wb[i].w, h4.z, h4.w);
-                    mma16816(acc, wa[i].z, wb[i].z, wa[i].w, wb[i].w, l4.z, l4.w);
+#pragma unroll
+                    for (int tt = 0; tt < NT; ++tt) {
+                        const size_t to = (size_t)tt * 8 * ldx + blk * 32;
+                        const uint4 h4 = *reinterpret_cast<const uint4 *>(xhr + to);
+                        const uint4 l4 = *reinterpret_cast<const uint4 *>(xlr + to);
+                        mma16816(acc[tt], wa[i].x, wb[i].x, wa[i].y, wb[i].y, h4.x, h4.y);
+                        mma16816(acc[tt], wa[i].x, wb[i].x, wa[i].y, wb[i].y, l4.x, l4.y);
+                        mma16816(acc[tt], wa[i].z, wb[i].z, wa[i].w, wb[i].w, h4.z, h4.w);
+                        mma16816(acc[tt], wa[i].z, wb[i].z, wa[i].w, wb[i].w, l4.z, l4.w);
+                    }
                 }
             }
 #pragma unroll
@@ -213,13 +222,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
                 wb[i] = nb[i];
             }
         }
-        // acc: (row ra, batch 2t), (ra, 2t+1), (rb, 2t), (rb, 2t+1)
+        // acc[tt]: (row ra, batch 2t), (ra, 2t+1), (rb, 2t), (rb, 2t+1) of tile tt
         if (S > 1) {
-            float *pp = a.mma_part + (((size_t)tile * a.mma_groups + grp) * S + sgm) * 128;
-            pp[g * 8 + 2 * t] = acc[0];
-            pp[g * 8 + 2 * t + 1] = acc[1];
-            pp[(g + 8) * 8 + 2 * t] = acc[2];
-            pp[(g + 8) * 8 + 2 * t + 1] = acc[3];
+            float *pp = a.mma_part + (((size_t)tile * a.mma_groups + grp) * S + sgm) * 128 * NT;
+#pragma unroll
+            for (int tt = 0; tt < NT; ++tt) {
+                pp[tt * 128 + g * 8 + 2 * t] = acc[tt][0];
+                pp[tt * 128 + g * 8 + 2 * t + 1] = acc[tt][1];
+                pp[tt * 128 + (g + 8) * 8 + 2 * t] = acc[tt][2];
+                pp[tt * 128 + (g + 8) * 8 + 2 * t + 1] = acc[tt][3];
+            }
             __threadfence();
             int last = 0;
             int *cnt = a.mma_cnt + (size_t)tile * a.mma_groups + grp;
@@ -229,31 +241,40 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
             if (!last)
                 continue;
             __threadfence();
-            float sum[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int q = 0; q < S; ++q) {
-                const float *qp = a.mma_part + (((size_t)tile * a.mma_groups + grp) * S + q) * 128;
-                sum[0] += __ldcg(qp + g * 8 + 2 * t);
-                sum[1] += __ldcg(qp + g * 8 + 2 * t + 1);
-                sum[2] += __ldcg(qp + (g + 8) * 8 + 2 * t);
-                sum[3] += __ldcg(qp + (g + 8) * 8 + 2 * t + 1);
-            }
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                acc[i] = sum[i];
+            for (int tt = 0; tt < NT; ++tt) {
+                float sum[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int q = 0; q < S; ++q) {
+                    const float *qp = a.mma_part +
+                                      (((size_t)tile * a.mma_groups + grp) * S + q) * 128 * NT +
+                                      tt * 128;
+                    sum[0] += __ldcg(qp + g * 8 + 2 * t);
+                    sum[1] += __ldcg(qp + g * 8 + 2 * t + 1);
+                    sum[2] += __ldcg(qp + (g + 8) * 8 + 2 * t);
+                    sum[3] += __ldcg(qp + (g + 8) * 8 + 2 * t + 1);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    acc[tt][i] = sum[i];
+            }
             if (lane == 0)
                 *cnt = 0;
         }
-        if (ma.p) {
-            if (b0 + 2 * t < a.B)
-                finalize_one<T, KIND>(a, ra, ma, b0 + 2 * t, acc[0]);
-            if (b0 + 2 * t + 1 < a.B)
-                finalize_one<T, KIND>(a, ra, ma, b0 + 2 * t + 1, acc[1]);
-        }
-        if (mb.p) {
-            if (b0 + 2 * t < a.B)
-                finalize_one<T, KIND>(a, rb, mb, b0 + 2 * t, acc[2]);
-            if (b0 + 2 * t + 1 < a.B)
-                finalize_one<T, KIND>(a, rb, mb, b0 + 2 * t + 1, acc[3]);
+#pragma unroll
+        for (int tt = 0; tt < NT; ++tt) {
+            const int bt = b0 + tt * 8 + 2 * t;
+            if (ma.p) {
+                if (bt < a.B)
+                    finalize_one<T, KIND>(a, ra, ma, bt, acc[tt][0]);
+                if (bt + 1 < a.B)
+                    finalize_one<T, KIND>(a, ra, ma, bt + 1, acc[tt][1]);
+            }
+            if (mb.p) {
+                if (bt < a.B)
+                    finalize_one<T, KIND>(a, rb, mb, bt, acc[tt][2]);
+                if (bt + 1 < a.B)
+                    finalize_one<T, KIND>(a, rb, mb, bt + 1, acc[tt][3]);
+            }
         }
     }
     chain_stamp_end(stamps);
@@ -368,19 +389,42 @@ cudaError_t launch_rowdot(int kind, int dtype, int nb, const RowArgs &a, dim3 gr
     return dispatch_kind<float>(kind, nb, a, grid, smem, st, pdl);
 }
 
-cudaError_t launch_rowdot_mma(int kind, const RowArgs &a, dim3 grid, size_t smem,
-                              cudaStream_t st, bool pdl)
+namespace {
+
+template <int KIND, int NT>
+cudaError_t launch_rowdot_mma_t(const cudaLaunchConfig_t &cfg, const RowArgs &a)
 {
-    if (kind != RK_QKV && kind != RK_FC1)
-        return cudaErrorInvalidValue;
-    void (*kern)(RowArgs) = kind == RK_QKV ? k_rowdot_mma<RK_QKV> : k_rowdot_mma<RK_FC1>;
-    static DeviceOnce once[2];
-    cudaError_t e = once[kind == RK_QKV ? 0 : 1].run([&] {
+    auto kern = k_rowdot_mma<KIND, NT>;
+    static DeviceOnce once;
+    cudaError_t e = once.run([&] {
         return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)kSmemCap);
     });
     if (e != cudaSuccess)
         return e;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+template <int KIND>
+cudaError_t dispatch_nt(int nt, const cudaLaunchConfig_t &cfg, const RowArgs &a)
+{
+    switch (nt) {
+    case 1: return launch_rowdot_mma_t<KIND, 1>(cfg, a);
+    case 2: return launch_rowdot_mma_t<KIND, 2>(cfg, a);
+    case 4: return launch_rowdot_mma_t<KIND, 4>(cfg, a);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+int rowdot_mma_tiles(int B) { return B <= 8 ? 1 : (B <= 16 ? 2 : 4); }
+
+cudaError_t launch_rowdot_mma(int kind, const RowArgs &a, dim3 grid, size_t smem,
+                              cudaStream_t st, bool pdl)
+{
+    if (kind != RK_QKV && kind != RK_FC1)
+        return cudaErrorInvalidValue;
     if (smem > kSmemCap)
         return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
@@ -393,17 +437,18 @@ cudaError_t launch_rowdot_mma(int kind, const RowArgs &a, dim3 grid, size_t smem
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    const int nt = a.mma_nt;
+    return kind == RK_QKV ? dispatch_nt<RK_QKV>(nt, cfg, a) : dispatch_nt<RK_FC1>(nt, cfg, a);
 }
 
 // K segments and their length for the tensor-core variant: each segment's
-// hi/lo activations of 8 batch rows (32 bytes per k, plus padding) must fit
-// the shared-memory budget.
-void rowdot_mma_plan(int K, int *S, int *ks)
+// hi/lo activations of 8 nt batch rows (32 nt bytes per k, plus padding)
+// must fit the shared-memory budget.
+void rowdot_mma_plan(int K, int nt, int *S, int *ks)
 {
     const size_t budget = 160 * 1024;
     int s = 1;
-    while ((size_t)32 * ((size_t)(K + s - 1) / s + 32) > budget)
+    while ((size_t)32 * nt * ((size_t)(K + s - 1) / s + 32) > budget)
         ++s;
     int len = (K + s - 1) / s;
     len = (len + 31) / 32 * 32;
@@ -411,6 +456,6 @@ void rowdot_mma_plan(int K, int *S, int *ks)
     *S = (K + len - 1) / len;
 }
 
-size_t rowdot_mma_smem(int ks) { return (size_t)32 * (ks + 32); }
+size_t rowdot_mma_smem(int ks, int nt) { return (size_t)32 * nt * (ks + 32); }
 
 }  // namespace dv

@@ -269,23 +269,25 @@ def test_opt66b_full(dv, B):
         assert CFG["opt66b"].k_neurons < g["u_n"].size <= 8 * CFG["opt66b"].k_neurons
 
 
-@pytest.mark.parametrize("B", [3, 16])
+@pytest.mark.parametrize("B", [3, 16, 25, 32])
 def test_opt67b_batches_tensor_core_path(dv, B):
     # B >= 3 with binary16 weights runs QKV and fc1 on the tensor-core row
-    # kernel (one partial batch tile at B = 3, two tiles at B = 16)
+    # kernel: one partial batch tile at B = 3, two tiles per weight pass at
+    # B = 16, four (the last one partial at B = 25) at B = 25 and 32
     case = make_case(CFG["opt6.7b"], B=B, gen_device="cuda", norm_affine=True)
     g = run_gpu_layer(dv, case)
     check_layer_parity(case, g)
 
 
 # d = 4128 leaves a 32-column last block for the tensor-core column kernel
-# (512-column blocks); batches 3, 5, 11 and 25 give partial tiles of 8 and
-# one or two CTA tiles of 16 rows (two batch tiles per weight pass)
+# (512-column blocks); batches 3, 5, 11, 17 and 25 give partial tiles of 8,
+# one or two CTA tiles of 16 rows, and row-kernel passes of one, two or four
+# batch tiles (four at 17 and 25, the last ones empty or partial)
 RAGGED_MMA = dv_inputs.LayerConfig("ragged_mma", 4128, 6, 128, 3000, 64, 70, 1, "f16",
                                    dv_inputs.Fraction(1, 10), k_heads_fixed=2)
 
 
-@pytest.mark.parametrize("B", [3, 5, 11, 25])
+@pytest.mark.parametrize("B", [3, 5, 11, 17, 25])
 def test_tensor_core_paths_ragged(dv, B):
     case = make_case(RAGGED_MMA, B=B, seed=20 + B)
     g = run_gpu_layer(dv, case)

@@ -66,7 +66,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
     using T = __half;
     unsigned long long *stamps = chain_stamps(a.stamps);
     extern __shared__ __align__(16) float smem[];
-    __shared__ float red[34];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     // NT batch tiles of 8 rows per weight pass: every weight fragment feeds
     // the MMAs of all of them
@@ -135,34 +134,46 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
         chain_stamp(stamps, 1);
         pdl_launch_dependents();
     }
-    // this segment's activations of batch rows b0 .. b0 + 8 NT - 1: hi and lo halves
+    // this segment's activations of batch rows b0 .. b0 + 8 NT - 1: hi and lo
+    // halves.  The rows' statistics first (a warp per row, over the whole
+    // row), then every thread normalises and splits chunks of any row.
     __half *xh = reinterpret_cast<__half *>(smem);
     __half *xl = xh + 8 * NT * ldx;
-    for (int bi = 0; bi < 8 * NT; ++bi) {
-        const int b = b0 + bi;
-        if (b >= a.B) {
-            for (int i = threadIdx.x; i < kn; i += blockDim.x) {
-                xh[bi * ldx + i] = __float2half_rn(0.f);
-                xl[bi * ldx + i] = __float2half_rn(0.f);
+    {
+        __shared__ float2 sstat[8 * NT];
+        const bool ln = a.norm_kind == DV_LAYERNORM;
+        if (a.norm_g) {
+            for (int bi = warp; bi < 8 * NT; bi += kWarpsPerBlock) {
+                const int b = b0 + bi;
+                if (b < a.B) {
+                    const float2 st = warp_row_stats(a.x + (size_t)b * a.x_ld, K, ln, a.eps, lane);
+                    if (lane == 0)
+                        sstat[bi] = st;
+                }
             }
-            continue;
+            __syncthreads();
         }
-        norm_row<T>(a.x + (size_t)b * a.x_ld, K, a.norm_g, a.norm_b, a.norm_kind, a.eps, red,
-                    [&](int c, const float(&v)[8]) {
-                        const int kk = c * 8 - k0;
-                        if (kk < 0 || kk >= kn)
-                            return;
-                        __align__(16) __half hi[8], lo[8];
+        const int cps = kn >> 3;  // 8-element chunks of the segment per row
+        for (int i = threadIdx.x; i < 8 * NT * cps; i += blockDim.x) {
+            const int bi = i / cps, c = i - bi * cps, b = b0 + bi;
+            float v[8];
+            if (b < a.B) {
+                norm_chunk<T>(a.x + (size_t)b * a.x_ld, (k0 >> 3) + c, a.norm_g, a.norm_b, ln,
+                              a.norm_g ? sstat[bi] : make_float2(0.f, 1.f), v);
+            } else {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            hi[e] = __float2half_rn(v[e]);
-                            lo[e] = __float2half_rn(v[e] - __half2float(hi[e]));
-                        }
-                        *reinterpret_cast<uint4 *>(xh + bi * ldx + kk) =
-                            *reinterpret_cast<const uint4 *>(hi);
-                        *reinterpret_cast<uint4 *>(xl + bi * ldx + kk) =
-                            *reinterpret_cast<const uint4 *>(lo);
-                    });
+                for (int e = 0; e < 8; ++e)
+                    v[e] = 0.f;
+            }
+            __align__(16) __half hi[8], lo[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                hi[e] = __float2half_rn(v[e]);
+                lo[e] = __float2half_rn(v[e] - __half2float(hi[e]));
+            }
+            *reinterpret_cast<uint4 *>(xh + bi * ldx + 8 * c) = *reinterpret_cast<const uint4 *>(hi);
+            *reinterpret_cast<uint4 *>(xl + bi * ldx + 8 * c) = *reinterpret_cast<const uint4 *>(lo);
+        }
     }
     __syncthreads();
 

@@ -193,10 +193,100 @@ DV_DEV void norm_row(const float *src, int K, const void *g_, const void *b_, in
     }
 }
 
+// Statistics of one row src[0..K) (K a multiple of 4, 16-byte aligned) by
+// one warp: (mean, 1/sqrt(var + eps)) for LayerNorm, (0, 1/sqrt(mean of
+// squares + eps)) for RMSNorm; two passes, the row read at L2 both times.
+DV_DEV float2 warp_row_stats(const float *src, int K, bool ln, float eps, int lane)
+{
+    const float4 *s4 = reinterpret_cast<const float4 *>(src);
+    const int n4 = K >> 2;
+    float mean = 0.f;
+    if (ln) {
+        float s = 0.f;
+#pragma unroll 8
+        for (int i = lane; i < n4; i += 32) {
+            const float4 t = __ldcg(s4 + i);
+            s += (t.x + t.y) + (t.z + t.w);
+        }
+        mean = warp_sum(s) / (float)K;
+    }
+    float ss = 0.f;
+#pragma unroll 8
+    for (int i = lane; i < n4; i += 32) {
+        const float4 t = __ldcg(s4 + i);
+        const float dx = t.x - mean, dy = t.y - mean, dz = t.z - mean, dw = t.w - mean;
+        ss = fmaf(dx, dx, ss);
+        ss = fmaf(dy, dy, ss);
+        ss = fmaf(dz, dz, ss);
+        ss = fmaf(dw, dw, ss);
+    }
+    return make_float2(mean, rsqrtf(warp_sum(ss) / (float)K + eps));
+}
+
+// Normalised chunk c (EPC values from src + c EPC) with the row statistics st.
+template <typename T>
+DV_DEV void norm_chunk(const float *src, int c, const void *g_, const void *b_, bool ln, float2 st,
+                       float (&v)[Elem<T>::EPC])
+{
+    constexpr int EPC = Elem<T>::EPC;
+    const float4 *s4 = reinterpret_cast<const float4 *>(src + (size_t)c * EPC);
+#pragma unroll
+    for (int e = 0; e < EPC; e += 4) {
+        const float4 t = __ldcg(s4 + e / 4);
+        v[e] = t.x;
+        v[e + 1] = t.y;
+        v[e + 2] = t.z;
+        v[e + 3] = t.w;
+    }
+    if (g_) {
+        float g[EPC], be[EPC];
+        Elem<T>::unpack(reinterpret_cast<const uint4 *>(g_)[c], g);
+        if (ln)
+            Elem<T>::unpack(reinterpret_cast<const uint4 *>(b_)[c], be);
+#pragma unroll
+        for (int e = 0; e < EPC; ++e)
+            v[e] = (v[e] - st.x) * st.y * g[e] + (ln ? be[e] : 0.f);
+    }
+}
+
 template <typename T, int NB>
 DV_DEV void stage_acts(const RowArgs &a, float *xs, int b0, float *red)
 {
     const int K = a.K;
+    if constexpr (NB >= 4) {
+        // several rows: their statistics a warp per row, then chunks of any
+        // row by every thread
+        constexpr int EPC = Elem<T>::EPC;
+        __shared__ float2 sstat[NB];
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        const bool ln = a.norm_kind == DV_LAYERNORM;
+        if (a.norm_g) {
+            for (int bi = warp; bi < NB; bi += kWarpsPerBlock)
+                if (b0 + bi < a.B) {
+                    const float2 st =
+                        warp_row_stats(a.x + (size_t)(b0 + bi) * a.x_ld, K, ln, a.eps, lane);
+                    if (lane == 0)
+                        sstat[bi] = st;
+                }
+            __syncthreads();
+        }
+        const int cpr = K / EPC;
+        for (int i = threadIdx.x; i < NB * cpr; i += blockDim.x) {
+            const int bi = i / cpr, c = i - bi * cpr, b = b0 + bi;
+            float v[EPC];
+            if (b < a.B) {
+                norm_chunk<T>(a.x + (size_t)b * a.x_ld, c, a.norm_g, a.norm_b, ln,
+                              a.norm_g ? sstat[bi] : make_float2(0.f, 1.f), v);
+            } else {
+#pragma unroll
+                for (int e = 0; e < EPC; ++e)
+                    v[e] = 0.f;
+            }
+            stage_chunk_store<T>(xs + (size_t)bi * K, K, c, v);
+        }
+        __syncthreads();
+        return;
+    }
     for (int bi = 0; bi < NB; ++bi) {
         const int b = b0 + bi;
         float *dst = xs + (size_t)bi * K;
@@ -216,27 +306,46 @@ DV_DEV void stage_acts(const RowArgs &a, float *xs, int b0, float *red)
 // Side work of one CTA of the stage-2 predictor kernel in the fused decode:
 // select the heads (the head scores come from the previous kernel) and
 // write the attention block's normalised input xn = norm(x) to global
-// memory, both for the QKV kernel that follows.
+// memory, both for the QKV kernel that follows.  From kSideWarpRows batch
+// rows on, the rows are dealt out to the warps (below it the whole CTA
+// normalises one row after the other: a lone warp per row was slower).
+constexpr int kSideWarpRows = 4;
+
 template <typename T>
 __device__ __noinline__ void pred2_side(const RowArgs &a, float *red)
 {
-    __shared__ unsigned hbits[2 * kHeadKPL];
-    __shared__ int32_t hsel[kHeadTopkMax];
+    __shared__ unsigned wbits[kWarpsPerBlock * kHeadKPL];
+    __shared__ unsigned ubits[kHeadKPL];
     const PredSide &p = a.side;
-    if (threadIdx.x < 32)
-        head_select(p.s_h, a.B, p.H, p.k_h, hbits, hsel, true, p.idx_h, p.u_h, p.n_u_h,
-                    threadIdx.x);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const bool ln = p.norm_kind == DV_LAYERNORM;
     constexpr int EPC = Elem<T>::EPC;
-    for (int b = 0; b < a.B; ++b) {
-        float *dst = p.xn + (size_t)b * p.d;
-        norm_row<T>(p.x + (size_t)b * p.x_ld, p.d, p.g, p.beta, p.norm_kind, p.eps, red,
-                    [&](int c, const float(&v)[EPC]) {
+    if (a.B < kSideWarpRows) {
+        for (int b = 0; b < a.B; ++b) {
+            float *dst = p.xn + (size_t)b * p.d;
+            norm_row<T>(p.x + (size_t)b * p.x_ld, p.d, p.g, p.beta, p.norm_kind, p.eps, red,
+                        [&](int c, const float(&v)[EPC]) {
 #pragma unroll
-                        for (int e = 0; e < EPC; e += 4)
-                            *reinterpret_cast<float4 *>(dst + (size_t)c * EPC + e) =
-                                make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
-                    });
+                            for (int e = 0; e < EPC; e += 4)
+                                *reinterpret_cast<float4 *>(dst + (size_t)c * EPC + e) =
+                                    make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+                        });
+        }
     }
+    for (int b = warp; b < a.B && a.B >= kSideWarpRows; b += kWarpsPerBlock) {
+        const float *src = p.x + (size_t)b * p.x_ld;
+        float *dst = p.xn + (size_t)b * p.d;
+        const float2 st = p.g ? warp_row_stats(src, p.d, ln, p.eps, lane) : make_float2(0.f, 1.f);
+        for (int c = lane; c < p.d / EPC; c += 32) {
+            float v[EPC];
+            norm_chunk<T>(src, c, p.g, p.beta, ln, st, v);
+#pragma unroll
+            for (int e = 0; e < EPC; e += 4)
+                *reinterpret_cast<float4 *>(dst + (size_t)c * EPC + e) =
+                    make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+        }
+    }
+    head_select_block(p.s_h, a.B, p.H, p.k_h, wbits, ubits, p.idx_h, p.u_h, p.n_u_h);
 }
 
 // ---------------------------------------------------------------------------

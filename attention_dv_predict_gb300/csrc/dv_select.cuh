@@ -118,6 +118,35 @@ DV_DEV int head_select(const float *s_h, int B, int H, int k, unsigned *sbits, i
     return nu;
 }
 
+// Head selection of B rows by all warps of the block, the rows dealt out
+// to the warps (warp w selects rows w, w + nw, ...): per-row lists to
+// idx_h, the union (ascending) to u_h and its length to n_u_h.  wbits holds
+// kHeadKPL words per warp, ubits kHeadKPL words (shared memory).  Every
+// thread of the block calls it; barriers inside.
+DV_DEV void head_select_block(const float *s_h, int B, int H, int k, unsigned *wbits,
+                              unsigned *ubits, int32_t *idx_h, int32_t *u_h, int32_t *n_u_h)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int W = (H + 31) >> 5;
+    unsigned *rowbits = wbits + warp * kHeadKPL;
+    if ((int)threadIdx.x < kHeadKPL)
+        ubits[threadIdx.x] = 0u;
+    __syncthreads();
+    for (int b = warp; b < B; b += nw) {
+        warp_topk_bits(s_h + (size_t)b * H, H, k, rowbits, lane);
+        if (lane < W)
+            atomicOr(&ubits[lane], rowbits[lane]);
+        warp_compact_bits(rowbits, W, idx_h + (size_t)b * k, lane);
+        __syncwarp();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int nu = warp_compact_bits(ubits, W, u_h, lane);
+        if (lane == 0)
+            *n_u_h = nu;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Neuron selection (state: NeuronSel in the workspace).
 

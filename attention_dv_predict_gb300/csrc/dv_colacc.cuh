@@ -270,6 +270,8 @@ DV_DEV void colacc_body(const ColArgs &a, int cta, int nct, const Dep &dep)
                             scoef[(i + f * blockDim.x - s0) * NB + b] = cv[f][b];
             }
             __syncthreads();
+            if (pp - (i1 - i0) == p0 && s0 == i0)
+                chain_stamp(dep.stamps, 4);  // the first stage's coefficients staged
             // warp w takes rows s0 + w + 16 t; R rows per batch, two batches in flight
             const int cnt = (s1 - s0 - warp + kWarpsPerBlock - 1) / kWarpsPerBlock;
             const int nbatch = cnt > 0 ? (cnt + R - 1) / R : 0;
@@ -319,6 +321,7 @@ DV_DEV void colacc_body(const ColArgs &a, int cta, int nct, const Dep &dep)
             }
         }
 
+        chain_stamp(dep.stamps, 5);  // this piece's rows consumed
         // reduce the warps in shared memory, one batch row at a time
         const bool whole = (i0 == 0 && i1 == rows);
         const int slot = (cb == first_cb) ? 0 : 1;
@@ -372,6 +375,7 @@ DV_DEV void colacc_body(const ColArgs &a, int cta, int nct, const Dep &dep)
         __syncthreads();
         if (!s_last)
             continue;
+        chain_stamp(dep.stamps, 6);  // finishing block cb
         __threadfence();
         // the CTAs sharing block cb (each used its slot 0), in CTA order
         if (tid < 32) {

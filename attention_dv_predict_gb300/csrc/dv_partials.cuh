@@ -53,6 +53,7 @@ __global__ void __launch_bounds__(kThreads) k_part_sum(const PartSumArgs a)
             }
         }
     }
+    chain_stamp(stamps, 4);  // partials summed (thread 0's slice)
     sred[s][q] = sum;
     __syncthreads();
     if (s == 0 && in) {

@@ -614,6 +614,7 @@ DV_DEV void rowdot_body(const RowArgs &a, int cta, int nct, const Dep &dep)
         }
     }
     stage_acts<T, NB>(a, xs, b0, red);
+    chain_stamp(dep.stamps, 4);  // activations staged
 
     if (seg) {
         float acc[NB];
@@ -730,6 +731,7 @@ DV_DEV void rowdot_body(const RowArgs &a, int cta, int nct, const Dep &dep)
             r = rn;
         }
     }
+    chain_stamp(dep.stamps, 5);  // rows done
     if constexpr (KIND == RK_PRED2) {  // this CTA's scores into the first-digit histogram
         __syncthreads();
         for (int i = threadIdx.x; i < NB * kTopkBins; i += blockDim.x) {

@@ -19,6 +19,7 @@ namespace {
 constexpr int kLayerLaunches = 7;
 constexpr int kSideFlagWord = 1;  // workspace control word of the side-work flag
 constexpr int kSelDoneWord = 2;   // ... CTAs done with their rows of a split neuron selection
+constexpr int kSideDoneWord = 3;  // ... side CTAs of the stage-2 predictor done
 constexpr int kMaxSelCtas = 8;    // CTAs the fused decode's neuron selection is split over
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -214,18 +215,58 @@ bool use_mma(const dv_layer_desc &D, int B)
 // Kernel launches of the fused (chained) decode.
 int layer_launches(const dv_layer_desc &, int) { return kLayerLaunches; }
 
+// Row count the tensor-core kernel's partial slots are sized for: the
+// largest of QKV, fc1 and the stage-1 predictor.
+int mma_rows_max(const dv_layer_desc &D)
+{
+    const int qkv = 3 * D.n_heads * D.head_dim, p1 = D.n_heads + D.pred_rank;
+    const int m = qkv > D.d_ffn ? qkv : D.d_ffn;
+    return m > p1 ? m : p1;
+}
+
+// The predictor stages run on the tensor-core row kernel too when the
+// others do, from 5 batch rows, and the rank is a whole number of 16-byte
+// chunks.  Below 5 batch rows the CUDA-core kernels (4 rows per weight pass) were
+// faster (OPT-175B, batch 4: 376 against 386 us per decode); from 5 rows
+// they take 8 rows a pass and fall behind (batch 8: 604 against 573 us).
+bool pred_mma(const dv_layer_desc &D, int B)
+{
+    return use_mma(D, B) && B >= 5 && D.pred_rank % 8 == 0;
+}
+
 // Fills the tensor-core fields of a; returns its dynamic shared memory.
-size_t set_mma(RowArgs &a, const dv_layer_desc &D, void *ws, const WsLayout &L)
+// fixed_rows > 0 (the predictor stages: every row, known on the host): when
+// there are fewer 16-row groups than warps, K is cut into more segments so
+// that every warp has a (group, segment) to stream, within the partial
+// slots the workspace holds.
+size_t set_mma(RowArgs &a, const dv_layer_desc &D, void *ws, const WsLayout &L, int nsm,
+               int fixed_rows = 0)
 {
     int S = 1, ks = 0;
     const int nt = rowdot_mma_tiles(a.B);
-    rowdot_mma_plan(D.d_model, nt, &S, &ks);
+    rowdot_mma_plan(a.K, nt, &S, &ks);
+    const int groups_max = ceil_div(mma_rows_max(D), 16);
+    a.mma_groups = groups_max;
+    if (fixed_rows > 0) {
+        const int groups = ceil_div(fixed_rows, 16);
+        int s_ws = 1, ks_ws = 0;  // the segments the partial slots are sized for
+        rowdot_mma_plan(D.d_model, nt, &s_ws, &ks_ws);
+        // at most K / 128 segments, and several CTAs per segment
+        const int want = std::min(std::min(ceil_div(nsm * kWarpsPerBlock, groups), a.K / 128),
+                                  nsm / 4);
+        if (want > S) {
+            const int ks2 = ceil_div(ceil_div(a.K, want), 32) * 32;
+            const int s2 = ceil_div(a.K, ks2);
+            if ((long long)groups * s2 <= (long long)groups_max * s_ws && s2 > S) {
+                S = s2;
+                ks = ks2;
+                a.mma_groups = groups;
+            }
+        }
+    }
     a.mma_seg = S;
     a.mma_ks = ks;
     a.mma_nt = nt;
-    const int rows_max = 3 * D.n_heads * D.head_dim > D.d_ffn ? 3 * D.n_heads * D.head_dim
-                                                               : D.d_ffn;
-    a.mma_groups = ceil_div(rows_max, 16);
     a.mma_part = at<float>(ws, L.mma_part);
     a.mma_cnt = at<int>(ws, L.mma_cnt);
     return rowdot_mma_smem(ks, nt);
@@ -269,9 +310,17 @@ dv_status run_scores(const dv_layer_desc &D, const dv_layer_weights &w, const fl
     dv_status s = lc.mark();
     if (s)
         return s;
-    if (failed(launch_rowdot(RK_PRED1, D.dtype, nb, a, grid, rowdot_smem(RK_PRED1, nb, d), lc.st,
-                           lc.pdl && pdl_first)))
+    // (the no-allocation scratch has no tensor-core partial slots: CUDA cores)
+    const bool mma = pred_mma(D, B) && L.mma_cnt != 0;
+    if (mma) {
+        const size_t sm = set_mma(a, D, ws, L, lc.nsm, H + r);
+        if (failed(launch_rowdot_mma(RK_PRED1, a, dim3(lc.nsm, ceil_div(B, 8 * a.mma_nt)), sm,
+                                     lc.st, lc.pdl && pdl_first)))
+            return DV_ERR_CUDA;
+    } else if (failed(launch_rowdot(RK_PRED1, D.dtype, nb, a, grid, rowdot_smem(RK_PRED1, nb, d),
+                                  lc.st, lc.pdl && pdl_first))) {
         return DV_ERR_CUDA;
+    }
 
     RowArgs b2;
     std::memset(&b2, 0, sizeof(b2));
@@ -291,16 +340,26 @@ dv_status run_scores(const dv_layer_desc &D, const dv_layer_weights &w, const fl
     b2.status = ctl;
     b2.stamps = lc.kernel_stamps();
     if (side) {
-        b2.side_cta = 1;
+        // the tensor-core kernel splits the side work (norm(x) rows) over up
+        // to kMaxSelCtas CTAs: one CTA's L2 bandwidth took ~60 us for 8 rows
+        // of 12288 at OPT-175B
+        b2.side_cta = mma ? std::min(B, kMaxSelCtas) : 1;
         b2.side = *side;
         b2.side_flag = ctl + kSideFlagWord;
+        b2.side_done = ctl + kSideDoneWord;
     }
     grid = dim3(lc.nsm, ceil_div(B, nb));
     if ((s = lc.mark()))
         return s;
-    if (failed(launch_rowdot(RK_PRED2, D.dtype, nb, b2, grid, rowdot_smem(RK_PRED2, nb, r), lc.st,
-                           lc.pdl)))
+    if (mma) {
+        const size_t sm = set_mma(b2, D, ws, L, lc.nsm, N);
+        if (failed(launch_rowdot_mma(RK_PRED2, b2, dim3(lc.nsm, ceil_div(B, 8 * b2.mma_nt)), sm,
+                                     lc.st, lc.pdl)))
+            return DV_ERR_CUDA;
+    } else if (failed(launch_rowdot(RK_PRED2, D.dtype, nb, b2, grid, rowdot_smem(RK_PRED2, nb, r),
+                                  lc.st, lc.pdl))) {
         return DV_ERR_CUDA;
+    }
     return DV_OK;
 }
 
@@ -368,7 +427,7 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     if (s)
         return s;
     if (use_mma(D, B)) {
-        size_t sm = set_mma(a, D, ws, L);
+        size_t sm = set_mma(a, D, ws, L, lc.nsm);
         if (ns && select_final_smem(D.d_ffn) > sm)
             sm = select_final_smem(D.d_ffn);
         // The stage-2 predictor -> QKV boundary stays in stream order here:
@@ -535,7 +594,7 @@ dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float
     if (s)
         return s;
     if (use_mma(D, B)) {
-        const size_t sm = set_mma(a, D, ws, L);
+        const size_t sm = set_mma(a, D, ws, L, lc.nsm);
         if (failed(launch_rowdot_mma(RK_FC1, a, dim3(lc.nsm, ceil_div(B, 8 * a.mma_nt)), sm, lc.st,
                               lc.pdl && !first)))
             return DV_ERR_CUDA;
@@ -852,10 +911,14 @@ bool ws_layout(const dv_layer_desc &D, int B, WsLayout *L)
     L->cnt_pred1 = take(bp * (H + r > N ? H + r : N) * 4);
     L->cnt_qkv = take(bp * 3 * H * dh * 4);
     L->cnt_fc1 = take(bp * N * 2 * 4);  // two rows per neuron for SwiGLU
-    // column kernel: two partial slots per CTA, one column block each
+    // column kernel: two partial slots per CTA, one column block each, for
+    // every batch row of its passes (the tensor-core variant's last pass of
+    // 8 nt rows may run past the padded batch)
     const size_t cb_max = (size_t)colacc_block_cols(D.dtype, 1) * 2;  // NB x block columns
-    L->cpart_o = take(bp * (kMaxWarps / kWarpsPerBlock) * 2 * cb_max * 4);
-    L->cpart_2 = take(bp * (kMaxWarps / kWarpsPerBlock) * 2 * cb_max * 4);
+    const size_t cnt_t = (size_t)colacc_mma_tiles(B);
+    const size_t cbp = std::max(bp, (size_t)ceil_div(B, 8 * (int)cnt_t) * 8 * cnt_t);
+    L->cpart_o = take(cbp * (kMaxWarps / kWarpsPerBlock) * 2 * cb_max * 4);
+    L->cpart_2 = take(cbp * (kMaxWarps / kWarpsPerBlock) * 2 * cb_max * 4);
     L->ccnt_o = take(bp * S * 4);
     L->ccnt_2 = take(bp * S * 4);
     L->stage_x = take((size_t)B * d * 4);
@@ -878,7 +941,7 @@ bool ws_layout(const dv_layer_desc &D, int B, WsLayout *L)
         const int nt = rowdot_mma_tiles(B);
         rowdot_mma_plan(D.d_model, nt, &S, &ks);
         const size_t passes = (size_t)ceil_div(B, 8 * nt);
-        const size_t groups = (size_t)ceil_div(3 * H * dh > N ? 3 * H * dh : N, 16);
+        const size_t groups = (size_t)ceil_div(mma_rows_max(D), 16);
         L->mma_part = take(passes * groups * S * 128 * nt * 4);
         L->mma_cnt = take(passes * groups * 4);
     }

@@ -162,6 +162,7 @@ struct RowArgs {
     // fused decode: PRED1 clears it, PRED2's side CTA sets it once its results
     // are published; the QKV kernel starts on it instead of the grid dependency
     int *side_flag;
+    int *side_done;       // PRED2 with several side CTAs: how many have finished
     // tensor-core variant (k_rowdot_mma): K segments, their length, group
     // partials [tiles][groups][segments][16][8] and arrival counters
     int mma_seg, mma_ks, mma_groups;

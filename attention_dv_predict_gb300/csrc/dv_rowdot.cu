@@ -15,7 +15,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot(const RowArgs a)
 }
 
 // ---------------------------------------------------------------------------
-// Tensor-core variant for batch tiles of 8 rows (binary16 weights; QKV, FC1).
+// Tensor-core variant for batch tiles of 8 rows (binary16 weights; every kind).
 //
 // out[b][row] = sum_k W[row][k] x[b][k] as mma.sync m16n8k16 (f32 accumulate):
 // A = 16 weight rows x 16 k, B = 16 k x 8 batch rows.  A lane loads 16
@@ -27,7 +27,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot(const RowArgs a)
 // separately, so the products keep binary32 accuracy.  K is cut into S
 // segments so one segment's hi/lo activations fit in shared memory; the
 // CTAs of segment s split the 16-row groups, and a group's S partial sums
-// are added in segment order by the last warp to finish it.
+// are added in segment order by the last warp to finish it.  K need only be
+// a multiple of 8 (whole 16-byte chunks): the last 32-k block is padded with
+// zero weights and zero activations.
 
 constexpr int kMmaBK = 4;  // 32-k blocks per load batch (two batches in flight)
 
@@ -45,7 +47,19 @@ DV_DEV void mma16816(float (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsig
 template <typename T, int KIND>
 DV_DEV void finalize_one(const RowArgs &a, int row, const RowRef &m, int b, float v)
 {
-    if constexpr (KIND == RK_QKV) {
+    if constexpr (KIND == RK_PRED1) {
+        if (row < a.split_rows) {
+            a.out0[(size_t)b * a.split_rows + row] = v;
+            if (a.user_scores)
+                a.user_scores[(size_t)b * a.split_rows + row] = v;
+        } else {
+            a.out1[(size_t)b * (a.max_rows - a.split_rows) + (row - a.split_rows)] = v;
+        }
+    } else if constexpr (KIND == RK_PRED2) {  // the histogram is added by the caller
+        a.out0[(size_t)b * a.max_rows + row] = v;
+        if (a.user_scores)
+            a.user_scores[(size_t)b * a.max_rows + row] = v;
+    } else if constexpr (KIND == RK_QKV) {
         v += Elem<T>::load(static_cast<const T *>(a.bias), ((size_t)m.t * a.H + m.h) * a.dh + m.e);
         if (m.t == 0) {
             a.out0[((size_t)b * a.max_sel + m.j) * a.dh + m.e] = v * a.q_scale;
@@ -71,6 +85,38 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
     // the MMAs of all of them
     const int tile = blockIdx.y, b0 = tile * 8 * NT;
     int ncta = gridDim.x;
+    if constexpr (KIND == RK_PRED2) {
+        if (a.side_cta) {
+            // the last side_cta CTAs: the head selection and norm(x), rows
+            // split among them; the last to finish publishes the flag
+            ncta = gridDim.x - a.side_cta;
+            if ((int)blockIdx.x >= ncta) {
+                pdl_wait();
+                chain_stamp(stamps, 1);
+                pdl_launch_dependents();
+                if (tile == 0) {
+                    __shared__ float sred[34];
+                    pred2_side<T>(a, sred, blockIdx.x - ncta, a.side_cta);
+                    __threadfence();
+                    __syncthreads();
+                    if (threadIdx.x == 0) {
+                        const bool last = a.side_cta == 1 ||
+                                          atomicAdd(a.side_done, 1) == a.side_cta - 1;
+                        if (last) {
+                            __threadfence();
+                            if (a.side_cta > 1)
+                                *a.side_done = 0;
+                            if (a.side_flag)
+                                st_release_gpu(a.side_flag, 1);
+                        }
+                    }
+                    chain_stamp(stamps, 6);  // side work done
+                }
+                chain_stamp_end(stamps);
+                return;
+            }
+        }
+    }
     if constexpr (KIND == RK_QKV) {
         if (a.side_cta) {
             ncta = gridDim.x - a.side_cta;
@@ -82,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
                     __shared__ int nscr[48];
                     neuron_select_cta(a.ns, final_smem(smem, a.ns.N, nscr), blockIdx.x - ncta,
                                       a.side_cta);
+                    chain_stamp(stamps, 6);  // selection done
                 }
                 chain_stamp_end(stamps);
                 return;
@@ -113,8 +160,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
     int rows;
     if constexpr (KIND == RK_QKV)
         rows = min(max(ld_cg(a.n_sel), 0), a.max_sel) * 3 * a.dh;
-    else
+    else if constexpr (KIND == RK_FC1)
         rows = min(max(ld_cg(a.n_sel), 0), a.max_sel);
+    else
+        rows = a.max_rows;
     const int ngroups = (rows + 15) >> 4;
     const int S = a.mma_seg;
     // segment of this CTA, its CTAs, and this CTA's share of the row groups
@@ -126,13 +175,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
     const int wg0 = g0 + (int)((long long)(g1 - g0) * warp / kWarpsPerBlock);
     const int wg1 = g0 + (int)((long long)(g1 - g0) * (warp + 1) / kWarpsPerBlock);
     const int k0 = sgm * a.mma_ks;
-    const int kn = min(a.mma_ks, K - k0);  // multiple of 32
+    const int kn = min(a.mma_ks, K - k0);  // multiple of 8
+    const int nblk = (kn + 31) >> 5;       // 32-k blocks, the last one zero-padded
     const int ldx = a.mma_ks + 32;         // staged row stride in halfs (64-byte pad)
 
-    if constexpr (KIND == RK_FC1) {  // h1 comes from the previous kernel
+    if constexpr (KIND != RK_QKV) {  // the activations come from the previous kernel
         pdl_wait();
         chain_stamp(stamps, 1);
         pdl_launch_dependents();
+        if constexpr (KIND == RK_PRED1) {
+            if (a.side_flag && blockIdx.x == 0 && tile == 0 && threadIdx.x == 0)
+                *a.side_flag = 0;
+        }
     }
     // this segment's activations of batch rows b0 .. b0 + 8 NT - 1: hi and lo
     // halves.  The rows' statistics first (a warp per row, over the whole
@@ -153,11 +207,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
             }
             __syncthreads();
         }
-        const int cps = kn >> 3;  // 8-element chunks of the segment per row
+        const int cps = nblk * 4;  // 8-element chunks of the segment per row
         for (int i = threadIdx.x; i < 8 * NT * cps; i += blockDim.x) {
             const int bi = i / cps, c = i - bi * cps, b = b0 + bi;
             float v[8];
-            if (b < a.B) {
+            if (b < a.B && 8 * c < kn) {
                 norm_chunk<T>(a.x + (size_t)b * a.x_ld, (k0 >> 3) + c, a.norm_g, a.norm_b, ln,
                               a.norm_g ? sstat[bi] : make_float2(0.f, 1.f), v);
             } else {
@@ -176,9 +230,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
         }
     }
     __syncthreads();
+    chain_stamp(stamps, 4);  // activations staged
 
     const int g = lane >> 2, t = lane & 3;
-    const int nblk = kn >> 5;
+    const int nlive = (kn - 8 * t + 31) >> 5;  // blocks whose chunk t is inside the segment
     const __half *xhr = xh + g * ldx + 8 * t, *xlr = xl + g * ldx + 8 * t;
     for (int grp = wg0; grp < wg1; ++grp) {
         const int ra = grp * 16 + g, rb = ra + 8;
@@ -200,16 +255,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
         uint4 wa[kMmaBK], wb[kMmaBK];
 #pragma unroll
         for (int i = 0; i < kMmaBK; ++i) {
-            wa[i] = (i < nblk && pa) ? ld_stream(pa + i * 32) : make_uint4(0u, 0u, 0u, 0u);
-            wb[i] = (i < nblk && pb) ? ld_stream(pb + i * 32) : make_uint4(0u, 0u, 0u, 0u);
+            wa[i] = (i < nlive && pa) ? ld_stream(pa + i * 32) : make_uint4(0u, 0u, 0u, 0u);
+            wb[i] = (i < nlive && pb) ? ld_stream(pb + i * 32) : make_uint4(0u, 0u, 0u, 0u);
         }
         for (int blk0 = 0; blk0 < nblk; blk0 += kMmaBK) {
             uint4 na[kMmaBK], nb[kMmaBK];
 #pragma unroll
             for (int i = 0; i < kMmaBK; ++i) {
                 const int blk = blk0 + kMmaBK + i;
-                na[i] = (blk < nblk && pa) ? ld_stream(pa + blk * 32) : make_uint4(0u, 0u, 0u, 0u);
-                nb[i] = (blk < nblk && pb) ? ld_stream(pb + blk * 32) : make_uint4(0u, 0u, 0u, 0u);
+                na[i] = (blk < nlive && pa) ? ld_stream(pa + blk * 32) : make_uint4(0u, 0u, 0u, 0u);
+                nb[i] = (blk < nlive && pb) ? ld_stream(pb + blk * 32) : make_uint4(0u, 0u, 0u, 0u);
             }
 #pragma unroll
             for (int i = 0; i < kMmaBK; ++i) {
@@ -254,15 +309,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
             __threadfence();
 #pragma unroll
             for (int tt = 0; tt < NT; ++tt) {
+                // the S partials in segment order, kSumBatch of them loaded at once
+                constexpr int kSumBatch = 8;
                 float sum[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int q = 0; q < S; ++q) {
-                    const float *qp = a.mma_part +
-                                      (((size_t)tile * a.mma_groups + grp) * S + q) * 128 * NT +
-                                      tt * 128;
-                    sum[0] += __ldcg(qp + g * 8 + 2 * t);
-                    sum[1] += __ldcg(qp + g * 8 + 2 * t + 1);
-                    sum[2] += __ldcg(qp + (g + 8) * 8 + 2 * t);
-                    sum[3] += __ldcg(qp + (g + 8) * 8 + 2 * t + 1);
+                for (int q0 = 0; q0 < S; q0 += kSumBatch) {
+                    float v[kSumBatch][4];
+#pragma unroll
+                    for (int u = 0; u < kSumBatch; ++u) {
+                        const float *qp = a.mma_part +
+                                          (((size_t)tile * a.mma_groups + grp) * S + q0 + u) *
+                                              128 * NT +
+                                          tt * 128;
+                        const bool in = q0 + u < S;
+                        v[u][0] = in ? __ldcg(qp + g * 8 + 2 * t) : 0.f;
+                        v[u][1] = in ? __ldcg(qp + g * 8 + 2 * t + 1) : 0.f;
+                        v[u][2] = in ? __ldcg(qp + (g + 8) * 8 + 2 * t) : 0.f;
+                        v[u][3] = in ? __ldcg(qp + (g + 8) * 8 + 2 * t + 1) : 0.f;
+                    }
+#pragma unroll
+                    for (int u = 0; u < kSumBatch; ++u)
+                        if (q0 + u < S)
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                sum[i] += v[u][i];
                 }
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
@@ -286,8 +355,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
                 if (bt + 1 < a.B)
                     finalize_one<T, KIND>(a, rb, mb, bt + 1, acc[tt][3]);
             }
+            if constexpr (KIND == RK_PRED2) {
+                // first-digit histogram: the lanes holding the same (batch
+                // row, digit) add their count once
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int b = bt + (i & 1);
+                    const bool live = (i < 2 ? ma.p : mb.p) != nullptr && b < a.B;
+                    const unsigned dig = score_key(acc[tt][i]) >> 21;
+                    const unsigned key = live ? ((unsigned)b << 11) | dig : 0xffffffffu;
+                    const unsigned same = __match_any_sync(0xffffffffu, key);
+                    if (live && lane == __ffs(same) - 1)
+                        atomicAdd(a.hist + (size_t)b * kTopkBins + dig, __popc(same));
+                }
+            }
         }
     }
+    chain_stamp(stamps, 5);  // groups done
     chain_stamp_end(stamps);
 }
 
@@ -434,7 +518,7 @@ int rowdot_mma_tiles(int B) { return B <= 8 ? 1 : (B <= 16 ? 2 : 4); }
 cudaError_t launch_rowdot_mma(int kind, const RowArgs &a, dim3 grid, size_t smem,
                               cudaStream_t st, bool pdl)
 {
-    if (kind != RK_QKV && kind != RK_FC1)
+    if (kind < RK_PRED1 || kind > RK_FC1)
         return cudaErrorInvalidValue;
     if (smem > kSmemCap)
         return cudaErrorInvalidValue;
@@ -449,7 +533,12 @@ cudaError_t launch_rowdot_mma(int kind, const RowArgs &a, dim3 grid, size_t smem
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     const int nt = a.mma_nt;
-    return kind == RK_QKV ? dispatch_nt<RK_QKV>(nt, cfg, a) : dispatch_nt<RK_FC1>(nt, cfg, a);
+    switch (kind) {
+    case RK_PRED1: return dispatch_nt<RK_PRED1>(nt, cfg, a);
+    case RK_PRED2: return dispatch_nt<RK_PRED2>(nt, cfg, a);
+    case RK_QKV: return dispatch_nt<RK_QKV>(nt, cfg, a);
+    default: return dispatch_nt<RK_FC1>(nt, cfg, a);
+    }
 }
 
 // K segments and their length for the tensor-core variant: each segment's

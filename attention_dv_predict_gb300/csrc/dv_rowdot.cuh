@@ -306,13 +306,16 @@ DV_DEV void stage_acts(const RowArgs &a, float *xs, int b0, float *red)
 // Side work of one CTA of the stage-2 predictor kernel in the fused decode:
 // select the heads (the head scores come from the previous kernel) and
 // write the attention block's normalised input xn = norm(x) to global
-// memory, both for the QKV kernel that follows.  From kSideWarpRows batch
-// rows on, the rows are dealt out to the warps (below it the whole CTA
-// normalises one row after the other: a lone warp per row was slower).
+// memory, both for the QKV kernel that follows.  The side work may be split
+// over nparts CTAs: this one (part) normalises rows part, part + nparts, ...
+// and part 0 also selects the heads.  A lone side CTA with kSideWarpRows
+// rows or more deals the rows out to its warps; otherwise the whole CTA
+// normalises one row after the other (a lone warp per row was slower for
+// few rows, and one CTA's L2 bandwidth too little for many).
 constexpr int kSideWarpRows = 4;
 
 template <typename T>
-__device__ __noinline__ void pred2_side(const RowArgs &a, float *red)
+__device__ __noinline__ void pred2_side(const RowArgs &a, float *red, int part, int nparts)
 {
     __shared__ unsigned wbits[kWarpsPerBlock * kHeadKPL];
     __shared__ unsigned ubits[kHeadKPL];
@@ -320,8 +323,9 @@ __device__ __noinline__ void pred2_side(const RowArgs &a, float *red)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const bool ln = p.norm_kind == DV_LAYERNORM;
     constexpr int EPC = Elem<T>::EPC;
-    if (a.B < kSideWarpRows) {
-        for (int b = 0; b < a.B; ++b) {
+    const bool by_warp = nparts == 1 && a.B >= kSideWarpRows;
+    if (!by_warp) {
+        for (int b = part; b < a.B; b += nparts) {
             float *dst = p.xn + (size_t)b * p.d;
             norm_row<T>(p.x + (size_t)b * p.x_ld, p.d, p.g, p.beta, p.norm_kind, p.eps, red,
                         [&](int c, const float(&v)[EPC]) {
@@ -332,7 +336,7 @@ __device__ __noinline__ void pred2_side(const RowArgs &a, float *red)
                         });
         }
     }
-    for (int b = warp; b < a.B && a.B >= kSideWarpRows; b += kWarpsPerBlock) {
+    for (int b = warp; b < a.B && by_warp; b += kWarpsPerBlock) {
         const float *src = p.x + (size_t)b * p.x_ld;
         float *dst = p.xn + (size_t)b * p.d;
         const float2 st = p.g ? warp_row_stats(src, p.d, ln, p.eps, lane) : make_float2(0.f, 1.f);
@@ -345,7 +349,8 @@ __device__ __noinline__ void pred2_side(const RowArgs &a, float *red)
                     make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
         }
     }
-    head_select_block(p.s_h, a.B, p.H, p.k_h, wbits, ubits, p.idx_h, p.u_h, p.n_u_h);
+    if (part == 0)
+        head_select_block(p.s_h, a.B, p.H, p.k_h, wbits, ubits, p.idx_h, p.u_h, p.n_u_h);
 }
 
 // ---------------------------------------------------------------------------
@@ -497,7 +502,7 @@ DV_DEV void rowdot_body(const RowArgs &a, int cta, int nct, const Dep &dep)
             if (cta == ncta) {  // the last CTA does the side work instead
                 dep.wait();
                 if (tile == 0) {
-                    pred2_side<T>(a, red);
+                    pred2_side<T>(a, red, 0, 1);
                     __threadfence();
                     __syncthreads();
                     if (threadIdx.x == 0 && a.side_flag)

@@ -119,6 +119,64 @@ def test_predict_scores_and_sets(dv):
     check_topk_rows(sel.idx_n.cpu().numpy(), p["idx_n"], p["s_n"], case.k_n, "neurons")
 
 
+# binary16 from batch 3 on: both predictor stages on the tensor-core row
+# kernel; rank 1000 leaves an 8-column last 32-k block in stage 2
+PRED_MMA = dv_inputs.LayerConfig("pred_mma", 4096, 6, 128, 3000, 1000, 70, 1, "f16",
+                                 dv_inputs.Fraction(1, 10), k_heads_fixed=2)
+
+
+@pytest.mark.parametrize("B", [3, 11, 32])
+def test_predict_tensor_core_path(dv, B):
+    case = make_case(PRED_MMA, B=B, seed=40 + B)
+    desc = dv.desc_from_config(case.cfg, case.kv_cap)
+    layer = dv.Layer(desc, case.w_dev)
+    sel = dv.SelectionBuffers(desc, case.B, case.k_h, case.k_n)
+    ws = dv.Workspace(desc, case.B)
+    x = torch.from_numpy(case.x).cuda()
+    sh = torch.empty((case.B, case.cfg.n_heads), device="cuda")
+    sn = torch.empty((case.B, case.cfg.d_ffn), device="cuda")
+    for _ in range(2):  # the second call finds the histograms cleared by the first
+        dv.dv_predict_topk(layer, x, case.k_h, case.k_n, sel, ws, sh, sn)
+    torch.cuda.synchronize()
+    assert dv.dv_check(ws) == dv.DV_OK
+    D = oracle.desc_from_config(case.cfg, case.kv_cap)
+    p = oracle.predict(D, case.w_host, case.x, case.k_h, case.k_n)
+    eh, en = tensor_core_score_bounds(case.w_host, case.x)
+    for got, want, tol, what in ((sh, p["s_h"], eh, "head"), (sn, p["s_n"], en, "neuron")):
+        err = np.abs(got.cpu().numpy().astype(np.float64) - want)
+        assert np.all(err <= tol), f"{what} scores: worst error / bound {np.max(err / tol):.3f}"
+    check_topk_rows(sel.idx_h.cpu().numpy(), p["idx_h"], p["s_h"], case.k_h, "heads")
+    check_topk_rows(sel.idx_n.cpu().numpy(), p["idx_n"], p["s_n"], case.k_n, "neurons")
+
+
+def tensor_core_score_bounds(w, x):
+    """Elementwise bounds on the tensor-core predictor scores.  Each stage
+    runs 2 ceil(K/16) binary32 MMA accumulations (the activations split into
+    binary16 hi and lo parts), each off by at most one binary32 ulp of the
+    running sum, which is bounded by sum_k |w_k x_k|; the split leaves a
+    residual of 2^-22 relative, and the result is rounded once more:
+    c = 2 ceil(K/16) + 4 units of 2^-23 sum |w x|.  Stage 2 also carries
+    stage 1's error in u through |Bm|."""
+    eps = 2.0 ** -23
+    x = np.abs(x.astype(np.float64))
+    wh = np.abs(w["pred_h"].astype(np.float64))
+    a = w["pred_a"].astype(np.float64)
+    bm = np.abs(w["pred_b"].astype(np.float64))
+    d, r = a.shape[1], a.shape[0]
+    c1 = 2 * -(-d // 16) + 4
+    c2 = 2 * -(-r // 16) + 4
+    eh = c1 * eps * x @ wh.T
+    ua = x @ np.abs(a).T  # bounds |u| and stage 1's running sums
+    en = c2 * eps * ua @ bm.T + c1 * eps * ua @ bm.T
+    return eh + 1e-12, en + 1e-12
+
+
+def test_layer_tensor_core_predictor(dv):
+    case = make_case(PRED_MMA, B=11, seed=61)
+    g = run_gpu_layer(dv, case)
+    check_layer_parity(case, g)
+
+
 def test_blocks_on_caller_index_sets(dv):
     """dv_sparse_attn and dv_sparse_mlp on index sets the caller chooses."""
     case = make_case(RAGGED, B=2, seed=5)

@@ -251,9 +251,12 @@ size_t set_mma(RowArgs &a, const dv_layer_desc &D, void *ws, const WsLayout &L, 
         const int groups = ceil_div(fixed_rows, 16);
         int s_ws = 1, ks_ws = 0;  // the segments the partial slots are sized for
         rowdot_mma_plan(D.d_model, nt, &s_ws, &ks_ws);
-        // at most K / 128 segments, and several CTAs per segment
+        // at most K / 128 segments, several CTAs per segment, and at most
+        // kMmaSegMax: the last warp of a group loads its S partials of 8 nt
+        // rows (35 segments at OPT-175B, batch 32: a 20 us tail)
+        constexpr int kMmaSegMax = 8;
         const int want = std::min(std::min(ceil_div(nsm * kWarpsPerBlock, groups), a.K / 128),
-                                  nsm / 4);
+                                  std::min(nsm / 4, kMmaSegMax));
         if (want > S) {
             const int ks2 = ceil_div(ceil_div(a.K, want), 32) * 32;
             const int s2 = ceil_div(a.K, ks2);

@@ -564,15 +564,22 @@ DV_DEV void rowdot_body(const RowArgs &a, int cta, int nct, const Dep &dep)
     const int units = seg ? rows * g.nsu : (rows + g.rpu - 1) / g.rpu;
     const int Wt = ncta * kWarpsPerBlock;
     const int gw = cta * kWarpsPerBlock + warp;
-    const int ub = range_start(units, Wt, gw), ue = range_start(units, Wt, gw + 1);
+    // at most one segmented row per warp (the stage-1 predictor: 1096 rows
+    // of 24 KB at OPT-175B): whole rows per warp, so no row is shared and
+    // no partial sums are combined; otherwise equal shares of the units
+    const bool whole = seg && rows <= Wt;
+    auto ustart = [&](int w) {
+        return whole ? (int)((long long)rows * w / Wt) * g.nsu : range_start(units, Wt, w);
+    };
+    const int ub = ustart(gw), ue = ustart(gw + 1);
     const int LG = 32 / g.rpu;
     const int grp = lane / LG, lig = lane - grp * LG;
 
     // gather indices of the rows this CTA touches, staged in shared memory
     const bool stage_sel = (KIND == RK_FC1) || (KIND == RK_QKV);
     if (stage_sel) {
-        const int cb = range_start(units, Wt, cta * kWarpsPerBlock);
-        const int ce = range_start(units, Wt, (cta + 1) * kWarpsPerBlock);
+        const int cb = ustart(cta * kWarpsPerBlock);
+        const int ce = ustart((cta + 1) * kWarpsPerBlock);
         if (ce > cb) {
             const int r0 = seg ? cb / g.nsu : cb * g.rpu;
             const int r1 = seg ? (ce - 1) / g.nsu : min(rows, ce * g.rpu) - 1;

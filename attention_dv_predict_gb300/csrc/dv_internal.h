@@ -328,6 +328,11 @@ size_t rowdot_smem(int kind, int nb, int K);
 cudaError_t launch_rowdot_mma(int kind, const RowArgs &a, dim3 grid, size_t smem,
                               cudaStream_t st, bool pdl);
 void rowdot_mma_plan(int K, int nt, int *S, int *ks);
+// Staged activation row stride (halves) of the tensor-core row kernel for K
+// segments of ks: 64 bytes modulo 128, so the two 8-row halves of a warp's
+// 16-byte fragment reads fall in distinct banks (a stride of 0 modulo 128
+// doubles the shared-memory wavefronts).
+__host__ __device__ inline int rowdot_mma_ldx(int ks) { return ks + (ks % 64 == 0 ? 32 : 64); }
 size_t rowdot_mma_smem(int ks, int nt);
 int rowdot_mma_tiles(int B);  // batch tiles per weight pass
 constexpr int kMmaMinBatch = 3;  // batches from which binary16 layers use tensor cores

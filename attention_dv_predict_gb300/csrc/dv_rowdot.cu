@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rowdot_mma(const RowArgs a)
     const int k0 = sgm * a.mma_ks;
     const int kn = min(a.mma_ks, K - k0);  // multiple of 8
     const int nblk = (kn + 31) >> 5;       // 32-k blocks, the last one zero-padded
-    const int ldx = a.mma_ks + 32;         // staged row stride in halfs (64-byte pad)
+    const int ldx = rowdot_mma_ldx(a.mma_ks);  // staged row stride in halves
 
     if constexpr (KIND != RK_QKV) {  // the activations come from the previous kernel
         pdl_wait();
@@ -547,15 +547,16 @@ cudaError_t launch_rowdot_mma(int kind, const RowArgs &a, dim3 grid, size_t smem
 void rowdot_mma_plan(int K, int nt, int *S, int *ks)
 {
     const size_t budget = 160 * 1024;
-    int s = 1;
-    while ((size_t)32 * nt * ((size_t)(K + s - 1) / s + 32) > budget)
-        ++s;
-    int len = (K + s - 1) / s;
-    len = (len + 31) / 32 * 32;
+    int s = 1, len = 0;
+    for (;; ++s) {
+        len = ((K + s - 1) / s + 31) / 32 * 32;
+        if ((size_t)32 * nt * rowdot_mma_ldx(len) <= budget || len <= 32)
+            break;
+    }
     *ks = len;
     *S = (K + len - 1) / len;
 }
 
-size_t rowdot_mma_smem(int ks, int nt) { return (size_t)32 * nt * (ks + 32); }
+size_t rowdot_mma_smem(int ks, int nt) { return (size_t)32 * nt * rowdot_mma_ldx(ks); }
 
 }  // namespace dv

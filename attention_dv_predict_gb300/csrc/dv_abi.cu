@@ -503,7 +503,7 @@ dv_status run_attn(const dv_layer_desc &D, const dv_layer_weights &w, const floa
     if ((s = lc.mark()))
         return s;
     if (use_mma(D, B)) {
-        const int nt = colacc_mma_tiles(B);
+        const int nt = colacc_mma_tiles(B, CK_OPROJ);
         if (failed(launch_colacc_mma(CK_OPROJ, nt, c, dim3(lc.nsm, ceil_div(B, 8 * nt)), lc.st, lc.pdl)))
             return DV_ERR_CUDA;
     } else if (failed(launch_colacc(CK_OPROJ, D.dtype, nb, c, dim3(lc.nsm, ceil_div(B, nb)), lc.st,
@@ -630,7 +630,7 @@ dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float
     if ((s = lc.mark()))
         return s;
     if (use_mma(D, B)) {
-        const int nt = colacc_mma_tiles(B);
+        const int nt = colacc_mma_tiles(B, CK_FC2);
         if (failed(launch_colacc_mma(CK_FC2, nt, c, dim3(lc.nsm, ceil_div(B, 8 * nt)), lc.st, lc.pdl)))
             return DV_ERR_CUDA;
     } else if (failed(launch_colacc(CK_FC2, D.dtype, nb, c, dim3(lc.nsm, ceil_div(B, nb)), lc.st,
@@ -918,7 +918,7 @@ bool ws_layout(const dv_layer_desc &D, int B, WsLayout *L)
     // every batch row of its passes (the tensor-core variant's last pass of
     // 8 nt rows may run past the padded batch)
     const size_t cb_max = (size_t)colacc_block_cols(D.dtype, 1) * 2;  // NB x block columns
-    const size_t cnt_t = (size_t)colacc_mma_tiles(B);
+    const size_t cnt_t = (size_t)std::max(colacc_mma_tiles(B, CK_OPROJ), colacc_mma_tiles(B, CK_FC2));
     const size_t cbp = std::max(bp, (size_t)ceil_div(B, 8 * (int)cnt_t) * 8 * cnt_t);
     L->cpart_o = take(cbp * (kMaxWarps / kWarpsPerBlock) * 2 * cb_max * 4);
     L->cpart_2 = take(cbp * (kMaxWarps / kWarpsPerBlock) * 2 * cb_max * 4);

@@ -1,5 +1,5 @@
 // dv_colacc_mma.cu -- tensor-core variant of the column-gather GEMV for batch
-// tiles of 8 rows, one or two tiles per weight pass (binary16 weights;
+// tiles of 8 rows, one, two or four tiles per weight pass (binary16 weights;
 // out-projection and fc2), sm_103a.
 //
 //   out[b][c] = res[b][c] + bias[c] + sum_i coef[b][i] * W[row(i)][c]
@@ -14,7 +14,7 @@
 //                 carries both and the products keep ~22 bits;
 //   B (16 x 8)  = 16 gathered weight rows x 8 columns;
 //   D (16 x 8)  = hi and lo partial sums, added at the end.
-// A CTA takes NT tiles of 8 batch rows (NT = 2 above 8 rows): the B
+// A CTA takes NT tiles of 8 batch rows (NT = 2 above 8 rows, 4 above 16): the B
 // fragments of each weight group feed the MMAs of every tile, so the
 // weights are read once per 8 NT batch rows.
 // Each warp owns 32 columns of a 512-column block.  The CTA copies groups of
@@ -356,18 +356,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_colacc_mma(const ColArgs a)
 
 size_t colacc_mma_smem() { return kCmSmem; }
 
-int colacc_mma_tiles(int B) { return B > 8 ? 2 : 1; }
+// Four tiles a pass (above 16 rows) only for fc2: the out-projection's
+// coefficient staging (the attention records' merge) spills at four tiles
+// and measured slower than two passes of two (batch 32: +25 us; fc2: -22).
+int colacc_mma_tiles(int B, int kind)
+{
+    return B > 16 && kind == CK_FC2 ? 4 : (B > 8 ? 2 : 1);
+}
 
 cudaError_t launch_colacc_mma(int kind, int nt, const ColArgs &a, dim3 grid, cudaStream_t st,
                               bool pdl)
 {
-    if ((kind != CK_OPROJ && kind != CK_FC2) || (nt != 1 && nt != 2))
+    if ((kind != CK_OPROJ && kind != CK_FC2) || (nt != 1 && nt != 2 && nt != 4))
         return cudaErrorInvalidValue;
-    void (*kern)(ColArgs) =
-        kind == CK_OPROJ ? (nt == 1 ? k_colacc_mma<CK_OPROJ, 1> : k_colacc_mma<CK_OPROJ, 2>)
-                         : (nt == 1 ? k_colacc_mma<CK_FC2, 1> : k_colacc_mma<CK_FC2, 2>);
-    static DeviceOnce once[2][2];
-    cudaError_t e = once[kind == CK_OPROJ ? 0 : 1][nt - 1].run([&] {
+    void (*const table[2][3])(ColArgs) = {
+        {k_colacc_mma<CK_OPROJ, 1>, k_colacc_mma<CK_OPROJ, 2>, k_colacc_mma<CK_OPROJ, 4>},
+        {k_colacc_mma<CK_FC2, 1>, k_colacc_mma<CK_FC2, 2>, k_colacc_mma<CK_FC2, 4>}};
+    const int ki = kind == CK_OPROJ ? 0 : 1, ti = nt == 4 ? 2 : nt - 1;
+    void (*kern)(ColArgs) = table[ki][ti];
+    static DeviceOnce once[2][3];
+    cudaError_t e = once[ki][ti].run([&] {
         return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)kCmSmem);
     });

@@ -338,7 +338,7 @@ int rowdot_mma_tiles(int B);  // batch tiles per weight pass
 constexpr int kMmaMinBatch = 3;  // batches from which binary16 layers use tensor cores
 // Tensor-core column kernel (binary16, nt batch tiles of 8 per CTA;
 // out-projection, fc2): grid.y = ceil(B / (8 nt)).
-int colacc_mma_tiles(int B);
+int colacc_mma_tiles(int B, int kind);
 cudaError_t launch_colacc_mma(int kind, int nt, const ColArgs &a, dim3 grid, cudaStream_t st,
                               bool pdl);
 size_t colacc_mma_smem();

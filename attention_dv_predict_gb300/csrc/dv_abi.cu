@@ -1,6 +1,7 @@
 // dv_abi.cu -- C entry points of libdv: argument checks, workspace layout and
 // the launch sequence of the sparse layer decode.  See include/dv.h.
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -273,6 +274,27 @@ size_t set_mma(RowArgs &a, const dv_layer_desc &D, void *ws, const WsLayout &L, 
     a.mma_part = at<float>(ws, L.mma_part);
     a.mma_cnt = at<int>(ws, L.mma_cnt);
     return rowdot_mma_smem(ks, nt);
+}
+
+// Row-kernel variant for fc1 on the tensor cores: 0 = mma.sync (default),
+// 1 = tcgen05 from 9 batch rows (dv_set_row_kernel).
+std::atomic<int> g_row_variant{0};
+
+bool row_tc(const dv_layer_desc &D, int B)
+{
+    return g_row_variant.load() == 1 && use_mma(D, B) && B > 8 && D.d_model % 64 == 0;
+}
+
+// Rows of the partial slots of the tcgen05 kernel: 128-row tiles.
+int tc_tiles_max(const dv_layer_desc &D) { return ceil_div(mma_rows_max(D), 128); }
+
+void set_row_tc(RowArgs &a, const dv_layer_desc &D, void *ws, const WsLayout &L)
+{
+    a.mma_nt = rowdot_mma_tiles(a.B);  // 2 or 4: batch tiles of 16 or 32 rows
+    rowdot_tc_plan(a.K, 8 * a.mma_nt, &a.mma_seg, &a.mma_ks);
+    a.mma_groups = tc_tiles_max(D);
+    a.mma_part = at<float>(ws, L.mma_part);
+    a.mma_cnt = at<int>(ws, L.mma_cnt);
 }
 
 // PRED1 (head scores, low-rank factor u) and PRED2 (neuron scores +
@@ -596,7 +618,12 @@ dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float
     dv_status s = lc.mark();
     if (s)
         return s;
-    if (use_mma(D, B)) {
+    if (row_tc(D, B)) {  // the tcgen05 fc1 kernel (opt-in, dv_set_row_kernel)
+        set_row_tc(a, D, ws, L);
+        if (failed(launch_rowdot_tc(a, dim3(lc.nsm, ceil_div(B, 8 * a.mma_nt)), lc.st,
+                                    lc.pdl && !first)))
+            return DV_ERR_CUDA;
+    } else if (use_mma(D, B)) {
         const size_t sm = set_mma(a, D, ws, L, lc.nsm);
         if (failed(launch_rowdot_mma(RK_FC1, a, dim3(lc.nsm, ceil_div(B, 8 * a.mma_nt)), sm, lc.st,
                               lc.pdl && !first)))
@@ -945,7 +972,14 @@ bool ws_layout(const dv_layer_desc &D, int B, WsLayout *L)
         rowdot_mma_plan(D.d_model, nt, &S, &ks);
         const size_t passes = (size_t)ceil_div(B, 8 * nt);
         const size_t groups = (size_t)ceil_div(mma_rows_max(D), 16);
-        L->mma_part = take(passes * groups * S * 128 * nt * 4);
+        size_t part = passes * groups * S * 128 * nt * 4;
+        if (nt >= 2) {  // or the tcgen05 fc1 kernel's: 128-row tiles x its segments
+            int St = 1, kst = 0;
+            rowdot_tc_plan(D.d_model, 8 * nt, &St, &kst);
+            const size_t tc = passes * (size_t)tc_tiles_max(D) * St * 128 * (8 * nt) * 4;
+            part = std::max(part, tc);
+        }
+        L->mma_part = take(part);
         L->mma_cnt = take(passes * groups * 4);
     }
     {  // streaming kernel (binary16, batches 1-2; sized for either when B <= 2)
@@ -975,6 +1009,14 @@ extern "C" {
 // process shares with every other user of the same CUDA runtime library (an
 // error another component left there is not this call's).  The error behind
 // the last DV_ERR_CUDA of this thread is kept in t_cuda_error instead.
+dv_status dv_set_row_kernel(int variant)
+{
+    if (variant != 0 && variant != 1)
+        return DV_ERR_INVALID_ARG;
+    g_row_variant.store(variant);
+    return DV_OK;
+}
+
 int dv_cuda_error(void)
 {
     const int e = t_cuda_error;

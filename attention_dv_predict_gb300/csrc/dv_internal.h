@@ -328,6 +328,11 @@ size_t rowdot_smem(int kind, int nb, int K);
 cudaError_t launch_rowdot_mma(int kind, const RowArgs &a, dim3 grid, size_t smem,
                               cudaStream_t st, bool pdl);
 void rowdot_mma_plan(int K, int nt, int *S, int *ks);
+// tcgen05 variant of the fc1 row kernel (batch tiles of 8 mma_nt = 16 or 32
+// rows; mma_groups = the 128-row tile stride of the partial slots).
+void rowdot_tc_plan(int K, int bt, int *S, int *ks);
+size_t rowdot_tc_smem();
+cudaError_t launch_rowdot_tc(const RowArgs &a, dim3 grid, cudaStream_t st, bool pdl);
 // Staged activation row stride (halves) of the tensor-core row kernel for K
 // segments of ks: 64 bytes modulo 128, so the two 8-row halves of a warp's
 // 16-byte fragment reads fall in distinct banks (a stride of 0 modulo 128

@@ -61,6 +61,7 @@ _SIGS = {
     "dv_status_string": ([_I], C.c_char_p),
     "dv_cuda_error": ([], _I),
     "dv_abi_version": ([], _I),
+    "dv_set_row_kernel": ([_I], _I),
     "dv_workspace_size": ([_D, _I], _SZ),
     "dv_workspace_init": ([_P, _SZ, _P], _I),
     "dv_check": ([_P, _SZ, _P], _I),
@@ -209,6 +210,11 @@ class SelectionBuffers:
 
 def workspace_size(desc: LayerDesc, batch: int) -> int:
     return int(_lib.dv_workspace_size(C.byref(desc), int(batch)))
+
+
+def dv_set_row_kernel(variant: int) -> None:
+    """0: fc1 rows on mma.sync (default); 1: on tcgen05 (binary16, ReLU, B >= 9)."""
+    _check("dv_set_row_kernel", _lib.dv_set_row_kernel(int(variant)))
 
 
 def dv_check(ws: Workspace, stream=None) -> int:

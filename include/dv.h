@@ -133,6 +133,19 @@ int dv_cuda_error(void);
 /* DV_ABI_VERSION of the built library. */
 int dv_abi_version(void);
 
+/* Row-kernel variant of the fc1 rows on the tensor cores ("DejaVu Guide:
+ * Contextual Sparsity for LLM Inference", the pipeline's "Sparse Gather GEMV
+ * on Tensor Cores"), process-wide, for calls issued after it returns:
+ *   0  mma.sync m16n8k16 kernel (the default);
+ *   1  tcgen05.mma kernel (M = 128 gathered rows, accumulator in tensor
+ *      memory) for binary16 ReLU layers from 9 batch rows with d_model a
+ *      multiple of 64; every other case keeps variant 0.
+ * Results agree within the binary32 accumulation error; the ring, segment
+ * and partial order differ, so the bits may not.  DV_ERR_INVALID_ARG for
+ * another value.  Not thread-safe against calls in flight on other
+ * threads. */
+dv_status dv_set_row_kernel(int variant);
+
 /* Bytes of workspace the calls below need for this layer shape and batch
  * (sized for the largest possible unions).  0 if desc or batch is invalid. */
 size_t dv_workspace_size(const dv_layer_desc *desc, int batch);

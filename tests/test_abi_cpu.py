@@ -124,3 +124,12 @@ def test_argument_checks_fail_before_any_launch(dv):
     assert lib.dv_layer_decode(C.byref(unsupported), C.byref(w), fake[0], None, 1, 2, 103, fake[1],
                                fake[2], 64, C.byref(sel), None, fake[3], ws, 1 << 30,
                                None) == dv.DV_ERR_UNSUPPORTED
+
+
+def test_row_kernel_variant_switch(dv):
+    """Host-only: the variant switch accepts 0 and 1 and refuses the rest."""
+    with pytest.raises(dv.DvError) as e:
+        dv.dv_set_row_kernel(2)
+    assert e.value.status == dv.DV_ERR_INVALID_ARG
+    dv.dv_set_row_kernel(1)
+    dv.dv_set_row_kernel(0)

@@ -194,33 +194,58 @@ DV_DEV void norm_row(const float *src, int K, const void *g_, const void *b_, in
 }
 
 // Statistics of one row src[0..K) (K a multiple of 4, 16-byte aligned) by
-// one warp: (mean, 1/sqrt(var + eps)) for LayerNorm, (0, 1/sqrt(mean of
-// squares + eps)) for RMSNorm; two passes, the row read at L2 both times.
+// one warp, in one pass over the row (read at L2): (mean, 1/sqrt(var + eps))
+// for LayerNorm, (0, 1/sqrt(mean of squares + eps)) for RMSNorm.  For
+// LayerNorm each lane sums its values shifted by its own first one, turns
+// that into (count, mean, M2) and the lanes merge pairwise (Chan, Golub and
+// LeVeque's update); lane 0's result is broadcast.
 DV_DEV float2 warp_row_stats(const float *src, int K, bool ln, float eps, int lane)
 {
     const float4 *s4 = reinterpret_cast<const float4 *>(src);
     const int n4 = K >> 2;
-    float mean = 0.f;
-    if (ln) {
-        float s = 0.f;
+    if (!ln) {
+        float ss = 0.f;
 #pragma unroll 8
         for (int i = lane; i < n4; i += 32) {
             const float4 t = __ldcg(s4 + i);
-            s += (t.x + t.y) + (t.z + t.w);
+            ss = fmaf(t.x, t.x, ss);
+            ss = fmaf(t.y, t.y, ss);
+            ss = fmaf(t.z, t.z, ss);
+            ss = fmaf(t.w, t.w, ss);
         }
-        mean = warp_sum(s) / (float)K;
+        return make_float2(0.f, rsqrtf(warp_sum(ss) / (float)K + eps));
     }
-    float ss = 0.f;
+    const float c = lane < n4 ? __ldcg(src + 4 * lane) : 0.f;
+    float s1 = 0.f, s2 = 0.f;
 #pragma unroll 8
     for (int i = lane; i < n4; i += 32) {
         const float4 t = __ldcg(s4 + i);
-        const float dx = t.x - mean, dy = t.y - mean, dz = t.z - mean, dw = t.w - mean;
-        ss = fmaf(dx, dx, ss);
-        ss = fmaf(dy, dy, ss);
-        ss = fmaf(dz, dz, ss);
-        ss = fmaf(dw, dw, ss);
+        const float dx = t.x - c, dy = t.y - c, dz = t.z - c, dw = t.w - c;
+        s1 += (dx + dy) + (dz + dw);
+        s2 = fmaf(dx, dx, s2);
+        s2 = fmaf(dy, dy, s2);
+        s2 = fmaf(dz, dz, s2);
+        s2 = fmaf(dw, dw, s2);
     }
-    return make_float2(mean, rsqrtf(warp_sum(ss) / (float)K + eps));
+    float n = (float)(4 * ((n4 - lane + 31) / 32 > 0 ? (n4 - lane + 31) / 32 : 0));
+    float mean = n > 0.f ? c + s1 / n : 0.f;
+    float m2 = n > 0.f ? fmaxf(s2 - s1 * (s1 / n), 0.f) : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float nb = __shfl_xor_sync(0xffffffffu, n, o);
+        const float mb = __shfl_xor_sync(0xffffffffu, mean, o);
+        const float m2b = __shfl_xor_sync(0xffffffffu, m2, o);
+        const float tot = n + nb;
+        if (tot > 0.f) {
+            const float delta = mb - mean;
+            mean = fmaf(delta, nb / tot, mean);
+            m2 = m2 + m2b + delta * delta * (n * nb / tot);
+            n = tot;
+        }
+    }
+    mean = __shfl_sync(0xffffffffu, mean, 0);
+    m2 = __shfl_sync(0xffffffffu, m2, 0);
+    return make_float2(mean, rsqrtf(m2 / (float)K + eps));
 }
 
 // Normalised chunk c (EPC values from src + c EPC) with the row statistics st.

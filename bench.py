@@ -52,6 +52,9 @@ def parse_args(argv=None):
     p.add_argument("--batch", type=int, default=None)
     p.add_argument("--copies", type=int, default=4)
     p.add_argument("--cpu-budget-s", type=float, default=15.0)
+    p.add_argument("--row-kernel", choices=["mma", "tc"], default="mma",
+                   help="fc1 rows on mma.sync (default) or on the opt-in tcgen05 kernel "
+                        "(binary16, from 9 batch rows)")
     p.add_argument("--no-extras", action="store_true",
                    help="skip dense baseline, e2e, copy peak, CPU baseline and stack legs")
     p.add_argument("--stack-layers", type=int, default=24,
@@ -205,6 +208,7 @@ def run_cuda(args):
     from attention_dv_predict_gb300 import traffic
     import dv_inputs
 
+    dv.dv_set_row_kernel(1 if args.row_kernel == "tc" else 0)
     cfg = dv_inputs.CONFIGS[args.config]
     B = args.batch or cfg.batch
     cfg = cfg.with_(batch=B)
@@ -366,7 +370,8 @@ def run_cuda(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": dict(workload_config(cfg, B), copies=copies,
                        l2="each step reads a different layer copy; 519 MB/step > 129 MB L2",
-                       parallelism="replicas" if world > 1 else "single GPU"),
+                       parallelism="replicas" if world > 1 else "single GPU",
+                       fc1_rows="tcgen05" if args.row_kernel == "tc" else "mma.sync"),
         "achieved_gbs": round(achieved, 1),
         "roofline_frac_step": round(achieved / peak, 4),
         "required_bytes_per_step": step_bytes.total,

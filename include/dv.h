@@ -238,10 +238,13 @@ int dv_sparse_mlp(const dv_layer_desc *desc, const dv_layer_weights *w, const fl
  * k_heads, k_neurons).)
  *   h1: optional device output [B, d] of the attention block's result
  *       (NULL keeps it in the workspace).
- * Seven kernels (the predictors, QKV, attention, out-projection, fc1, fc2)
- * chained by programmatic dependent launch; plain stream order for binary16
- * layers from 3 batch rows, where QKV, fc1, out-projection and fc2 use
- * tensor cores.  Serves every shape and batch.
+ * Seven kernels (the predictors, QKV, attention, out-projection, fc1, fc2;
+ * at batches 1-2 fc1 and fc2 are one pass plus a sum of partials) chained
+ * by programmatic dependent launch.  Binary16 layers run QKV, fc1,
+ * out-projection and fc2 on tensor cores from 3 batch rows and both
+ * predictor stages from 5; there the stage-2 predictor -> QKV boundary is
+ * in stream order, and from 8 rows every boundary is.  Serves every shape
+ * and batch.
  */
 int dv_layer_decode(const dv_layer_desc *desc, const dv_layer_weights *w, const float *x,
                     const float *x_pred, int batch, int k_heads, int k_neurons, void *k_cache,
@@ -289,8 +292,11 @@ int dv_layer_decode_persistent(const dv_layer_desc *desc, const dv_layer_weights
  *     ready, 2 it ends, 3 the SM it ran on (%smid); 4 .. 7 points inside a
  *     kernel (attention: 4 warp 0's first batch of keys consumed, 5 warp
  *     0's keys done, 6 the chunk record written; the one-pass MLP: 4 its
- *     activations summed).  The tensor-core kernels (binary16 layers from 3 batch rows)
- *     record nothing.
+ *     activations summed; row kernels: 4 activations staged, 5 rows done,
+ *     6 a side CTA's selection done; column kernels: 4 the first
+ *     coefficients staged, 5 the last piece consumed, 6 a block's combine
+ *     starts; the sum of partials: 4 summed).  Slots a CTA never reaches
+ *     keep what an earlier call wrote.
  *   persistent != 0: n_stamps >= 32 G; stamps[c * 32 + i] for CTA c at
  *     fixed points: its consumer warps: 0 start, 1 first predictor stage
  *     done, 2 predictor results complete, 3 neuron scoring starts, 4 done, 5

@@ -575,8 +575,7 @@ dv_status run_mlp(const dv_layer_desc &D, const dv_layer_weights &w, const float
         ps.part = m.part;
         ps.out = y;
         ps.stamps = lc.kernel_stamps();
-        if (part_sum_groups(d) > lc.nsm)
-            ps.stamps = nullptr;  // more CTAs than timeline slots
+        ps.stamp_ctas = lc.nsm;  // the timeline has a slot per SM
         dv_status s = lc.mark();
         if (s)
             return s;

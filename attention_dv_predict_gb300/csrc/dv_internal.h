@@ -266,9 +266,11 @@ struct PartSumArgs {
     const float *part;    // [nparts][B][d]
     float *out;           // [B][d]
     unsigned long long *stamps;
+    int stamp_ctas;       // CTAs (first ones) that record a timeline
 };
 constexpr int kPartMaxCtas = 256;  // CTAs of a one-pass kernel (partials' workspace)
-inline int part_sum_groups(int d) { return (d / 4 + 31) / 32; }
+// CTAs per batch row: 64 columns each (192 at d = 12288, so every SM works)
+inline int part_sum_groups(int d) { return (d / 4 + 15) / 16; }
 cudaError_t launch_part_sum(int dtype, const PartSumArgs &a, cudaStream_t st);
 
 // Dynamic shared memory of the attention kernel: the 16 warps' partial
